@@ -1,0 +1,46 @@
+"""Oracle for the GPTQ fold + q4tp sweep: plain, slow, CPU-only.
+
+TEST INFRASTRUCTURE, NOT PRODUCT CODE.  Only the tests, the smoke check and
+the benchmark's CPU-baseline leg may import this package.  It shares no code
+with the CUDA library (``gptq_post_weight_gb300``) and imports nothing from
+it; the library never imports it.
+
+What it follows (pages of the ``cortiq`` project, cited by page title and
+item):
+
+* ``cortiq-cli src/gptq.rs``, ``gptq_fold_operator_par``: the host fold.  Dead
+  channels (``!(H_ii > 0)``) get a zero row/column and unit diagonal; damping
+  ``lambda * max(mean(diag), 1e-12)`` is added to the whole diagonal; a failed
+  Cholesky raises lambda (0 -> 1e-4, else x10, stop once > 10); then
+  ``L = chol(H_d)``, ``L^-1``, ``H_d^-1 = L^-T L^-1``, ``M = chol(H_d^-1)``,
+  ``U = M^T`` -- computed here in f64 and returned as f32 like the page does.
+* ``cortiq-cli src/gptq.rs``, ``gptq_quantize_q4tp``: the host q4tp sweep in f32
+  (rung rule, ties-even rounding into [-8, 7], ``e = (w - q s) / U_jj`` and the
+  full-row update ``w[j+1..] -= e * U[j, j+1..]`` right after each column).
+* ``cortiq-engine src/gpu_wgpu/gptq_dev.rs``, ``build_a``: the equilibrated,
+  reversed, damped matrix (only to check the library's builder step).
+
+Readings of points the pages leave open are stated where they are used
+(``ladder`` for the missing converter ladder, ``nominal_rung`` for the f32
+log2).
+
+Every function is pinned by ``tests/test_oracle_*.py`` (closed forms,
+hand-computed cases, invariants, brute force); none is "parity unpinned".
+"""
+from .fold import (  # noqa: F401
+    NotSPD,
+    fold,
+    unpack_upper,
+    equilibrated_reversed,
+    fold_damping,
+)
+from .q4tp import (  # noqa: F401
+    ladder,
+    nominal_rung,
+    group_q4tp,
+    sweep_q4tp,
+    sweep_q4tp_f64,
+    dequant_q4tp,
+    output_error,
+    nibbles_to_codes,
+)
