@@ -1,0 +1,362 @@
+"""Benchmark: seconds per GPTQ group (fold + q4tp sweep) at n = 17408.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step = one full pass of the hot path on one synthetic Hessian group
+already resident in HBM: fold (builder, Cholesky, inverse, U), dead-column
+zeroing, ladder, q4tp sweep, through the C ABI (gptq_quantize_group).  With
+N > 1 (torchrun) every rank folds and quantizes its own group (independent
+problems, no collective on the data path): weak scaling.
+
+``--impl reference`` times the CPU oracle (the plain f64/f32 restatement of
+the pages) on the host cores, on a bounded sample of the same workload
+scaled to seconds per group.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "s per GPTQ group (fold+q4tp) at n=17408"
+UNIT = "s/group"
+
+# Peaks for the roofline denominators when the driver's measured file is absent.
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# Nominal dense tensor ratios (TF32 : BF16 = 1.1 : 2.25 PFLOP/s).
+TF32_PER_BF16 = 1.1 / 2.25
+# FP32 FMA pipe: 152 SMs x 128 lanes x 2 flop x 2.07 GHz.
+F32_SIMT_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK), "fallback"
+
+
+def workload_desc(cfg):
+    return (f"{cfg.name}: one Hessian group, n={cfg.n} channels, W [{cfg.rows}, {cfg.n}] f32 "
+            f"N(0, {cfg.w_std}^2); H = X X^T / T, X [{cfg.n}, {cfg.T}] N(0,1) with lognormal(0, {cfg.sigma}) "
+            f"channel scales, {cfg.n_outlier} outlier channels x100, {cfg.n_dead} dead; "
+            f"lambda={cfg.lam}, group 32, q4tp")
+
+
+def fold_gemm_flops(n, NB=128):
+    """Useful flops of the fold's update GEMM launches (SYRK lower tiles +
+    inverse rectangle) over one fold, on the padded size."""
+    N = (n + NB - 1) // NB * NB
+    tot = 0
+    for k in range(0, N, NB):
+        s0 = k + NB
+        m = N - s0
+        if m <= 0:
+            continue
+        tot += 2 * NB * (m * (m + 1) // 2) + 2 * NB * s0 * m
+    return tot
+
+
+def sweep_gemm_flops(rows, n, SB=128):
+    tot = 0
+    for b0 in range(0, n, SB):
+        b1 = min(b0 + SB, n)
+        if b1 < n:
+            tot += 2 * (b1 - b0) * rows * (n - b1)
+    return tot
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def cpu_baseline_sample(cfg, n_fold=None, rows_sweep=8):
+    """Oracle on a bounded sample, scaled to seconds per full group:
+    the fold on the leading n_fold x n_fold block of the group's H (cost
+    scaled by (n / n_fold)^3) and the q4tp sweep of `rows_sweep` rows at full
+    n against that block's operator padded with the identity (cost scaled by
+    rows / rows_sweep)."""
+    import numpy as np
+    import torch
+
+    import oracle
+    import synth
+
+    n_fold = n_fold or max(256, (cfg.n // 4) // 32 * 32)
+    sub = synth.Config(cfg.name + "_sample", n_fold, rows_sweep, max(1, cfg.T * n_fold // cfg.n), cfg.w_std,
+                       cfg.sigma, max(1, cfg.n_outlier * n_fold // cfg.n), max(1, cfg.n_dead * n_fold // cfg.n),
+                       cfg.lam, cfg.seed)
+    hp = synth.make_h_packed(sub, "cpu").numpy()
+    w = synth.make_w(synth.Config(cfg.name, cfg.n, rows_sweep, cfg.T, cfg.w_std, cfg.sigma, cfg.n_outlier,
+                                  cfg.n_dead, cfg.lam, cfg.seed), "cpu").numpy()
+    t0 = time.perf_counter()
+    u, d, dead, lam = oracle.fold(hp, n_fold, cfg.lam)
+    t_fold = time.perf_counter() - t0
+    # Sweep at full width: the sample operator on the leading block, identity
+    # elsewhere (the sweep's cost does not depend on U's values).
+    big = np.eye(cfg.n, dtype=np.float32)
+    big[:n_fold, :n_fold] = u.astype(np.float32)
+    hw = np.ones(cfg.n, dtype=np.float32)
+    tab, lost = oracle.ladder(w)
+    t0 = time.perf_counter()
+    oracle.sweep_q4tp(w, big, hw, tab, lost)
+    t_sweep = time.perf_counter() - t0
+    est = t_fold * (cfg.n / n_fold) ** 3 + t_sweep * (cfg.rows / rows_sweep)
+    sample = (f"oracle fold at n={n_fold} ({t_fold:.2f} s, x(n/{n_fold})^3) + oracle q4tp sweep of "
+              f"{rows_sweep} rows at n={cfg.n} ({t_sweep:.2f} s, x{cfg.rows}/{rows_sweep})")
+    return est, sample, t_fold + t_sweep
+
+
+def run_reference(args, cfg, rank):
+    if rank != 0:
+        return
+    cores = os.cpu_count()
+    vals = []
+    sample = ""
+    for i in range(args.warmup + args.steps):
+        est, sample, spent = cpu_baseline_sample(cfg, n_fold=args.ref_n, rows_sweep=args.ref_rows)
+        if i >= args.warmup:
+            vals.append(est)
+    v = statistics.median(vals)
+    line = {"metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": v * 1e3, "higher_is_better": False, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": workload_desc(cfg)},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="n17408")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--ref-n", type=int, default=None)
+    ap.add_argument("--ref-rows", type=int, default=8)
+    args = ap.parse_args()
+
+    import synth
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    cfg = synth.config(args.config, seed=rank)
+    if args.impl == "reference":
+        run_reference(args, cfg, rank)
+        return
+
+    import numpy as np  # noqa: F401
+    import torch
+
+    from gptq_post_weight_gb300 import _lib
+
+    if not os.path.exists(_lib.LIB_PATH):
+        raise SystemExit("libgptqfold.so is not built (python -m gptq_post_weight_gb300.build)")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+    lib = _lib.load()
+
+    hp, w = synth.make_problem(cfg, dev)
+    n, rows = cfg.n, cfg.rows
+    gpr = n // 32
+    ws = _lib.workspace(lib.gptq_group_workspace_bytes(rows, n), dev)
+    outs = (torch.empty(rows * n // 2, dtype=torch.uint8, device=dev),
+            torch.empty(rows * gpr, dtype=torch.uint8, device=dev),
+            torch.empty(rows * gpr, dtype=torch.float32, device=dev))
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        return _lib.quantize_group(hp, n, w, cfg.lam, ws=ws, want_u=False, stream=stream, out=outs)
+
+    for _ in range(max(args.warmup, 0)):
+        res = step()
+    torch.cuda.synchronize()
+    lam_used = res["lam"]
+
+    def barrier():
+        if pg is not None:
+            pg.barrier()
+        torch.cuda.synchronize()
+
+    sampler = ClockSampler(local)
+    barrier()
+    sampler.start()
+    time.sleep(0.3)
+    launches0 = _lib.launch_count()
+    _lib.profile_start(200000)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    prof = _lib.profile_stop()
+    launches = _lib.launch_count() - launches0
+    clocks = sampler.stop()
+    t_dev = e0.elapsed_time(e1) / 1e3  # s for K steps on this rank
+    if pg is not None:
+        tt = torch.tensor([t_dev], device=dev, dtype=torch.float64)
+        pg.all_reduce(tt, op=pg.ReduceOp.MAX)
+        t_dev = float(tt.item())
+    value = t_dev / (args.steps * world)
+
+    # End to end through the public call with host buffers: H2D of the
+    # group's inputs from pinned memory, the call, D2H of its outputs.
+    e2e = None
+    if not args.no_e2e:
+        hp_h = hp.cpu().pin_memory()
+        w_h = w.cpu().pin_memory()
+        outs_h = tuple(torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs)
+        hp_d = torch.empty_like(hp)
+        w_d = torch.empty_like(w)
+
+        def e2e_step():
+            hp_d.copy_(hp_h, non_blocking=True)
+            w_d.copy_(w_h, non_blocking=True)
+            _lib.quantize_group(hp_d, n, w_d, cfg.lam, ws=ws, want_u=False, stream=stream, out=outs)
+            for o_h, o in zip(outs_h, outs):
+                o_h.copy_(o, non_blocking=True)
+
+        e2e_step()
+        barrier()
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            e2e_step()
+        torch.cuda.synchronize()
+        t_e2e = time.perf_counter() - t0
+        if pg is not None:
+            tt = torch.tensor([t_e2e], device=dev, dtype=torch.float64)
+            pg.all_reduce(tt, op=pg.ReduceOp.MAX)
+            t_e2e = float(tt.item())
+        e2e = {"value": t_e2e / (args.steps * world), "unit": UNIT,
+               "h2d_bytes_per_step": hp.numel() * 4 + w.numel() * 4,
+               "d2h_bytes_per_step": sum(o.numel() * o.element_size() for o in outs)}
+
+    # Roofline of the dominant kernel kind, from the live event timings.
+    pk, src = peaks()
+    kinds = {k: v for k, v in prof.items() if not k.startswith("_")}
+    top = max(kinds, key=lambda k: kinds[k][0])
+    ms_top, cnt_top = kinds[top]
+    flops = {"fold_gemm": fold_gemm_flops(n) * args.steps,
+             "sweep_gemm": sweep_gemm_flops(rows, n) * args.steps}
+    roof = None
+    if top in flops and cnt_top > 0:
+        per_launch = flops[top] / cnt_top
+        achieved = per_launch / (ms_top / cnt_top / 1e3) / 1e12
+        peak = F32_SIMT_TFLOPS
+        roof = {"bound": "alu", "kernel": top, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": None,
+                "peak_source": "f32 FMA pipe: 152 SMs x 128 lanes x 2 flop x 2.07 GHz (recipe unit counts)",
+                "flop_per_launch": per_launch}
+    fold_flops = 2 * n ** 3 / 3
+    per_kind = {k: {"ms_per_step": v[0] / args.steps, "launches_per_step": v[1] / args.steps}
+                for k, v in kinds.items() if v[1] > 0}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        est, sample, spent = cpu_baseline_sample(cfg, n_fold=args.ref_n, rows_sweep=args.ref_rows)
+        cpu = {"value": est, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle", "sample": sample}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": t_dev / args.steps * 1e3, "higher_is_better": False,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": workload_desc(cfg), "n": n, "rows": rows, "lambda_used": lam_used,
+                       "l2": "inputs larger than L2 (H_packed %.0f MB, W %.0f MB, U %.0f MB); no flush"
+                             % (hp.numel() * 4 / 1e6, w.numel() * 4 / 1e6, n * n * 4 / 1e6),
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "roofline": roof,
+            "fold_tflops_algorithmic": fold_flops / (per_kind.get("fold_gemm", {}).get("ms_per_step", 0) / 1e3
+                                                     + sum(per_kind.get(k, {}).get("ms_per_step", 0) / 1e3
+                                                           for k in ("build", "potrf", "trsm_panel", "trsm_inv", "diag"))
+                                                     ) / 1e12 if "fold_gemm" in per_kind else None,
+            "per_kernel": per_kind,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": launches,
+            "clocks": clocks,
+            "peaks": {"source": src, "hbm_gbs": pk.get("hbm_gbs"), "bf16_tflops": pk.get("bf16_tflops"),
+                      "tf32_tflops_equiv": pk.get("bf16_tflops", 0) * TF32_PER_BF16},
+        }
+        print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.barrier()
+        pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

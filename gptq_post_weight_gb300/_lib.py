@@ -1,0 +1,229 @@
+"""ctypes binding of libgptqfold.so (include/gptq_fold.h).
+
+Argument marshalling only: every step runs in the library's CUDA kernels.
+The wrappers take torch CUDA tensors (device memory and the current stream
+come from PyTorch) and raise ``GptqError`` on a non-zero status.  There is
+no fallback: without the built library every call fails loudly.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libgptqfold.so")
+
+STATUS = {0: "GPTQ_OK", 1: "GPTQ_ERR_ARG", 2: "GPTQ_ERR_SHAPE", 3: "GPTQ_ERR_NOMEM",
+          4: "GPTQ_ERR_NOT_SPD", 5: "GPTQ_ERR_CUDA", 6: "GPTQ_ERR_TIMEOUT"}
+
+# name -> (restype, argtypes); the full exported surface of the header.
+_P, _I, _D, _S = ctypes.c_void_p, ctypes.c_int, ctypes.c_double, ctypes.c_size_t
+SIGNATURES = {
+    "gptq_status_string": (ctypes.c_char_p, [_I]),
+    "gptq_fold_workspace_bytes": (_S, [_I]),
+    "gptq_fold": (_I, [_P, _I, _D, _P, _P, _P, _P, _P, _S, _P]),
+    "gptq_ladder": (_I, [_P, _I, _I, _P, _P, _P]),
+    "gptq_sweep_workspace_bytes": (_S, [_I, _I]),
+    "gptq_q4tp_sweep": (_I, [_P, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _S, _P]),
+    "gptq_q4tp_group": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "gptq_group_workspace_bytes": (_S, [_I, _I]),
+    "gptq_quantize_group": (_I, [_P, _I, _D, _P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _S, _P]),
+    "gptq_build_equilibrated": (_I, [_P, _I, _D, _P, _P, _P, _S, _P]),
+    "gptq_launch_count": (ctypes.c_longlong, []),
+    "gptq_kernel_kinds": (_I, []),
+    "gptq_kernel_kind_name": (ctypes.c_char_p, [_I]),
+    "gptq_profile_start": (_I, [_I]),
+    "gptq_profile_stop": (_I, [_P, _P, _I]),
+}
+
+
+class GptqError(RuntimeError):
+    def __init__(self, fn, code):
+        self.code = code
+        super().__init__(f"{fn}: {STATUS.get(code, code)}")
+
+
+_lib = None
+
+
+def load(path: str = LIB_PATH):
+    """Load the library (built by ``gptq_post_weight_gb300.build``)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with `python -m gptq_post_weight_gb300.build`")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        f = getattr(lib, name)
+        f.restype = res
+        f.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(torch, stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(fn, code):
+    if code != 0:
+        raise GptqError(fn, code)
+
+
+def _cuda_f32(t, name):
+    import torch
+
+    if not (t.is_cuda and t.dtype == torch.float32 and t.is_contiguous()):
+        raise ValueError(f"{name} must be a contiguous CUDA float32 tensor")
+
+
+def workspace(nbytes: int, device):
+    import torch
+
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+def fold(h_packed, n: int, lam: float = 0.01, ws=None, stream=None, want_d=True):
+    """U [n, n], D [n], hdiag [n], lambda_used.  Raises GptqError(NOT_SPD)."""
+    import torch
+
+    lib = load()
+    _cuda_f32(h_packed, "h_packed")
+    dev = h_packed.device
+    u = torch.empty(n, n, dtype=torch.float32, device=dev)
+    d = torch.empty(n, dtype=torch.float32, device=dev) if want_d else None
+    hd = torch.empty(n, dtype=torch.float32, device=dev)
+    need = lib.gptq_fold_workspace_bytes(n)
+    if ws is None:
+        ws = workspace(need, dev)
+    lam_used = ctypes.c_double(0.0)
+    code = lib.gptq_fold(_ptr(h_packed), n, float(lam), _ptr(u), _ptr(d), _ptr(hd),
+                         ctypes.byref(lam_used), _ptr(ws), ws.numel(), _stream(torch, stream))
+    _check("gptq_fold", code)
+    return u, d, hd, lam_used.value
+
+
+def build_equilibrated(h_packed, n: int, lam: float = 0.01):
+    import torch
+
+    lib = load()
+    dev = h_packed.device
+    a = torch.zeros(n, n, dtype=torch.float32, device=dev)
+    d = torch.empty(n, dtype=torch.float32, device=dev)
+    ws = workspace(lib.gptq_fold_workspace_bytes(n), dev)
+    code = lib.gptq_build_equilibrated(_ptr(h_packed), n, float(lam), _ptr(a), _ptr(d), _ptr(ws),
+                                       ws.numel(), _stream(torch))
+    _check("gptq_build_equilibrated", code)
+    return a, d
+
+
+def ladder(w):
+    import torch
+
+    lib = load()
+    _cuda_f32(w, "w")
+    rows, n = w.shape
+    tab = torch.empty(rows, 32, dtype=torch.float32, device=w.device)
+    lost = torch.empty(rows, 2, dtype=torch.float32, device=w.device)
+    _check("gptq_ladder", lib.gptq_ladder(_ptr(w), rows, n, _ptr(tab), _ptr(lost), _stream(torch)))
+    return tab, lost
+
+
+def _outs(torch, rows, n, dev):
+    gpr = n // 32
+    nib = torch.empty(rows * n // 2, dtype=torch.uint8, device=dev)
+    rungs = torch.empty(rows * gpr, dtype=torch.uint8, device=dev)
+    scales = torch.empty(rows * gpr, dtype=torch.float32, device=dev)
+    return nib, rungs, scales
+
+
+def q4tp_sweep(w, u, hw, tab, lost, ws=None, out=None, stream=None):
+    """Sweep W (consumed in place).  Returns (nibbles, rungs, scales)."""
+    import torch
+
+    lib = load()
+    for t, nm in ((w, "w"), (u, "u"), (hw, "hw"), (tab, "tab"), (lost, "lost")):
+        _cuda_f32(t, nm)
+    rows, n = w.shape
+    nib, rungs, scales = out if out is not None else _outs(torch, rows, n, w.device)
+    if ws is None:
+        ws = workspace(lib.gptq_sweep_workspace_bytes(rows, n), w.device)
+    code = lib.gptq_q4tp_sweep(_ptr(w), rows, n, _ptr(u), _ptr(hw), _ptr(tab), _ptr(lost),
+                               _ptr(nib), _ptr(rungs), _ptr(scales), _ptr(ws), ws.numel(),
+                               _stream(torch, stream))
+    _check("gptq_q4tp_sweep", code)
+    return nib, rungs, scales
+
+
+def q4tp_group(tile, ublk, hw, tab, lost):
+    """The group rule on given tiles: (nibbles [rows,16], rungs, scales, E)."""
+    import torch
+
+    lib = load()
+    rows = tile.shape[0]
+    dev = tile.device
+    nib = torch.empty(rows, 16, dtype=torch.uint8, device=dev)
+    rungs = torch.empty(rows, dtype=torch.uint8, device=dev)
+    scales = torch.empty(rows, dtype=torch.float32, device=dev)
+    e = torch.empty(rows, 32, dtype=torch.float32, device=dev)
+    code = lib.gptq_q4tp_group(_ptr(tile), rows, _ptr(ublk), _ptr(hw), _ptr(tab), _ptr(lost),
+                               _ptr(nib), _ptr(rungs), _ptr(scales), _ptr(e), _stream(torch))
+    _check("gptq_q4tp_group", code)
+    return nib, rungs, scales, e
+
+
+def quantize_group(h_packed, n, w, lam=0.01, ws=None, want_u=True, stream=None, out=None):
+    """Fold + ladder + sweep.  Returns dict(nibbles, rungs, scales, tab, lost,
+    u, d, hdiag, lam)."""
+    import torch
+
+    lib = load()
+    _cuda_f32(h_packed, "h_packed")
+    _cuda_f32(w, "w")
+    rows = w.shape[0]
+    dev = w.device
+    nib, rungs, scales = out if out is not None else _outs(torch, rows, n, dev)
+    tab = torch.empty(rows, 32, dtype=torch.float32, device=dev)
+    lost = torch.empty(rows, 2, dtype=torch.float32, device=dev)
+    u = torch.empty(n, n, dtype=torch.float32, device=dev) if want_u else None
+    d = torch.empty(n, dtype=torch.float32, device=dev)
+    hd = torch.empty(n, dtype=torch.float32, device=dev)
+    if ws is None:
+        ws = workspace(lib.gptq_group_workspace_bytes(rows, n), dev)
+    lam_used = ctypes.c_double(0.0)
+    code = lib.gptq_quantize_group(_ptr(h_packed), n, float(lam), _ptr(w), rows, _ptr(nib),
+                                   _ptr(rungs), _ptr(scales), _ptr(tab), _ptr(lost), _ptr(u),
+                                   _ptr(d), _ptr(hd), ctypes.byref(lam_used), _ptr(ws), ws.numel(),
+                                   _stream(torch, stream))
+    _check("gptq_quantize_group", code)
+    return dict(nibbles=nib, rungs=rungs, scales=scales, tab=tab, lost=lost, u=u, d=d, hdiag=hd,
+                lam=lam_used.value)
+
+
+def launch_count() -> int:
+    return int(load().gptq_launch_count())
+
+
+def profile_start(max_launches: int = 100000):
+    _check("gptq_profile_start", load().gptq_profile_start(int(max_launches)))
+
+
+def profile_stop():
+    """{kind name: (total ms, launches)} for the launches since profile_start."""
+    lib = load()
+    nk = lib.gptq_kernel_kinds()
+    ms = (ctypes.c_double * nk)()
+    cnt = (ctypes.c_longlong * nk)()
+    r = lib.gptq_profile_stop(ms, cnt, nk)
+    if r == -1:
+        raise GptqError("gptq_profile_stop", 5)
+    out = {lib.gptq_kernel_kind_name(k).decode(): (ms[k], cnt[k]) for k in range(nk)}
+    if r == -2:
+        out["_truncated"] = (0.0, 1)
+    return out

@@ -1,0 +1,146 @@
+// C ABI entry points (include/gptq_fold.h): argument checks, workspace
+// carving and the chaining of fold -> ladder -> sweep.  No device memory is
+// allocated here; every buffer is the caller's.
+#include "common.cuh"
+
+#include <math.h>
+
+namespace gq {
+size_t fold_ws_bytes(int n);
+size_t sweep_ws_bytes(int rows, int n);
+gptq_status fold_run(const float* hp, int n, double lambda, float* U, float* D, float* hdiag,
+                     double* lambda_used, void* ws, size_t ws_bytes, cudaStream_t s);
+gptq_status build_only(const float* hp, int n, double lambda, float* A, float* D, void* ws,
+                       size_t ws_bytes, cudaStream_t s);
+gptq_status ladder_run(const float* W, int rows, int n, float* tab, float* lost, cudaStream_t s);
+gptq_status group_run(const float* tile, int rows, const float* ublk, const float* hw,
+                      const float* tab, const float* lost, uint8_t* nib, uint8_t* rungs,
+                      float* scales, float* E, cudaStream_t s);
+gptq_status copy_dead_zeroed(const float* W, int rows, int n, const float* hdiag, float* out,
+                             cudaStream_t s);
+gptq_status sweep_run(float* W, int rows, int n, const float* U, const float* hw, const float* tab,
+                      const float* lost, uint8_t* nib, uint8_t* rungs, float* scales, void* ws,
+                      size_t ws_bytes, cudaStream_t s);
+}  // namespace gq
+
+using namespace gq;
+
+namespace {
+bool bad_n(int n) { return n <= 0 || n > GPTQ_MAX_N; }
+bool bad_rows(int rows) { return rows <= 0 || rows > GPTQ_MAX_ROWS; }
+bool ptr_ok(const void* p) { return p != nullptr && aligned16(p); }
+bool opt_ok(const void* p) { return p == nullptr || aligned16(p); }
+cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+}  // namespace
+
+extern "C" {
+
+const char* gptq_status_string(int status) {
+  switch (status) {
+    case GPTQ_OK: return "ok";
+    case GPTQ_ERR_ARG: return "invalid argument (null/misaligned pointer or non-finite lambda)";
+    case GPTQ_ERR_SHAPE: return "invalid shape";
+    case GPTQ_ERR_NOMEM: return "workspace too small";
+    case GPTQ_ERR_NOT_SPD: return "not positive definite with damping up to lambda = 10";
+    case GPTQ_ERR_CUDA: return "CUDA error";
+    case GPTQ_ERR_TIMEOUT: return "device wait timed out";
+    default: return "unknown status";
+  }
+}
+
+size_t gptq_fold_workspace_bytes(int n) { return bad_n(n) ? 0 : fold_ws_bytes(n); }
+
+size_t gptq_sweep_workspace_bytes(int rows, int n) {
+  if (bad_n(n) || bad_rows(rows)) return 0;
+  return sweep_ws_bytes(rows, n);
+}
+
+size_t gptq_group_workspace_bytes(int rows, int n) {
+  if (bad_n(n) || bad_rows(rows)) return 0;
+  const size_t f = fold_ws_bytes(n), sw = sweep_ws_bytes(rows, n);
+  const size_t own = round_up((size_t)n * n * 4, 256) + 3 * round_up((size_t)n * 4, 256) +
+                     round_up((size_t)rows * n * 4, 256) + round_up((size_t)rows * 32 * 4, 256) +
+                     round_up((size_t)rows * 2 * 4, 256) + 1024;
+  return own + (f > sw ? f : sw);
+}
+
+gptq_status gptq_fold(const float* H_packed, int n, double lambda, float* U, float* D,
+                      float* hdiag, double* lambda_used, void* ws, size_t ws_bytes,
+                      void* stream) {
+  if (bad_n(n)) return GPTQ_ERR_SHAPE;
+  if (!ptr_ok(H_packed) || !ptr_ok(U) || !opt_ok(D) || !opt_ok(hdiag) || ws == nullptr)
+    return GPTQ_ERR_ARG;
+  if (!isfinite(lambda)) return GPTQ_ERR_ARG;
+  if (ws_bytes < fold_ws_bytes(n)) return GPTQ_ERR_NOMEM;
+  return fold_run(H_packed, n, lambda, U, D, hdiag, lambda_used, ws, ws_bytes, as_stream(stream));
+}
+
+gptq_status gptq_build_equilibrated(const float* H_packed, int n, double lambda, float* A,
+                                    float* D, void* ws, size_t ws_bytes, void* stream) {
+  if (bad_n(n)) return GPTQ_ERR_SHAPE;
+  if (!ptr_ok(H_packed) || !ptr_ok(A) || !opt_ok(D) || ws == nullptr) return GPTQ_ERR_ARG;
+  if (!isfinite(lambda)) return GPTQ_ERR_ARG;
+  if (ws_bytes < fold_ws_bytes(n)) return GPTQ_ERR_NOMEM;
+  return build_only(H_packed, n, lambda, A, D, ws, ws_bytes, as_stream(stream));
+}
+
+gptq_status gptq_ladder(const float* W, int rows, int n, float* tab, float* lost, void* stream) {
+  if (bad_n(n) || bad_rows(rows) || n % GPTQ_GROUP != 0) return GPTQ_ERR_SHAPE;
+  if (!ptr_ok(W) || !ptr_ok(tab) || !ptr_ok(lost)) return GPTQ_ERR_ARG;
+  return ladder_run(W, rows, n, tab, lost, as_stream(stream));
+}
+
+gptq_status gptq_q4tp_group(const float* tile, int rows, const float* ublk, const float* hw,
+                            const float* tab, const float* lost, uint8_t* nibbles,
+                            uint8_t* rungs, float* scales, float* E, void* stream) {
+  if (bad_rows(rows)) return GPTQ_ERR_SHAPE;
+  if (!ptr_ok(tile) || !ptr_ok(ublk) || !ptr_ok(hw) || !ptr_ok(tab) || !ptr_ok(lost) ||
+      !ptr_ok(nibbles) || rungs == nullptr || !ptr_ok(scales) || !ptr_ok(E))
+    return GPTQ_ERR_ARG;
+  return group_run(tile, rows, ublk, hw, tab, lost, nibbles, rungs, scales, E, as_stream(stream));
+}
+
+gptq_status gptq_q4tp_sweep(float* W, int rows, int n, const float* U, const float* hw,
+                            const float* tab, const float* lost, uint8_t* nibbles,
+                            uint8_t* rungs, float* scales, void* ws, size_t ws_bytes,
+                            void* stream) {
+  if (bad_n(n) || bad_rows(rows) || n % GPTQ_GROUP != 0) return GPTQ_ERR_SHAPE;
+  if (!ptr_ok(W) || !ptr_ok(U) || !ptr_ok(hw) || !ptr_ok(tab) || !ptr_ok(lost) ||
+      !ptr_ok(nibbles) || rungs == nullptr || !ptr_ok(scales) || ws == nullptr)
+    return GPTQ_ERR_ARG;
+  if (ws_bytes < sweep_ws_bytes(rows, n)) return GPTQ_ERR_NOMEM;
+  return sweep_run(W, rows, n, U, hw, tab, lost, nibbles, rungs, scales, ws, ws_bytes,
+                   as_stream(stream));
+}
+
+gptq_status gptq_quantize_group(const float* H_packed, int n, double lambda, const float* W,
+                                int rows, uint8_t* nibbles, uint8_t* rungs, float* scales,
+                                float* tab, float* lost, float* U, float* D, float* hdiag,
+                                double* lambda_used, void* ws, size_t ws_bytes, void* stream) {
+  if (bad_n(n) || bad_rows(rows) || n % GPTQ_GROUP != 0) return GPTQ_ERR_SHAPE;
+  if (!ptr_ok(H_packed) || !ptr_ok(W) || !ptr_ok(nibbles) || rungs == nullptr ||
+      !ptr_ok(scales) || !opt_ok(tab) || !opt_ok(lost) || !opt_ok(U) || !opt_ok(D) ||
+      !opt_ok(hdiag) || ws == nullptr)
+    return GPTQ_ERR_ARG;
+  if (!isfinite(lambda)) return GPTQ_ERR_ARG;
+  if (ws_bytes < gptq_group_workspace_bytes(rows, n)) return GPTQ_ERR_NOMEM;
+  cudaStream_t s = as_stream(stream);
+  Carve c(ws, ws_bytes);
+  float* u = U ? U : c.take<float>((size_t)n * n);
+  float* d = D ? D : c.take<float>((size_t)n);
+  float* hd = hdiag ? hdiag : c.take<float>((size_t)n);
+  float* wz = c.take<float>((size_t)rows * n);
+  float* tb = tab ? tab : c.take<float>((size_t)rows * 32);
+  float* ls = lost ? lost : c.take<float>((size_t)rows * 2);
+  c.take<float>((size_t)n);  // keeps the layout independent of which outputs are given
+  if (!c.ok) return GPTQ_ERR_NOMEM;
+  const size_t off = round_up(c.off, 256);
+  void* rest = static_cast<char*>(ws) + off;
+  const size_t rest_bytes = ws_bytes - off;
+  GQ_TRY(fold_run(H_packed, n, lambda, u, d, hd, lambda_used, rest, rest_bytes, s));
+  GQ_TRY(copy_dead_zeroed(W, rows, n, hd, wz, s));
+  GQ_TRY(ladder_run(wz, rows, n, tb, ls, s));
+  return sweep_run(wz, rows, n, u, hd, tb, ls, nibbles, rungs, scales, rest, rest_bytes, s);
+}
+
+}  // extern "C"

@@ -1,0 +1,346 @@
+// The q4tp sweep on the device (cortiq-engine src/gpu_wgpu/gptq_dev.rs,
+// module doc step 5 and WGSL q4tp_group / q4tp_trail; the same rule as the
+// host page's gptq_quantize_q4tp).
+//
+// Lazy blocks of SB = 128 columns (4 groups): one kernel runs the four
+// groups of a block for 64 rows per CTA out of shared memory (rung choice,
+// rounding, in-group feedback, then the group's residuals into the rest of
+// the block), then one GEMM applies the block's residuals to every later
+// column: W[:, b1:] -= E_blk U[b0:b1, b1:].  With SB = 32 this is the fold
+// page's per-group q4tp_trail; a wider block is the same mathematics with
+// the residual sums taken in a different order.
+//
+// The per-group rule uses one rounding per operation (no contraction) so it
+// reproduces the pages' f32 arithmetic bit for bit.
+#include "common.cuh"
+
+#include <cuda_fp16.h>
+#include <math.h>
+
+namespace gq {
+namespace {
+
+constexpr int ROWS_PER_CTA = 64;
+
+// Rung of one (row, group) tile ([fold page] q4tp_group; [host page]
+// gptq_quantize_q4tp): nominal = clamp(round_half_away((log2(amax/7) - lo)
+// / step), 0, 31) (0 if amax == 0 or step <= 0; log2 = the f64 value rounded
+// to f32), then the best of nominal-2..min(nominal+1, 31) by
+// sum_t hw_t (w_t - q_t s)^2 with q_t = clamp(rne(w_t * (1/s)), -8, 7),
+// strict '<', rungs with s <= 0 skipped.
+__device__ __forceinline__ int q4tp_pick(const float (&w)[GROUP], const float* hw,
+                                         const float* tabrow, float lo, float st) {
+  float amax = 0.f;
+#pragma unroll
+  for (int t = 0; t < GROUP; ++t) amax = fmaxf(amax, fabsf(w[t]));
+  int nominal = 0;
+  if (amax > 0.f && st > 0.f) {
+    const float x = __fdiv_rn(amax, 7.0f);
+    const float l2 = (float)log2((double)x);
+    const float tt = __fdiv_rn(__fsub_rn(l2, lo), st);
+    const float r = fminf(fmaxf(roundf(tt), 0.f), 31.f);
+    nominal = (int)r;
+  }
+  int best_c = nominal;
+  if (amax > 0.f) {
+    float best_e = INFINITY;
+    const int lo_c = nominal >= 2 ? nominal - 2 : 0;
+    const int hi_c = nominal + 1 < 31 ? nominal + 1 : 31;
+    for (int cand = lo_c; cand <= hi_c; ++cand) {
+      const float sc = tabrow[cand];
+      if (!(sc > 0.f)) continue;
+      const float iv = __fdiv_rn(1.0f, sc);
+      float err = 0.f;
+#pragma unroll
+      for (int t = 0; t < GROUP; ++t) {
+        const float q = fminf(fmaxf(rintf(__fmul_rn(w[t], iv)), -8.f), 7.f);
+        const float d = __fsub_rn(w[t], __fmul_rn(q, sc));
+        err = __fadd_rn(err, __fmul_rn(__fmul_rn(hw[t], d), d));
+      }
+      if (err < best_e) {
+        best_e = err;
+        best_c = cand;
+      }
+    }
+  }
+  return best_c;
+}
+
+// Codes, residuals and in-group feedback for one tile at scale s:
+// q_j = clamp(rne(w_j / s), -8, 7) (0 if s <= 0), nibble q_j + 8 (byte j/2,
+// low nibble for even j), e_j = (w_j - q_j s) / U_jj (0 if U_jj <= 0), then
+// w_t -= e_j U_jt for t > j.
+__device__ __forceinline__ void q4tp_round(float (&w)[GROUP], float s, const float* U, int ldu,
+                                           uint32_t (&words)[4], float (&e)[GROUP]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) words[i] = 0u;
+#pragma unroll
+  for (int j = 0; j < GROUP; ++j) {
+    float q = 0.f;
+    if (s > 0.f) q = fminf(fmaxf(rintf(__fdiv_rn(w[j], s)), -8.f), 7.f);
+    const uint32_t nb = (uint32_t)((int)q + 8) & 15u;
+    words[j / 8] |= nb << (4 * (j % 8));
+    const float dj = U[j * ldu + j];
+    float ej = 0.f;
+    if (dj > 0.f) ej = __fdiv_rn(__fsub_rn(w[j], __fmul_rn(q, s)), dj);
+    e[j] = ej;
+    if (ej != 0.f) {
+#pragma unroll
+      for (int t = j + 1; t < GROUP; ++t) w[t] = __fsub_rn(w[t], __fmul_rn(ej, U[j * ldu + t]));
+    }
+  }
+}
+
+// Per-row ladder ([host page] gptq_quantize_q4tp_dev's tab / lost; the
+// converter itself is not on the pages -- reading in the header).
+__global__ void __launch_bounds__(128) k_ladder(const float* __restrict__ W, int n,
+                                                float* __restrict__ tab, float* __restrict__ lost) {
+  const int r = blockIdx.x;
+  const float* wr = W + (long long)r * n;
+  const int gpr = n / GROUP;
+  float xmin = INFINITY, xmax = 0.f;
+  int cnt = 0;
+  for (int g = threadIdx.x; g < gpr; g += blockDim.x) {
+    const float4* p = reinterpret_cast<const float4*>(wr + g * GROUP);
+    float a = 0.f;
+#pragma unroll
+    for (int q = 0; q < GROUP / 4; ++q) {
+      float4 v = p[q];
+      a = fmaxf(a, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+    }
+    if (a > 0.f) {
+      const float x = __fdiv_rn(a, 7.0f);
+      xmin = fminf(xmin, x);
+      xmax = fmaxf(xmax, x);
+      ++cnt;
+    }
+  }
+  for (int o = 16; o > 0; o >>= 1) {
+    xmin = fminf(xmin, __shfl_xor_sync(0xffffffffu, xmin, o));
+    xmax = fmaxf(xmax, __shfl_xor_sync(0xffffffffu, xmax, o));
+    cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+  }
+  __shared__ float smin[4], smax[4];
+  __shared__ int scnt[4];
+  __shared__ float slo, sst;
+  const int wid = threadIdx.x / 32, lane = threadIdx.x % 32;
+  if (lane == 0) {
+    smin[wid] = xmin;
+    smax[wid] = xmax;
+    scnt[wid] = cnt;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float mn = smin[0], mx = smax[0];
+    int c = scnt[0];
+    for (int i = 1; i < 4; ++i) {
+      mn = fminf(mn, smin[i]);
+      mx = fmaxf(mx, smax[i]);
+      c += scnt[i];
+    }
+    float lo = 0.f, st = 0.f;
+    if (c > 0) {
+      lo = __half2float(__double2half(log2((double)mn)));
+      if (mx > mn) {
+        double sd = (log2((double)mx) - (double)lo) / 31.0;
+        st = __half2float(__double2half(sd > 0.0 ? sd : 0.0));
+      }
+    }
+    slo = lo;
+    sst = st;
+    lost[2 * r] = lo;
+    lost[2 * r + 1] = st;
+    scnt[0] = c;
+  }
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    const int c = threadIdx.x;
+    tab[r * 32 + c] = scnt[0] > 0 ? (float)exp2((double)slo + (double)c * (double)sst) : 0.f;
+  }
+}
+
+// The group rule on given tiles (one thread per row).
+__global__ void __launch_bounds__(128) k_group(const float* __restrict__ tile, int rows,
+                                               const float* __restrict__ ublk,
+                                               const float* __restrict__ hw,
+                                               const float* __restrict__ tab,
+                                               const float* __restrict__ lost,
+                                               uint8_t* __restrict__ nib, uint8_t* __restrict__ rungs,
+                                               float* __restrict__ scales, float* __restrict__ E) {
+  __shared__ float Us[GROUP * GROUP];
+  __shared__ float hws[GROUP];
+  for (int e = threadIdx.x; e < GROUP * GROUP; e += blockDim.x) Us[e] = ublk[e];
+  if (threadIdx.x < GROUP) hws[threadIdx.x] = hw[threadIdx.x];
+  __syncthreads();
+  const int r = blockIdx.x * blockDim.x + threadIdx.x;
+  if (r >= rows) return;
+  float w[GROUP], e[GROUP];
+#pragma unroll
+  for (int t = 0; t < GROUP; ++t) w[t] = tile[(long long)r * GROUP + t];
+  const int c = q4tp_pick(w, hws, tab + (long long)r * 32, lost[2 * r], lost[2 * r + 1]);
+  const float s = tab[(long long)r * 32 + c];
+  uint32_t words[4];
+  q4tp_round(w, s, Us, GROUP, words, e);
+  reinterpret_cast<uint4*>(nib)[r] = make_uint4(words[0], words[1], words[2], words[3]);
+  rungs[r] = (uint8_t)c;
+  scales[r] = s;
+#pragma unroll
+  for (int t = 0; t < GROUP; ++t) E[(long long)r * GROUP + t] = e[t];
+}
+
+// One lazy block [b0, b0+B) for 64 rows: the groups in order, each followed
+// by its residuals into the rest of the block; E_blk -> E (ld SB).
+__global__ void __launch_bounds__(ROWS_PER_CTA) k_sweep_block(
+    const float* __restrict__ W, int rows, int n, int b0, int B, const float* __restrict__ U,
+    const float* __restrict__ hw, const float* __restrict__ tab, const float* __restrict__ lost,
+    uint8_t* __restrict__ nib, uint8_t* __restrict__ rungs, float* __restrict__ scales,
+    float* __restrict__ E) {
+  extern __shared__ __align__(16) float sm[];
+  float* Us = sm;                       // [SB][SB]
+  float* hws = Us + SB * SB;            // [SB]
+  float* Ws = hws + SB;                 // [ROWS_PER_CTA][SB + 1]
+  constexpr int LW = SB + 1;
+  const int tid = threadIdx.x;
+  const int r0 = blockIdx.x * ROWS_PER_CTA;
+  for (int e = tid; e < B * B; e += ROWS_PER_CTA) {
+    const int i = e / B, j = e % B;
+    Us[i * SB + j] = U[(long long)(b0 + i) * n + b0 + j];
+  }
+  for (int e = tid; e < B; e += ROWS_PER_CTA) hws[e] = hw[b0 + e];
+  for (int e = tid; e < ROWS_PER_CTA * B; e += ROWS_PER_CTA) {
+    const int i = e / B, j = e % B;
+    Ws[i * LW + j] = (r0 + i < rows) ? W[(long long)(r0 + i) * n + b0 + j] : 0.f;
+  }
+  __syncthreads();
+  const int r = r0 + tid;
+  if (r >= rows) return;
+  const int gpr = n / GROUP;
+  const float lo = lost[2 * r], st = lost[2 * r + 1];
+  const float* tabrow = tab + (long long)r * 32;
+  float* wrow = Ws + tid * LW;
+  for (int g = 0; g < B / GROUP; ++g) {
+    float w[GROUP], e[GROUP];
+#pragma unroll
+    for (int t = 0; t < GROUP; ++t) w[t] = wrow[g * GROUP + t];
+    const int c = q4tp_pick(w, hws + g * GROUP, tabrow, lo, st);
+    const float s = tabrow[c];
+    uint32_t words[4];
+    q4tp_round(w, s, Us + g * GROUP * SB + g * GROUP, SB, words, e);
+    const long long tix = (long long)r * gpr + b0 / GROUP + g;
+    reinterpret_cast<uint4*>(nib)[tix] = make_uint4(words[0], words[1], words[2], words[3]);
+    rungs[tix] = (uint8_t)c;
+    scales[tix] = s;
+    float4* erow = reinterpret_cast<float4*>(E + (long long)r * SB + g * GROUP);
+#pragma unroll
+    for (int t = 0; t < GROUP / 4; ++t) erow[t] = make_float4(e[4 * t], e[4 * t + 1], e[4 * t + 2], e[4 * t + 3]);
+    for (int col = (g + 1) * GROUP; col < B; ++col) {
+      float acc = 0.f;
+#pragma unroll
+      for (int j = 0; j < GROUP; ++j) acc = fmaf(e[j], Us[(g * GROUP + j) * SB + col], acc);
+      wrow[col] -= acc;
+    }
+  }
+}
+
+// Ut[c][t] = U[b0 + t][b1 + c]: the block row of U, K-major for the GEMM.
+__global__ void k_prep_ut(const float* __restrict__ U, int n, int b0, int b1,
+                          float* __restrict__ Ut) {
+  __shared__ float tile[32][33];
+  const int c0 = blockIdx.x * 32, t0 = blockIdx.y * 32;
+  const int ncol = n - b1;
+  for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+    const int c = c0 + threadIdx.x;
+    tile[i][threadIdx.x] = (c < ncol) ? U[(long long)(b0 + t0 + i) * n + b1 + c] : 0.f;
+  }
+  __syncthreads();
+  for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+    const int c = c0 + i;
+    if (c < ncol) Ut[(long long)c * SB + t0 + threadIdx.x] = tile[threadIdx.x][i];
+  }
+}
+
+// W copy with dead channels (!(H_ii > 0)) zeroed ([host page]
+// gptq_quantize_q4tp_dev: "zero the dead columns").
+__global__ void k_copy_dz(const float* __restrict__ W, long long total, int n,
+                          const float* __restrict__ hdiag, float* __restrict__ out) {
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+       i += (long long)gridDim.x * blockDim.x) {
+    const int c = (int)(i % n);
+    out[i] = (hdiag[c] > 0.f) ? W[i] : 0.f;
+  }
+}
+
+}  // namespace
+
+size_t sweep_ws_bytes(int rows, int n) {
+  return round_up((size_t)rows * SB * 4, 256) + round_up((size_t)n * SB * 4, 256) + 512;
+}
+
+static gptq_status sweep_attrs() {
+  static bool done = false;
+  if (done) return GPTQ_OK;
+  const int smem = (SB * SB + SB + ROWS_PER_CTA * (SB + 1)) * 4;
+  GQ_CUDA(cudaFuncSetAttribute(k_sweep_block, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
+  done = true;
+  return GPTQ_OK;
+}
+
+gptq_status ladder_run(const float* W, int rows, int n, float* tab, float* lost, cudaStream_t s) {
+  GQ_PROF(K_LADDER, s);
+  k_ladder<<<rows, 128, 0, s>>>(W, n, tab, lost);
+  GQ_LAUNCHED();
+  return GPTQ_OK;
+}
+
+gptq_status group_run(const float* tile, int rows, const float* ublk, const float* hw,
+                      const float* tab, const float* lost, uint8_t* nib, uint8_t* rungs,
+                      float* scales, float* E, cudaStream_t s) {
+  GQ_PROF(K_GROUP, s);
+  k_group<<<(rows + 127) / 128, 128, 0, s>>>(tile, rows, ublk, hw, tab, lost, nib, rungs, scales, E);
+  GQ_LAUNCHED();
+  return GPTQ_OK;
+}
+
+gptq_status copy_dead_zeroed(const float* W, int rows, int n, const float* hdiag, float* out,
+                             cudaStream_t s) {
+  const long long total = (long long)rows * n;
+  GQ_PROF(K_COPY, s);
+  k_copy_dz<<<152 * 8, 256, 0, s>>>(W, total, n, hdiag, out);
+  GQ_LAUNCHED();
+  return GPTQ_OK;
+}
+
+gptq_status sweep_run(float* W, int rows, int n, const float* U, const float* hw, const float* tab,
+                      const float* lost, uint8_t* nib, uint8_t* rungs, float* scales, void* ws,
+                      size_t ws_bytes, cudaStream_t s) {
+  GQ_TRY(sweep_attrs());
+  Carve c(ws, ws_bytes);
+  float* E = c.take<float>((size_t)rows * SB);
+  float* Ut = c.take<float>((size_t)n * SB);
+  if (!c.ok) return GPTQ_ERR_NOMEM;
+  const int smem = (SB * SB + SB + ROWS_PER_CTA * (SB + 1)) * 4;
+  const GemmJob none{};
+  for (int b0 = 0; b0 < n; b0 += SB) {
+    const int B = (n - b0) < SB ? (n - b0) : SB;
+    const int b1 = b0 + B;
+    {
+      GQ_PROF(K_SWEEP_BLOCK, s);
+      k_sweep_block<<<(rows + ROWS_PER_CTA - 1) / ROWS_PER_CTA, ROWS_PER_CTA, smem, s>>>(
+          W, rows, n, b0, B, U, hw, tab, lost, nib, rungs, scales, E);
+      GQ_LAUNCHED();
+    }
+    if (b1 < n) {
+      {
+        GQ_PROF(K_PREP_UT, s);
+        dim3 grid((n - b1 + 31) / 32, SB / 32);
+        k_prep_ut<<<grid, dim3(32, 8), 0, s>>>(U, n, b0, b1, Ut);
+        GQ_LAUNCHED();
+      }
+      GQ_TRY(gemm_sub(gemm_rect(W + b1, n, E, SB, Ut, SB, rows, n - b1), none, SB, nullptr,
+                      K_SWEEP_GEMM, s));
+    }
+  }
+  return GPTQ_OK;
+}
+
+}  // namespace gq

@@ -1,0 +1,199 @@
+/*
+ * gptq_fold.h -- C ABI of the GB300 GPTQ fold + q4tp sweep library
+ * (libgptqfold.so).
+ *
+ * What it computes is defined by two pages of the cortiq project:
+ *   [fold page]  cortiq-engine src/gpu_wgpu/gptq_dev.rs -- module doc comment
+ *                (steps 1-5), WGSL kernels build_a, chol_*, inv_*, make_u,
+ *                q4tp_group, q4tp_trail, and the host functions fold /
+ *                sweep_q4tp;
+ *   [host page]  cortiq-cli src/gptq.rs -- gptq_fold_operator_par (the f64
+ *                host fold), gptq_quantize_q4tp (host sweep) and
+ *                gptq_quantize_q4tp_dev (ladder tables handed to the device).
+ *
+ * Conventions (all entry points):
+ *   - Every pointer argument is a DEVICE pointer owned by the caller, unless
+ *     the comment says "host".  The library never frees or keeps a caller
+ *     buffer, and allocates no device memory itself: scratch comes from the
+ *     caller's workspace (size from the matching *_workspace_bytes call).
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream).  Calls return once the work is enqueued, except gptq_fold and
+ *     gptq_quantize_group, which read back one 4-byte pivot flag per
+ *     factorisation attempt (a stream synchronisation) to decide the damping.
+ *   - float buffers must be 16-byte aligned; shapes are checked before any
+ *     launch.  Errors come back as a gptq_status; nothing traps.
+ *   - Matrices are row-major and dense (leading dimension = column count).
+ */
+#ifndef GPTQ_FOLD_H
+#define GPTQ_FOLD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  GPTQ_OK = 0,
+  GPTQ_ERR_ARG = 1,      /* null or misaligned pointer, lambda not finite  */
+  GPTQ_ERR_SHAPE = 2,    /* n, rows out of range; n % 32 != 0 for a sweep  */
+  GPTQ_ERR_NOMEM = 3,    /* workspace smaller than *_workspace_bytes       */
+  GPTQ_ERR_NOT_SPD = 4,  /* damping raised past lambda = 10 still failed   */
+  GPTQ_ERR_CUDA = 5,     /* a CUDA runtime call or launch failed           */
+  GPTQ_ERR_TIMEOUT = 6   /* a bounded device-side wait gave up             */
+} gptq_status;
+
+/* Largest n / rows accepted (n * n floats must stay addressable by int64). */
+#define GPTQ_MAX_N 65536
+#define GPTQ_MAX_ROWS (1 << 24)
+#define GPTQ_GROUP 32
+
+/* Human-readable name of a status code (static string). */
+const char* gptq_status_string(int status);
+
+/* Workspace bytes gptq_fold needs for n channels (0 if n is out of range). */
+size_t gptq_fold_workspace_bytes(int n);
+
+/*
+ * gptq_fold -- the fold operator of one Hessian group.
+ * [fold page] module doc, steps 1-4; kernels diag_get, build_a, chol_diag,
+ * chol_panel, chol_update, inv_diag, inv_rows, inv_update, make_u; host fn
+ * fold / fold_inner (damping retry).
+ *
+ *   H_packed  in   f32, n(n+1)/2: upper triangle of H by rows (row r starts
+ *                  at r(2n-r+1)/2, element (a<=b) at start(a)+(b-a)).  Not
+ *                  modified.
+ *   n         in   channels, 1 <= n <= GPTQ_MAX_N.
+ *   lambda    in   relative damping (the pages use 0.01); negative -> 0.
+ *   U         out  f32 n*n row-major: upper Cholesky factor of H_d^-1
+ *                  (U^T U = H_d^-1, U_jj > 0, zeros below the diagonal),
+ *                  H_d = H + lambda_used * max(mean(diag), 1e-12) * I with
+ *                  dead channels (!(H_ii > 0)) replaced by a unit row/column.
+ *   D         out  f32 n (may be NULL): sqrt(H_ii + damp) for a live channel,
+ *                  -sqrt(1 + damp) for a dead one (sign marks dead).
+ *   hdiag     out  f32 n (may be NULL): raw H_ii, the sweep's rung weights.
+ *   lambda_used out host double (may be NULL): the damping that factored.
+ *   ws, ws_bytes   workspace, >= gptq_fold_workspace_bytes(n), 256-B aligned.
+ *
+ * Damping retry (fold page, fold_inner): a pivot that is not positive (or
+ * NaN) raises lambda (0 -> 1e-4, otherwise x10) and refactors from H; past
+ * 10 the call returns GPTQ_ERR_NOT_SPD (U then holds no valid operator).
+ */
+gptq_status gptq_fold(const float* H_packed, int n, double lambda, float* U, float* D,
+                      float* hdiag, double* lambda_used, void* ws, size_t ws_bytes,
+                      void* stream);
+
+/*
+ * gptq_ladder -- per-row q4tp scale ladder (a7).  The pages only call the
+ * converter that makes it (host page, gptq_quantize_q4tp_dev: "the
+ * converter's ladder", rungs 2^(lo + c*step), f16 lo/step); the reading
+ * implemented: over the row's groups with absmax a_g > 0, x_g = f32(a_g/7),
+ * lo = f16(log2 min x_g), step = f16(max(0, (log2 max x_g - lo)/31)) (0 when
+ * min == max), tab[c] = f32(2^(lo + c*step)); an all-zero row gets zeros.
+ *
+ *   W     in  f32 rows*n (dead columns already zeroed), n % 32 == 0.
+ *   tab   out f32 rows*32;  lost out f32 rows*2 = (lo, step) per row.
+ */
+gptq_status gptq_ladder(const float* W, int rows, int n, float* tab, float* lost, void* stream);
+
+/* Workspace bytes gptq_q4tp_sweep needs. */
+size_t gptq_sweep_workspace_bytes(int rows, int n);
+
+/*
+ * gptq_q4tp_sweep -- the column-sequential q4tp GPTQ sweep of W against U.
+ * [fold page] module doc step 5, WGSL q4tp_group + q4tp_trail, host fn
+ * sweep_q4tp; [host page] gptq_quantize_q4tp (same rule, host form).
+ *
+ * Per 32-column group: rung = best of nominal-2..nominal+1 by the
+ * hw-weighted error (nominal from the corrected absmax), codes
+ * clamp(rne(w/s), -8, 7), residual e_j = (w_j - q s)/U_jj with in-group
+ * feedback; the residuals reach the later columns through
+ * W[:, later] -= E * U[group, later] (applied here per block of 128 columns:
+ * same mathematics, different f32 summation order than one group at a time).
+ *
+ *   W       in/out f32 rows*n: the weights (dead columns zeroed); consumed
+ *                  (holds partially corrected values afterwards).
+ *   U       in  f32 n*n from gptq_fold.   hw in f32 n: rung-error weights
+ *                  (the pages pass the raw H_ii).
+ *   tab, lost in  from gptq_ladder.
+ *   nibbles out u8 rows*n/2: tile (row, group) = 16 bytes at
+ *                  (row*n/32 + group)*16; column j -> byte j/2, low nibble
+ *                  for even j; nibble = code + 8.
+ *   rungs   out u8 rows*n/32 (rung index 0..31 per (row, group)).
+ *   scales  out f32 rows*n/32 = tab[row][rung].
+ *   n % 32 == 0 (else GPTQ_ERR_SHAPE, as the fold page's sweep declines).
+ */
+gptq_status gptq_q4tp_sweep(float* W, int rows, int n, const float* U, const float* hw,
+                            const float* tab, const float* lost, uint8_t* nibbles,
+                            uint8_t* rungs, float* scales, void* ws, size_t ws_bytes,
+                            void* stream);
+
+/*
+ * gptq_q4tp_group -- the rung + rounding + in-group feedback rule alone, on
+ * one 32-column tile of every row ([fold page] WGSL q4tp_group).  Exposed so
+ * the rule can be checked bit for bit against a reference on given tiles.
+ *
+ *   tile  in  f32 rows*32 (the group's current weights per row).
+ *   ublk  in  f32 32*32 row-major: U[c0..c0+32, c0..c0+32].
+ *   hw    in  f32 32.  tab/lost in as for the sweep (rows*32, rows*2).
+ *   nibbles out u8 rows*16; rungs out u8 rows; scales out f32 rows;
+ *   E     out f32 rows*32 (the scaled residuals e_j).
+ */
+gptq_status gptq_q4tp_group(const float* tile, int rows, const float* ublk, const float* hw,
+                            const float* tab, const float* lost, uint8_t* nibbles,
+                            uint8_t* rungs, float* scales, float* E, void* stream);
+
+/* Workspace bytes gptq_quantize_group needs. */
+size_t gptq_group_workspace_bytes(int rows, int n);
+
+/*
+ * gptq_quantize_group -- fold + dead-column zeroing + ladder + sweep for one
+ * Hessian group ([host page] run_quantize_gptq_tiled's device path:
+ * gptq_fold_dev then gptq_quantize_q4tp_dev).  W is not modified (a zeroed
+ * copy lives in the workspace).  U, D, hdiag may be NULL (then they live in
+ * the workspace only); otherwise they receive the fold's outputs.
+ */
+gptq_status gptq_quantize_group(const float* H_packed, int n, double lambda, const float* W,
+                                int rows, uint8_t* nibbles, uint8_t* rungs, float* scales,
+                                float* tab, float* lost, float* U, float* D, float* hdiag,
+                                double* lambda_used, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * gptq_build_equilibrated -- the builder step alone ([fold page] build_a):
+ * A[i][j] = (H[ii][jj] + delta_ij damp) / (d_ii d_jj), ii = n-1-i, dead
+ * channels an identity row/column, damp = lambda * max(mean diag, 1e-12).
+ * Writes the lower triangle of the n*n f32 A (upper left untouched) and the
+ * signed D.  Uses the fold workspace.
+ */
+gptq_status gptq_build_equilibrated(const float* H_packed, int n, double lambda, float* A,
+                                    float* D, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Tracing: launch accounting and per-kernel timing.  Every kernel launch of
+ * the library is counted; between gptq_profile_start and gptq_profile_stop
+ * each launch is also bracketed by a pair of CUDA events recorded on the
+ * launching stream (host-side event objects, created once and reused; no
+ * device memory).  Single host thread at a time.
+ *
+ *   gptq_launch_count     kernels launched by the library since it loaded.
+ *   gptq_kernel_kinds     number of kernel kinds; gptq_kernel_kind_name(k)
+ *                         their names ("fold_gemm", "sweep_gemm", ...).
+ *   gptq_profile_start    start recording, up to max_launches launches.
+ *   gptq_profile_stop     synchronise the recorded events, write per-kind
+ *                         total milliseconds and launch counts (host arrays
+ *                         of nkinds entries, either may be NULL), stop.
+ *                         Returns the kinds written, -2 if max_launches was
+ *                         reached (later launches went unrecorded), -1 on a
+ *                         CUDA error.
+ */
+long long gptq_launch_count(void);
+int gptq_kernel_kinds(void);
+const char* gptq_kernel_kind_name(int kind);
+gptq_status gptq_profile_start(int max_launches);
+int gptq_profile_stop(double* ms_by_kind, long long* launches_by_kind, int nkinds);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GPTQ_FOLD_H */

@@ -9,6 +9,7 @@ from __future__ import annotations
 
 import numpy as np
 import scipy.linalg
+import scipy.linalg.lapack
 
 
 class NotSPD(Exception):
@@ -23,10 +24,13 @@ def unpack_upper(hp, n: int) -> np.ndarray:
     """
     hp = np.asarray(hp, dtype=np.float32)
     assert hp.shape == (n * (n + 1) // 2,)
-    h = np.zeros((n, n), dtype=np.float64)
-    iu = np.triu_indices(n)  # row-major order == packed order
-    h[iu] = hp.astype(np.float64)
-    h.T[iu] = hp.astype(np.float64)
+    h = np.empty((n, n), dtype=np.float64)
+    off = 0
+    for r in range(n):
+        row = hp[off : off + n - r]
+        h[r, r:] = row
+        h[r:, r] = row
+        off += n - r
     return h
 
 
@@ -81,23 +85,29 @@ def fold(hp, n: int, lam: float = 0.01):
     """
     dead, h, base = fold_damping(hp, n)
     lam = max(float(lam), 0.0)
-    eye = np.eye(n)
+    diag = np.arange(n)
+    hdiag0 = h[diag, diag].copy()
     while True:
         if not np.isfinite(lam * base):
             raise NotSPD(f"non-finite damping (base={base})")
-        hd = h + (lam * base) * eye
-        lo = _chol_ok(hd)
+        h[diag, diag] = hdiag0 + lam * base
+        lo = _chol_ok(h)
         if lo is not None:
             break
         lam = 1e-4 if lam == 0.0 else lam * 10.0
         if lam > 10.0:
             raise NotSPD("no damping up to 10 x mean(diag) makes H positive definite")
+    del h
     damp = lam * base
-    # L^-1 (forward substitution), H_d^-1 = L^-T L^-1, M = chol(H_d^-1), U = M^T.
-    linv = scipy.linalg.solve_triangular(lo, eye, lower=True)
-    hinv = linv.T @ linv
-    hinv = 0.5 * (hinv + hinv.T)
+    # L^-1 and H_d^-1 = L^-T L^-1 (LAPACK potri: triangular inverse, then
+    # the product), M = chol(H_d^-1), U = M^T.
+    hinv, info = scipy.linalg.lapack.dpotri(lo, lower=1)
+    if info != 0:
+        raise NotSPD(f"potri failed (info={info})")
+    del lo
+    hinv = np.tril(hinv) + np.tril(hinv, -1).T
     m = _chol_ok(hinv)
+    del hinv
     if m is None:
         raise NotSPD("H_d^-1 did not factor")
     u = np.ascontiguousarray(m.T)

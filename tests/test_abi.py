@@ -1,0 +1,76 @@
+"""The C-ABI library loads, exports every symbol include/gptq_fold.h
+declares, and rejects bad arguments before any device work (CPU only: no
+call here reaches a kernel)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gptq_fold.h")
+
+
+@pytest.fixture(scope="module")
+def clib():
+    from gptq_post_weight_gb300 import _lib, build
+
+    if not os.path.exists(_lib.LIB_PATH):
+        build.build()
+    return _lib.load()
+
+
+def declared():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(gptq_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    names = declared()
+    for want in ("gptq_fold", "gptq_q4tp_sweep", "gptq_quantize_group", "gptq_ladder",
+                 "gptq_q4tp_group", "gptq_fold_workspace_bytes"):
+        assert want in names
+
+
+def test_every_declared_symbol_is_exported(clib):
+    from gptq_post_weight_gb300 import _lib
+
+    for name in declared():
+        assert hasattr(clib, name), name
+        assert name in _lib.SIGNATURES, f"binding lacks {name}"
+
+
+def test_workspace_sizes(clib):
+    assert clib.gptq_fold_workspace_bytes(0) == 0
+    assert clib.gptq_fold_workspace_bytes(70000) == 0
+    n = 17408
+    need = clib.gptq_fold_workspace_bytes(n)
+    assert need >= n * n * 4
+    assert need < n * n * 4 * 1.1
+    assert clib.gptq_sweep_workspace_bytes(5120, n) > 0
+    assert clib.gptq_group_workspace_bytes(5120, n) > need
+
+
+def test_argument_errors_before_launch(clib):
+    P = ctypes.c_void_p
+    fake = P(1 << 20)  # never dereferenced: every call below fails its checks first
+    mis = P((1 << 20) + 4)
+    ws = P(1 << 21)
+    lam = ctypes.c_double()
+    # shape errors
+    assert clib.gptq_fold(fake, 0, 0.01, fake, None, None, None, ws, 1 << 40, None) == 2
+    assert clib.gptq_ladder(fake, 4, 48, fake, fake, None) == 2
+    assert clib.gptq_q4tp_sweep(fake, 4, 40, fake, fake, fake, fake, fake, fake, fake, ws, 1 << 40, None) == 2
+    assert clib.gptq_q4tp_sweep(fake, 0, 64, fake, fake, fake, fake, fake, fake, fake, ws, 1 << 40, None) == 2
+    # null / misaligned pointers
+    assert clib.gptq_fold(None, 16, 0.01, fake, None, None, None, ws, 1 << 40, None) == 1
+    assert clib.gptq_fold(mis, 16, 0.01, fake, None, None, None, ws, 1 << 40, None) == 1
+    assert clib.gptq_fold(fake, 16, float("nan"), fake, None, None, ctypes.byref(lam), ws, 1 << 40, None) == 1
+    assert clib.gptq_q4tp_group(fake, 8, fake, fake, None, fake, fake, fake, fake, fake, None) == 1
+    # workspace too small
+    assert clib.gptq_fold(fake, 16, 0.01, fake, None, None, None, ws, 16, None) == 3
+    assert clib.gptq_q4tp_sweep(fake, 4, 64, fake, fake, fake, fake, fake, fake, fake, ws, 16, None) == 3
+    assert clib.gptq_quantize_group(fake, 64, 0.01, fake, 4, fake, fake, fake, None, None, None, None,
+                                    None, None, ws, 16, None) == 3
+    assert clib.gptq_status_string(4).startswith(b"not positive definite")

@@ -1,0 +1,276 @@
+"""Parity of the CUDA path (through the C ABI) with the oracle, on seeded
+inputs shaped like the pages' workloads.
+
+Tolerances (from the acceptance bar of the build and the arithmetic):
+* U: relative Frobenius error <= 1e-4 against the f64 oracle;
+* the rung/rounding rule: bit-exact on the oracle's own tiles and U;
+* the ladder: bit-exact (f64 log2/exp2 on both sides, f16/f32 rounding);
+* end to end: >= 99.9 % of codes equal, output error tr(E H E^T) within 1 %.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+F32 = np.float32
+DEV = "cuda"
+
+
+def np_(t):
+    return t.detach().cpu().numpy()
+
+
+def pack(h):
+    n = h.shape[0]
+    return np.concatenate([h[r, r:] for r in range(n)]).astype(F32)
+
+
+def rel_fro(a, b):
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    return float(np.linalg.norm(a - b) / np.linalg.norm(b))
+
+
+def small_problem(n, rows, seed=0, sigma=1.0, n_out=2, n_dead=2, T=None):
+    cfg = synth.Config(f"n{n}", n, rows, T or 4 * n, 0.02, sigma, n_out, n_dead, 0.01, seed)
+    hp, w = synth.make_problem(cfg, "cpu")
+    return cfg, hp.numpy(), w.numpy()
+
+
+# ------------------------------------------------------------------ fold
+
+@pytest.mark.parametrize("n", [256, 200, 333, 1000])
+def test_build_equilibrated(lib, n):
+    from gptq_post_weight_gb300 import _lib
+
+    cfg, hp, _ = small_problem(n, 8, seed=n)
+    a, d = _lib.build_equilibrated(torch.from_numpy(hp).to(DEV), n, 0.01)
+    want, dw, damp = oracle.equilibrated_reversed(hp, n, 0.01)
+    got = np.tril(np_(a))
+    assert np.abs(got - want).max() <= 2e-6 * np.abs(want).max()
+    np.testing.assert_allclose(np_(d), dw, rtol=1e-6)
+
+
+@pytest.mark.parametrize("n,sigma", [(256, 1.0), (200, 1.5), (333, 1.5), (1000, 1.5), (1536, 1.0)])
+def test_fold_parity(lib, n, sigma):
+    from gptq_post_weight_gb300 import _lib
+
+    cfg, hp, _ = small_problem(n, 8, seed=1, sigma=sigma, n_out=max(2, n // 256), n_dead=2)
+    u, d, hd, lam = _lib.fold(torch.from_numpy(hp).to(DEV), n, 0.01)
+    uo, do, dead, lamo = oracle.fold(hp, n, 0.01)
+    assert lam == lamo
+    u = np_(u)
+    assert np.all(np.tril(u, -1) == 0)
+    assert rel_fro(u, uo) <= 1e-4, rel_fro(u, uo)
+    np.testing.assert_allclose(np_(d), do, rtol=2e-7)
+    assert np.array_equal(np_(hd), hp[np.arange(n) * (2 * n - np.arange(n) + 1) // 2])
+
+
+def test_fold_rank_deficient_retry(lib):
+    # Rank n/2, lambda = 0: the first attempt must fail and damping rise.
+    from gptq_post_weight_gb300 import _lib
+
+    n = 384
+    cfg = synth.Config("rd", n, 8, n // 2, 0.02, 1.0, 2, 2, 0.0, 3)
+    hp = synth.make_h_packed(cfg).numpy()
+    u, d, hd, lam = _lib.fold(torch.from_numpy(hp).to(DEV), n, 0.0)
+    lamo = oracle.fold(hp, n, 0.0)[3]
+    assert lam >= 1e-4
+    # f32 may need one more x10 step than f64; never less damping.
+    assert lamo <= lam <= 10 * lamo * (1 + 1e-12)
+    uo = oracle.fold(hp, n, lam)[0]
+    assert rel_fro(np_(u), uo) <= 1e-3
+
+
+def test_fold_not_spd_and_nan(lib):
+    from gptq_post_weight_gb300 import _lib
+
+    n = 64
+    rng = np.random.default_rng(0)
+    v = rng.standard_normal(n)
+    h = (np.eye(n) - 30.0 * np.outer(v, v) / (v @ v)).astype(F32)  # eigenvalue -29
+    with pytest.raises(_lib.GptqError) as ei:
+        _lib.fold(torch.from_numpy(pack(h)).to(DEV), n, 0.01)
+    assert ei.value.code == 4
+    with pytest.raises(oracle.NotSPD):
+        oracle.fold(pack(h), n, 0.01)
+    x = rng.standard_normal((n, 3 * n)).astype(F32)
+    h2 = (x @ x.T / (3 * n)).astype(F32)
+    h2[3, 9] = h2[9, 3] = np.nan
+    with pytest.raises(_lib.GptqError) as ei:
+        _lib.fold(torch.from_numpy(pack(h2)).to(DEV), n, 0.01)
+    assert ei.value.code == 4
+
+
+def test_fold_all_dead(lib):
+    from gptq_post_weight_gb300 import _lib
+
+    n = 160
+    hp = np.zeros(n * (n + 1) // 2, dtype=F32)
+    u, d, hd, lam = _lib.fold(torch.from_numpy(hp).to(DEV), n, 0.01)
+    uo = oracle.fold(hp, n, 0.01)[0]
+    assert rel_fro(np_(u), uo) <= 1e-6
+    assert np.all(np_(d) < 0)
+
+
+# ------------------------------------------------------------------ ladder and the group rule
+
+@pytest.mark.parametrize("rows,n,seed", [(64, 256, 0), (333, 1024, 5)])
+def test_ladder_bit_exact(lib, rows, n, seed):
+    from gptq_post_weight_gb300 import _lib
+
+    rng = np.random.default_rng(seed)
+    w = (rng.standard_normal((rows, n)) * 0.02 * np.exp(rng.standard_normal((rows, 1)))).astype(F32)
+    w[3] = 0.0
+    w[5, :] = 0.0
+    w[5, 40] = 0.3
+    w[:, 64:96] = 0.0
+    tab, lost = _lib.ladder(torch.from_numpy(w).to(DEV))
+    to, lo = oracle.ladder(w)
+    assert np.array_equal(np_(tab).view(np.uint32), to.view(np.uint32))
+    assert np.array_equal(np_(lost).view(np.uint32), lo.view(np.uint32))
+
+
+def _nibble_bytes(q):
+    """Oracle codes [rows, 32] -> the 16 tile bytes the kernel writes."""
+    nib = (q.astype(np.int16) + 8).astype(np.uint8)
+    return (nib[:, 0::2] | (nib[:, 1::2] << 4)).astype(np.uint8)
+
+
+@pytest.mark.parametrize("rows,n,seed", [(64, 256, 0), (300, 1024, 2)])
+def test_group_rule_bit_exact(lib, rows, n, seed):
+    # The oracle's own sweep records every group's starting tile; the device
+    # rule, given that tile and the oracle's U, must reproduce rung, codes,
+    # scale and residuals bit for bit.
+    from gptq_post_weight_gb300 import _lib
+
+    cfg, hp, w = small_problem(n, rows, seed=seed, sigma=1.5, n_out=3, n_dead=3)
+    uo, do, dead, lam = oracle.fold(hp, n, 0.01)
+    u32 = uo.astype(F32)
+    wdz = w.copy()
+    wdz[:, dead] = 0
+    tab, lost = oracle.ladder(wdz)
+    hw = oracle.unpack_upper(hp, n).diagonal().astype(F32)
+    res = oracle.sweep_q4tp(w, u32, hw, tab, lost, dead, record=True)
+    tab_d = torch.from_numpy(tab).to(DEV)
+    lost_d = torch.from_numpy(lost).to(DEV)
+    for g in range(n // 32):
+        c0 = g * 32
+        tile = torch.from_numpy(np.ascontiguousarray(res["tiles"][g])).to(DEV)
+        ublk = torch.from_numpy(np.ascontiguousarray(u32[c0:c0 + 32, c0:c0 + 32])).to(DEV)
+        hwb = torch.from_numpy(np.ascontiguousarray(hw[c0:c0 + 32])).to(DEV)
+        nib, rungs, scales, e = _lib.q4tp_group(tile, ublk, hwb, tab_d, lost_d)
+        assert np.array_equal(np_(rungs).astype(np.int64), res["rung"][:, g]), g
+        assert np.array_equal(np_(nib), _nibble_bytes(res["q"][:, c0:c0 + 32])), g
+        assert np.array_equal(np_(scales).view(np.uint32), res["scale"][:, g].view(np.uint32)), g
+        assert np.array_equal(np_(e).view(np.uint32), res["e"][:, c0:c0 + 32].view(np.uint32)), g
+
+
+# ------------------------------------------------------------------ end to end
+
+def _compare_e2e(hp, w, n, rows_idx, out, lam=0.01, uo=None):
+    """Oracle fold (unless given) + ladder + sweep on rows_idx; compare."""
+    if uo is None:
+        uo, do, dead, lamo = oracle.fold(hp, n, lam)
+    else:
+        dead = ~(oracle.unpack_upper(hp, n).diagonal() > 0)
+    u32 = uo.astype(F32)
+    ws = w[rows_idx].copy()
+    ws[:, dead] = 0
+    tab, lost = oracle.ladder(ws)
+    hraw = oracle.unpack_upper(hp, n)
+    hw = hraw.diagonal().astype(F32)
+    res = oracle.sweep_q4tp(w[rows_idx], u32, hw, tab, lost, dead)
+    rows = w.shape[0]
+    q_dev = oracle.nibbles_to_codes(np_(out["nibbles"]), rows, n)[rows_idx]
+    rung_dev = np_(out["rungs"]).reshape(rows, n // 32)[rows_idx]
+    sc_dev = np_(out["scales"]).reshape(rows, n // 32)[rows_idx]
+    assert np.array_equal(np_(out["tab"])[rows_idx].view(np.uint32), tab.view(np.uint32))
+    agree = float((q_dev == res["q"]).mean())
+    rung_agree = float((rung_dev == res["rung"]).mean())
+    e_dev = oracle.output_error(w[rows_idx], oracle.dequant_q4tp(q_dev, sc_dev), hraw)
+    e_or = oracle.output_error(w[rows_idx], oracle.dequant_q4tp(res["q"], res["scale"]), hraw)
+    return agree, rung_agree, e_dev, e_or
+
+
+@pytest.mark.parametrize("n,rows,sigma", [(256, 64, 1.0), (1024, 300, 1.5), (2048, 200, 1.5)])
+def test_quantize_group_end_to_end(lib, n, rows, sigma):
+    from gptq_post_weight_gb300 import _lib
+
+    cfg, hp, w = small_problem(n, rows, seed=4, sigma=sigma, n_out=max(2, n // 256), n_dead=4)
+    out = _lib.quantize_group(torch.from_numpy(hp).to(DEV), n, torch.from_numpy(w).to(DEV), 0.01)
+    agree, rung_agree, e_dev, e_or = _compare_e2e(hp, w, n, np.arange(rows), out)
+    assert agree >= 0.999, agree
+    assert rung_agree >= 0.999, rung_agree
+    assert abs(e_dev - e_or) <= 0.01 * e_or, (e_dev, e_or)
+
+
+def test_sweep_alone_matches_chain(lib):
+    # gptq_q4tp_sweep on the chain's own U / ladder reproduces the chain.
+    from gptq_post_weight_gb300 import _lib
+
+    n, rows = 512, 130
+    cfg, hp, w = small_problem(n, rows, seed=9, n_dead=3)
+    hpd = torch.from_numpy(hp).to(DEV)
+    wd = torch.from_numpy(w).to(DEV)
+    out = _lib.quantize_group(hpd, n, wd, 0.01)
+    u, d, hd, lam = _lib.fold(hpd, n, 0.01)
+    assert torch.equal(u, out["u"])
+    wz = wd.clone()
+    wz[:, ~(hd > 0)] = 0
+    tab, lost = _lib.ladder(wz)
+    nib, rungs, scales = _lib.q4tp_sweep(wz, u, hd, tab, lost)
+    assert torch.equal(nib, out["nibbles"]) and torch.equal(rungs, out["rungs"])
+    assert torch.equal(scales, out["scales"])
+
+
+def test_gptq_beats_rtn_on_device(lib):
+    # The pages' quality claim on the device path: output error < 0.8 x the
+    # round-to-nearest error with the same ladder (U = identity).
+    from gptq_post_weight_gb300 import _lib
+
+    rows, n, t = 24, 96, 400
+    rng = np.random.default_rng(12345)
+    lat = rng.uniform(-0.5, 0.5, (t, 4))
+    mix = rng.uniform(-0.5, 0.5, (4, n))
+    x = lat @ mix + 0.2 * rng.uniform(-0.5, 0.5, (t, n))
+    x[:, 5] *= 8.0
+    h = (x.T @ x).astype(F32)
+    w = rng.uniform(-0.5, 0.5, (rows, n)).astype(F32)
+    out = _lib.quantize_group(torch.from_numpy(pack(h)).to(DEV), n, torch.from_numpy(w).to(DEV), 0.01)
+    q = oracle.nibbles_to_codes(np_(out["nibbles"]), rows, n)
+    eg = oracle.output_error(w, oracle.dequant_q4tp(q, np_(out["scales"]).reshape(rows, -1)), h)
+    tab, lost = oracle.ladder(w)
+    r = oracle.sweep_q4tp(w, np.eye(n, dtype=F32), h.diagonal().astype(F32), tab, lost)
+    er = oracle.output_error(w, oracle.dequant_q4tp(r["q"], r["scale"]), h)
+    assert eg < 0.8 * er
+
+
+# ------------------------------------------------------------------ full sizes (sampled rows)
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["n4096", "n17408"])
+def test_full_size_group(lib, name):
+    """The bench's workload: GPU inputs, full fold compared with the f64
+    oracle, the sweep on sampled rows (rows are independent given U)."""
+    from gptq_post_weight_gb300 import _lib
+
+    cfg = synth.config(name)
+    hpd, wd = synth.make_problem(cfg, DEV)
+    out = _lib.quantize_group(hpd, cfg.n, wd, cfg.lam)
+    hp = np_(hpd)
+    w = np_(wd)
+    del hpd, wd
+    uo, do, dead, lamo = oracle.fold(hp, cfg.n, cfg.lam)
+    assert out["lam"] == lamo
+    assert rel_fro(np_(out["u"]), uo) <= 1e-4
+    rng = np.random.default_rng(0)
+    rows_idx = np.sort(rng.choice(cfg.rows, 24, replace=False))
+    agree, rung_agree, e_dev, e_or = _compare_e2e(hp, w, cfg.n, rows_idx, out, uo=uo)
+    assert agree >= 0.999, agree
+    assert rung_agree >= 0.999, rung_agree
+    assert abs(e_dev - e_or) <= 0.01 * e_or, (e_dev, e_or)
