@@ -1,6 +1,7 @@
 // Shared definitions for the GB300 GPTQ fold + q4tp sweep kernels.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 #include <stddef.h>
@@ -78,42 +79,64 @@ struct Carve {
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// GEMM job: C[r][s] -= sum_t A[r][t] * B[s][t] over a set of 128x128 tiles.
-// A and B are K-major (row-major with the contraction index contiguous).
-// mode 0: rectangle of mt x nt tiles (row-major order); mode 1: lower
-// triangle of an mt x mt tile grid (tiles with ti >= tj; inside a diagonal
-// tile only r >= s is written).  Rows >= M or columns >= N are masked.
-struct GemmJob {
+// GEMM job for the tensor-core kernel: C[r][s] -= sum_t A[r][t] * B[s][t]
+// over a set of 128x128 tiles.  A and B are K-major (row-major, contraction
+// index contiguous, leading dimension K) and given as TF32 hi/lo pairs
+// through TMA tensor maps: OperandMaps.m[a_map] / m[a_map + 1] hold A_hi /
+// A_lo, likewise for B; operand row = a_row0 + tile row (b_row0 + tile col).
+// mode 0: rectangle of mt x nt tiles; mode 1: lower triangle of an mt x mt
+// tile grid (ti >= tj; inside a diagonal tile only r >= s is written).
+// Rows >= M or columns >= N are masked.
+struct TcJob {
   float* C;
-  const float* A;
-  const float* B;
-  long long ldc, lda, ldb;
+  long long ldc;
+  int a_map, b_map, a_row0, b_row0;
   int mode, mt, nt, M, N, ntiles;
 };
 
-inline GemmJob gemm_rect(float* C, long long ldc, const float* A, long long lda, const float* B,
-                         long long ldb, int M, int N) {
-  GemmJob j{};
-  j.C = C; j.A = A; j.B = B; j.ldc = ldc; j.lda = lda; j.ldb = ldb;
+struct OperandMaps {
+  CUtensorMap m[4];
+};
+
+inline TcJob tc_rect(float* C, long long ldc, int a_map, int a_row0, int b_map, int b_row0, int M,
+                     int N) {
+  TcJob j{};
+  j.C = C; j.ldc = ldc; j.a_map = a_map; j.b_map = b_map; j.a_row0 = a_row0; j.b_row0 = b_row0;
   j.mode = 0; j.M = M; j.N = N;
   j.mt = (M + 127) / 128; j.nt = (N + 127) / 128;
   j.ntiles = (M > 0 && N > 0) ? j.mt * j.nt : 0;
   return j;
 }
 
-inline GemmJob gemm_lower(float* C, long long ldc, const float* A, long long lda, int M) {
-  GemmJob j{};
-  j.C = C; j.A = A; j.B = A; j.ldc = ldc; j.lda = lda; j.ldb = lda;
+inline TcJob tc_lower(float* C, long long ldc, int map, int row0, int M) {
+  TcJob j{};
+  j.C = C; j.ldc = ldc; j.a_map = map; j.b_map = map; j.a_row0 = row0; j.b_row0 = row0;
   j.mode = 1; j.M = M; j.N = M;
   j.mt = (M + 127) / 128; j.nt = j.mt;
   j.ntiles = M > 0 ? j.mt * (j.mt + 1) / 2 : 0;
   return j;
 }
 
-// Enqueue C -= A B^T for up to two jobs in one launch (K = contraction
-// length, multiple of 32).  `flag` (device, may be null): skip all work when
-// non-zero.
-gptq_status gemm_sub(const GemmJob& j0, const GemmJob& j1, int K, const unsigned* flag,
-                     int kind, cudaStream_t s);
+// Tensor map over a K-major f32 operand array [rows][K] (box 32 x 128,
+// 128-byte swizzle).  K must be a multiple of 32, base 16-byte aligned.
+gptq_status make_operand_map(CUtensorMap* m, const float* base, long long rows, int K);
+
+// Enqueue C -= A B^T for up to two jobs in one persistent launch.
+// `flag`: skip everything when non-zero (may be null).  `status`: bit 1 is
+// set if a device-side wait timed out.
+gptq_status gemm_tc_sub(const OperandMaps& maps, const TcJob& j0, const TcJob& j1, int K,
+                        const unsigned* flag, unsigned* status, int kind, cudaStream_t s);
+
+// TF32 split: hi = x rounded to TF32 (10-bit mantissa, nearest, ties away),
+// lo = (x - hi) rounded to TF32; x - hi is exact in f32.
+__device__ __forceinline__ float tf32_rna(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return __uint_as_float(r);
+}
+__device__ __forceinline__ void split_tf32(float x, float& hi, float& lo) {
+  hi = tf32_rna(x);
+  lo = tf32_rna(x - hi);
+}
 
 }  // namespace gq

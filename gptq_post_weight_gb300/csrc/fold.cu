@@ -179,11 +179,13 @@ __global__ void __launch_bounds__(256) k_potrf(const float* __restrict__ A, long
 // row, fold page inv_diag + inv_rows): rows c < k+NB, v = Y[c][k..k+NB)
 // (the unit vector e_{c-k} when c is in block k), z -> Yp[c][*] and the
 // finished entries of U: U[n-1-i][n-1-c] = X[i][c] / |d_{n-1-c}|
-// ([fold page] make_u), i = k + t.
+// ([fold page] make_u), i = k + t.  z is stored as its TF32 hi/lo split,
+// the operand format of the update GEMM.
 template <int MODE>
 __global__ void __launch_bounds__(128) k_trsm(const float* __restrict__ A, long long lda, int k,
                                               int row0, int nrows, const float* __restrict__ Lkk,
-                                              float* __restrict__ out, const unsigned* flag,
+                                              float* __restrict__ out_hi, float* __restrict__ out_lo,
+                                              const unsigned* flag,
                                               float* __restrict__ U, const float* __restrict__ dabs,
                                               int n) {
   if (flagged(flag)) return;
@@ -227,9 +229,18 @@ __global__ void __launch_bounds__(128) k_trsm(const float* __restrict__ A, long 
     for (int t = 0; t < NB; ++t)
       if (t < unit) x[t] = 0.f;
   }
-  float4* dst = reinterpret_cast<float4*>(out + (long long)r * NB);
+  float4* dh = reinterpret_cast<float4*>(out_hi + (long long)r * NB);
+  float4* dl = reinterpret_cast<float4*>(out_lo + (long long)r * NB);
 #pragma unroll
-  for (int t = 0; t < NB / 4; ++t) dst[t] = make_float4(x[4 * t], x[4 * t + 1], x[4 * t + 2], x[4 * t + 3]);
+  for (int t = 0; t < NB / 4; ++t) {
+    float4 h, l;
+    split_tf32(x[4 * t], h.x, l.x);
+    split_tf32(x[4 * t + 1], h.y, l.y);
+    split_tf32(x[4 * t + 2], h.z, l.z);
+    split_tf32(x[4 * t + 3], h.w, l.w);
+    dh[t] = h;
+    dl[t] = l;
+  }
   if (MODE == 1 && r < n) {
     const int m = n - 1 - r;
     const float dm = dabs[m];
@@ -246,8 +257,10 @@ __global__ void __launch_bounds__(128) k_trsm(const float* __restrict__ A, long 
 struct FoldWs {
   int n, N;
   float* A;       // N x N
-  float* P;       // N x NB   (L panel of the current step)
-  float* Yp;      // N x NB   (Y panel of the current step)
+  float* P_hi;    // N x NB   (L panel of the current step, TF32 hi/lo)
+  float* P_lo;
+  float* Yp_hi;   // N x NB   (Y panel of the current step, TF32 hi/lo)
+  float* Yp_lo;
   float* Lkk;     // NB x NB
   float* hdiag;   // n
   float* dabs;    // n
@@ -260,8 +273,10 @@ static bool carve_fold(Carve& c, int n, FoldWs& w) {
   w.N = (int)round_up((size_t)n, NB);
   const size_t N = (size_t)w.N;
   w.A = c.take<float>(N * N);
-  w.P = c.take<float>(N * NB);
-  w.Yp = c.take<float>(N * NB);
+  w.P_hi = c.take<float>(N * NB);
+  w.P_lo = c.take<float>(N * NB);
+  w.Yp_hi = c.take<float>(N * NB);
+  w.Yp_lo = c.take<float>(N * NB);
   w.Lkk = c.take<float>((size_t)NB * NB);
   w.hdiag = c.take<float>((size_t)n);
   w.dabs = c.take<float>((size_t)n);
@@ -289,8 +304,8 @@ static gptq_status init_attrs() {
 
 // One factorisation attempt at damping lam: build, interleaved Cholesky +
 // inverse, U.  The pivot flag is left on the device.
-static gptq_status fold_attempt(const float* hp, const FoldWs& w, double lam, float* U, float* D,
-                                cudaStream_t s) {
+static gptq_status fold_attempt(const float* hp, const FoldWs& w, const OperandMaps& maps,
+                                double lam, float* U, float* D, cudaStream_t s) {
   const int n = w.n, N = w.N;
   const long long ld = N;
   GQ_CUDA(cudaMemsetAsync(w.flag, 0, sizeof(unsigned), s));
@@ -308,21 +323,21 @@ static gptq_status fold_attempt(const float* hp, const FoldWs& w, double lam, fl
     }
     if (s0 < N) {
       GQ_PROF(K_TRSM_PANEL, s);
-      k_trsm<0><<<(N - s0) / 128, 128, NB * NB * 4, s>>>(w.A, ld, k, s0, N - s0, w.Lkk, w.P,
-                                                         w.flag, nullptr, nullptr, n);
+      k_trsm<0><<<(N - s0) / 128, 128, NB * NB * 4, s>>>(w.A, ld, k, s0, N - s0, w.Lkk, w.P_hi,
+                                                         w.P_lo, w.flag, nullptr, nullptr, n);
       GQ_LAUNCHED();
     }
     {
       GQ_PROF(K_TRSM_INV, s);
-      k_trsm<1><<<s0 / 128, 128, NB * NB * 4, s>>>(w.A, ld, k, 0, s0, w.Lkk, w.Yp, w.flag, U,
-                                                   w.dabs, n);
+      k_trsm<1><<<s0 / 128, 128, NB * NB * 4, s>>>(w.A, ld, k, 0, s0, w.Lkk, w.Yp_hi, w.Yp_lo,
+                                                   w.flag, U, w.dabs, n);
       GQ_LAUNCHED();
     }
     if (s0 < N) {
-      GemmJob syrk = gemm_lower(w.A + (long long)s0 * ld + s0, ld, w.P + (long long)s0 * NB, NB,
-                                N - s0);
-      GemmJob inv = gemm_rect(w.A + s0, ld, w.Yp, NB, w.P + (long long)s0 * NB, NB, s0, N - s0);
-      GQ_TRY(gemm_sub(syrk, inv, NB, w.flag, K_FOLD_GEMM, s));
+      // maps: 0/1 = P hi/lo, 2/3 = Yp hi/lo.
+      const TcJob syrk = tc_lower(w.A + (long long)s0 * ld + s0, ld, 0, s0, N - s0);
+      const TcJob inv = tc_rect(w.A + s0, ld, 2, 0, 0, s0, s0, N - s0);
+      GQ_TRY(gemm_tc_sub(maps, syrk, inv, NB, w.flag, w.flag, K_FOLD_GEMM, s));
     }
   }
   return GPTQ_OK;
@@ -341,12 +356,18 @@ gptq_status fold_run(const float* hp, int n, double lambda, float* U, float* D, 
   }
   if (hdiag) GQ_CUDA(cudaMemcpyAsync(hdiag, w.hdiag, (size_t)n * 4, cudaMemcpyDeviceToDevice, s));
   GQ_CUDA(cudaMemsetAsync(U, 0, (size_t)n * n * 4, s));
+  OperandMaps maps;
+  GQ_TRY(make_operand_map(&maps.m[0], w.P_hi, w.N, NB));
+  GQ_TRY(make_operand_map(&maps.m[1], w.P_lo, w.N, NB));
+  GQ_TRY(make_operand_map(&maps.m[2], w.Yp_hi, w.N, NB));
+  GQ_TRY(make_operand_map(&maps.m[3], w.Yp_lo, w.N, NB));
   double lam = lambda > 0.0 ? lambda : 0.0;
   for (;;) {
-    GQ_TRY(fold_attempt(hp, w, lam, U, D, s));
+    GQ_TRY(fold_attempt(hp, w, maps, lam, U, D, s));
     unsigned hflag = 0;
     GQ_CUDA(cudaMemcpyAsync(&hflag, w.flag, sizeof(unsigned), cudaMemcpyDeviceToHost, s));
     GQ_CUDA(cudaStreamSynchronize(s));
+    if (hflag & 2u) return GPTQ_ERR_TIMEOUT;
     if (hflag == 0u) break;
     lam = (lam == 0.0) ? 1e-4 : lam * 10.0;
     if (lam > 10.0) return GPTQ_ERR_NOT_SPD;

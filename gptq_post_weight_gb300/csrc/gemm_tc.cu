@@ -1,0 +1,436 @@
+// C -= A B^T on the 5th-generation tensor cores (tcgen05, kind::tf32) with
+// the 3xTF32 split: A = A_hi + A_lo, B = B_hi + B_lo (each part exactly a
+// TF32 value), and C -= A_lo B_hi + A_hi B_lo + A_hi B_hi accumulated in f32
+// in tensor memory.  That keeps the products at about f32 accuracy, which the
+// fold needs (the pages compute in f32).
+//
+// This is the rank-K update every hot loop of the path reduces to: the
+// Cholesky's trailing SYRK and the inverse's block update (fold page,
+// chol_update / inv_update) and the sweep's trailing GEMM (q4tp_trail).
+//
+// Persistent kernel, one CTA per SM, 6 warps:
+//   warp 0      TMA producer: 128x32 f32 boxes of A_hi, A_lo, B_hi, B_lo
+//               (128-byte swizzle) into a 3-stage shared-memory ring;
+//   warp 1      allocates 256 TMEM columns (two 128x128 f32 accumulators)
+//               and issues the MMAs from one thread; tcgen05.commit frees a
+//               stage / publishes a finished accumulator;
+//   warps 2-5   epilogue: tcgen05.ld of one accumulator row per thread,
+//               C -= acc in global memory (masked), then release the buffer,
+//               so the epilogue of tile i overlaps the MMAs of tile i+1.
+// Every wait is bounded (about 2 s of globaltimer); on expiry the kernel
+// stops issuing, drains what it started, frees TMEM and sets bit 1 of the
+// status word.
+#include "common.cuh"
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+namespace gq {
+namespace {
+
+constexpr int BM = 128, BN = 128, BK = 32, STAGES = 3;
+constexpr int TILE_A = BM * BK * 4;  // 16 KB
+constexpr int TILE_B = BN * BK * 4;  // 16 KB
+constexpr int STAGE_BYTES = 2 * TILE_A + 2 * TILE_B;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024;
+constexpr int THREADS = 192;
+constexpr uint32_t TMEM_COLS = 2 * BN;
+constexpr unsigned long long WAIT_NS = 2000000000ull;
+
+// Instruction descriptor, kind::tf32: D f32 (bits 4-5 = 1), A and B TF32
+// (bits 7-9, 10-12 = 2), both K-major (bits 15, 16 = 0), N >> 3 at bit 17,
+// M >> 4 at bit 24.
+constexpr uint32_t IDESC = (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(BN >> 3) << 17) |
+                           ((uint32_t)(BM >> 4) << 24);
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0u;
+}
+
+// Wait for the phase of `bar` with the given parity; false once `abort` is
+// set (by anyone) or after WAIT_NS (then this thread sets it).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (;;) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort) return false;
+    if (globaltimer() - t0 > WAIT_NS) {
+      *abort = 1;
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+      "[%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor, K-major, 128-byte swizzle: start >> 4
+// (bits 0-13), leading offset 1 (unused for this layout, bits 16-29),
+// stride offset 1024 B between 8-row groups (bits 32-45), the fixed 0b001
+// at bits 46-48, swizzle mode 2 = 128B (bits 61-63).
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr) {
+  uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)1 << 16;
+  d |= (uint64_t)(1024 >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t accum) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(IDESC), "r"(accum)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   smem_u32(bar))
+               : "memory");
+}
+
+// 32 lanes x 16 consecutive 32-bit columns (one row per thread).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, "
+      "[%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+        "=r"(r[15])
+      : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_ld_wait() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tile_of(const TcJob& J, int t, int& ti, int& tj) {
+  if (J.mode == 1) {
+    int i = (int)((sqrtf(8.0f * (float)t + 1.0f) - 1.0f) * 0.5f);
+    while ((i + 1) * (i + 2) / 2 <= t) ++i;
+    while (i * (i + 1) / 2 > t) --i;
+    ti = i;
+    tj = t - i * (i + 1) / 2;
+  } else {
+    ti = t / J.nt;
+    tj = t % J.nt;
+  }
+}
+
+__global__ void __launch_bounds__(THREADS, 1)
+    k_gemm_tc(const __grid_constant__ CUtensorMap m0, const __grid_constant__ CUtensorMap m1,
+              const __grid_constant__ CUtensorMap m2, const __grid_constant__ CUtensorMap m3,
+              TcJob j0, TcJob j1, int K, const unsigned* flag, unsigned* status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ __align__(8) uint64_t full[STAGES], empty[STAGES], tfull[2], tempty[2], drain;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_sh;
+  __shared__ int issued_sh, consumed_sh;
+  __shared__ int skip_sh;
+  // One read of the skip flag, shared by the whole CTA (uniform exit).
+  if (threadIdx.x == 0) skip_sh = (flag != nullptr && *(volatile const unsigned*)flag != 0u) ? 1 : 0;
+  __syncthreads();
+  if (skip_sh) return;
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int total = j0.ntiles + j1.ntiles;
+  const int nk = K / BK;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 128);
+    }
+    mbar_init(&drain, 1);
+    abort_sh = 0;
+    issued_sh = 0;
+    consumed_sh = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(&tmem_base_sh)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+  volatile int* abort = &abort_sh;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      const CUtensorMap* maps[4] = {&m0, &m1, &m2, &m3};
+      int stage = 0, issued = 0;
+      uint32_t phase = 0;
+      for (int t = blockIdx.x; t < total && !*abort; t += gridDim.x) {
+        const bool second = t >= j0.ntiles;
+        const TcJob& J = second ? j1 : j0;
+        int ti, tj;
+        tile_of(J, second ? t - j0.ntiles : t, ti, tj);
+        const int ay = J.a_row0 + ti * BM, by = J.b_row0 + tj * BN;
+        const CUtensorMap* ahi = maps[J.a_map];
+        const CUtensorMap* alo = maps[J.a_map + 1];
+        const CUtensorMap* bhi = maps[J.b_map];
+        const CUtensorMap* blo = maps[J.b_map + 1];
+        for (int c = 0; c < nk; ++c) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, abort)) break;
+          const uint32_t sb = smem_u32(smem + stage * STAGE_BYTES);
+          mbar_expect_tx(&full[stage], STAGE_BYTES);
+          tma_load_2d(sb, ahi, c * BK, ay, &full[stage]);
+          tma_load_2d(sb + TILE_A, alo, c * BK, ay, &full[stage]);
+          tma_load_2d(sb + 2 * TILE_A, bhi, c * BK, by, &full[stage]);
+          tma_load_2d(sb + 2 * TILE_A + TILE_B, blo, c * BK, by, &full[stage]);
+          ++issued;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      issued_sh = issued;
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      int stage = 0, acc = 0, consumed = 0;
+      uint32_t phase = 0, aphase = 0;
+      for (int t = blockIdx.x; t < total && !*abort; t += gridDim.x) {
+        if (!mbar_wait(&tempty[acc], aphase ^ 1u, abort)) break;
+        tc_fence_after();
+        const uint32_t d = tmem + (uint32_t)(acc * BN);
+        bool ok = true;
+        for (int c = 0; c < nk; ++c) {
+          if (!mbar_wait(&full[stage], phase, abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_hi = smem_u32(smem + stage * STAGE_BYTES);
+          const uint32_t a_lo = a_hi + TILE_A, b_hi = a_hi + 2 * TILE_A, b_lo = b_hi + TILE_B;
+#pragma unroll
+          for (int kk = 0; kk < BK / 8; ++kk) {
+            const uint32_t off = (uint32_t)kk * 32u;
+            mma_tf32(d, sdesc(a_lo + off), sdesc(b_hi + off), (c | kk) ? 1u : 0u);
+            mma_tf32(d, sdesc(a_hi + off), sdesc(b_lo + off), 1u);
+            mma_tf32(d, sdesc(a_hi + off), sdesc(b_hi + off), 1u);
+          }
+          mma_commit(&empty[stage]);
+          ++consumed;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit(&tfull[acc]);
+        if (++acc == 2) {
+          acc = 0;
+          aphase ^= 1u;
+        }
+      }
+      consumed_sh = consumed;
+      // Every MMA this thread issued has completed once `drain` flips.
+      mma_commit(&drain);
+      if (!mbar_wait(&drain, 0u, abort)) {
+        // Give the drain a last bounded chance even after an abort.
+        const uint64_t t0 = globaltimer();
+        while (!mbar_try_wait(&drain, 0u) && globaltimer() - t0 < WAIT_NS) {
+        }
+      }
+    }
+  } else {
+    const int q = warp & 3;  // TMEM lane quarter this warp may read
+    int acc = 0;
+    uint32_t aphase = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+      // Warp-uniform wait: every lane must reach the .sync.aligned loads.
+      const bool ok = __all_sync(0xffffffffu, mbar_wait(&tfull[acc], aphase, abort));
+      if (!ok) break;
+      tc_fence_after();
+      const bool second = t >= j0.ntiles;
+      const TcJob& J = second ? j1 : j0;
+      int ti, tj;
+      tile_of(J, second ? t - j0.ntiles : t, ti, tj);
+      const int rr = q * 32 + lane;  // row inside the tile
+      const int r = ti * BM + rr;
+      const bool diag = (J.mode == 1) && (ti == tj);
+      float* crow = J.C + (long long)r * J.ldc + (long long)tj * BN;
+      const uint32_t tbase = tmem + (uint32_t)(acc * BN) + ((uint32_t)(q * 32) << 16);
+#pragma unroll 1
+      for (int cc = 0; cc < BN; cc += 32) {
+        uint32_t v0[16], v1[16];
+        __syncwarp();
+        tmem_ld16(tbase + (uint32_t)cc, v0);
+        tmem_ld16(tbase + (uint32_t)cc + 16u, v1);
+        tmem_ld_wait();
+        if (r < J.M) {
+          const int s0 = tj * BN + cc;
+          const bool full_seg = (s0 + 32 <= J.N) && !(diag && cc + 31 > rr);
+          if (full_seg) {
+            float4* p = reinterpret_cast<float4*>(crow + cc);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              float4 c = p[i];
+              c.x -= __uint_as_float(v0[4 * i]);
+              c.y -= __uint_as_float(v0[4 * i + 1]);
+              c.z -= __uint_as_float(v0[4 * i + 2]);
+              c.w -= __uint_as_float(v0[4 * i + 3]);
+              p[i] = c;
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              float4 c = p[4 + i];
+              c.x -= __uint_as_float(v1[4 * i]);
+              c.y -= __uint_as_float(v1[4 * i + 1]);
+              c.z -= __uint_as_float(v1[4 * i + 2]);
+              c.w -= __uint_as_float(v1[4 * i + 3]);
+              p[4 + i] = c;
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              if (s0 + i < J.N && !(diag && cc + i > rr))
+                crow[cc + i] -= __uint_as_float(i < 16 ? v0[i] : v1[i - 16]);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&tempty[acc]);
+      if (++acc == 2) {
+        acc = 0;
+        aphase ^= 1u;
+      }
+    }
+  }
+
+  __syncthreads();
+  if (threadIdx.x == 0 && abort_sh) {
+    // Loads issued but never consumed still target this CTA's shared memory:
+    // wait (bounded) for them to land before the CTA exits.
+    for (int i = consumed_sh; i < issued_sh; ++i) {
+      const uint64_t t0 = globaltimer();
+      while (!mbar_try_wait(&full[i % STAGES], (uint32_t)((i / STAGES) & 1)) &&
+             globaltimer() - t0 < WAIT_NS) {
+      }
+    }
+    atomicOr(status, 2u);
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS)
+                 : "memory");
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+int num_sms() {
+  static int sms = 0;
+  if (sms == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (sms <= 0) sms = 148;
+  }
+  return sms;
+}
+
+}  // namespace
+
+gptq_status make_operand_map(CUtensorMap* m, const float* base, long long rows, int K) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return GPTQ_ERR_CUDA;
+  if ((reinterpret_cast<uintptr_t>(base) & 15u) != 0 || K % BK != 0) return GPTQ_ERR_ARG;
+  cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)K * 4u};
+  cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)BM};
+  cuuint32_t es[2] = {1u, 1u};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? GPTQ_OK : GPTQ_ERR_CUDA;
+}
+
+gptq_status gemm_tc_sub(const OperandMaps& maps, const TcJob& j0, const TcJob& j1, int K,
+                        const unsigned* flag, unsigned* status, int kind, cudaStream_t s) {
+  static bool attr = false;
+  if (!attr) {
+    GQ_CUDA(cudaFuncSetAttribute(k_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES));
+    attr = true;
+  }
+  if (K % BK != 0 || K <= 0) return GPTQ_ERR_ARG;
+  const int total = j0.ntiles + j1.ntiles;
+  if (total <= 0) return GPTQ_OK;
+  const int grid = total < num_sms() ? total : num_sms();
+  GQ_PROF(kind, s);
+  k_gemm_tc<<<grid, THREADS, SMEM_BYTES, s>>>(maps.m[0], maps.m[1], maps.m[2], maps.m[3], j0, j1, K,
+                                              flag, status);
+  GQ_LAUNCHED();
+  return GPTQ_OK;
+}
+
+}  // namespace gq

@@ -194,7 +194,7 @@ __global__ void __launch_bounds__(ROWS_PER_CTA) k_sweep_block(
     const float* __restrict__ W, int rows, int n, int b0, int B, const float* __restrict__ U,
     const float* __restrict__ hw, const float* __restrict__ tab, const float* __restrict__ lost,
     uint8_t* __restrict__ nib, uint8_t* __restrict__ rungs, float* __restrict__ scales,
-    float* __restrict__ E) {
+    float* __restrict__ E_hi, float* __restrict__ E_lo) {
   extern __shared__ __align__(16) float sm[];
   float* Us = sm;                       // [SB][SB]
   float* hws = Us + SB * SB;            // [SB]
@@ -230,9 +230,18 @@ __global__ void __launch_bounds__(ROWS_PER_CTA) k_sweep_block(
     reinterpret_cast<uint4*>(nib)[tix] = make_uint4(words[0], words[1], words[2], words[3]);
     rungs[tix] = (uint8_t)c;
     scales[tix] = s;
-    float4* erow = reinterpret_cast<float4*>(E + (long long)r * SB + g * GROUP);
+    float4* eh = reinterpret_cast<float4*>(E_hi + (long long)r * SB + g * GROUP);
+    float4* el = reinterpret_cast<float4*>(E_lo + (long long)r * SB + g * GROUP);
 #pragma unroll
-    for (int t = 0; t < GROUP / 4; ++t) erow[t] = make_float4(e[4 * t], e[4 * t + 1], e[4 * t + 2], e[4 * t + 3]);
+    for (int t = 0; t < GROUP / 4; ++t) {
+      float4 h, l;
+      split_tf32(e[4 * t], h.x, l.x);
+      split_tf32(e[4 * t + 1], h.y, l.y);
+      split_tf32(e[4 * t + 2], h.z, l.z);
+      split_tf32(e[4 * t + 3], h.w, l.w);
+      eh[t] = h;
+      el[t] = l;
+    }
     for (int col = (g + 1) * GROUP; col < B; ++col) {
       float acc = 0.f;
 #pragma unroll
@@ -242,9 +251,10 @@ __global__ void __launch_bounds__(ROWS_PER_CTA) k_sweep_block(
   }
 }
 
-// Ut[c][t] = U[b0 + t][b1 + c]: the block row of U, K-major for the GEMM.
+// Ut[c][t] = U[b0 + t][b1 + c]: the block row of U, K-major for the GEMM,
+// stored as its TF32 hi/lo split.
 __global__ void k_prep_ut(const float* __restrict__ U, int n, int b0, int b1,
-                          float* __restrict__ Ut) {
+                          float* __restrict__ Ut_hi, float* __restrict__ Ut_lo) {
   __shared__ float tile[32][33];
   const int c0 = blockIdx.x * 32, t0 = blockIdx.y * 32;
   const int ncol = n - b1;
@@ -255,7 +265,12 @@ __global__ void k_prep_ut(const float* __restrict__ U, int n, int b0, int b1,
   __syncthreads();
   for (int i = threadIdx.y; i < 32; i += blockDim.y) {
     const int c = c0 + i;
-    if (c < ncol) Ut[(long long)c * SB + t0 + threadIdx.x] = tile[threadIdx.x][i];
+    if (c < ncol) {
+      float h, l;
+      split_tf32(tile[threadIdx.x][i], h, l);
+      Ut_hi[(long long)c * SB + t0 + threadIdx.x] = h;
+      Ut_lo[(long long)c * SB + t0 + threadIdx.x] = l;
+    }
   }
 }
 
@@ -273,7 +288,7 @@ __global__ void k_copy_dz(const float* __restrict__ W, long long total, int n,
 }  // namespace
 
 size_t sweep_ws_bytes(int rows, int n) {
-  return round_up((size_t)rows * SB * 4, 256) + round_up((size_t)n * SB * 4, 256) + 512;
+  return 2 * round_up((size_t)rows * SB * 4, 256) + 2 * round_up((size_t)n * SB * 4, 256) + 1024;
 }
 
 static gptq_status sweep_attrs() {
@@ -315,32 +330,44 @@ gptq_status sweep_run(float* W, int rows, int n, const float* U, const float* hw
                       size_t ws_bytes, cudaStream_t s) {
   GQ_TRY(sweep_attrs());
   Carve c(ws, ws_bytes);
-  float* E = c.take<float>((size_t)rows * SB);
-  float* Ut = c.take<float>((size_t)n * SB);
+  float* E_hi = c.take<float>((size_t)rows * SB);
+  float* E_lo = c.take<float>((size_t)rows * SB);
+  float* Ut_hi = c.take<float>((size_t)n * SB);
+  float* Ut_lo = c.take<float>((size_t)n * SB);
+  unsigned* status = c.take<unsigned>(4);
   if (!c.ok) return GPTQ_ERR_NOMEM;
+  GQ_CUDA(cudaMemsetAsync(status, 0, sizeof(unsigned), s));
+  OperandMaps maps;  // 0/1 = Ut hi/lo, 2/3 = E hi/lo
+  GQ_TRY(make_operand_map(&maps.m[0], Ut_hi, n, SB));
+  GQ_TRY(make_operand_map(&maps.m[1], Ut_lo, n, SB));
+  GQ_TRY(make_operand_map(&maps.m[2], E_hi, rows, SB));
+  GQ_TRY(make_operand_map(&maps.m[3], E_lo, rows, SB));
   const int smem = (SB * SB + SB + ROWS_PER_CTA * (SB + 1)) * 4;
-  const GemmJob none{};
+  const TcJob none{};
   for (int b0 = 0; b0 < n; b0 += SB) {
     const int B = (n - b0) < SB ? (n - b0) : SB;
     const int b1 = b0 + B;
     {
       GQ_PROF(K_SWEEP_BLOCK, s);
       k_sweep_block<<<(rows + ROWS_PER_CTA - 1) / ROWS_PER_CTA, ROWS_PER_CTA, smem, s>>>(
-          W, rows, n, b0, B, U, hw, tab, lost, nib, rungs, scales, E);
+          W, rows, n, b0, B, U, hw, tab, lost, nib, rungs, scales, E_hi, E_lo);
       GQ_LAUNCHED();
     }
     if (b1 < n) {
       {
         GQ_PROF(K_PREP_UT, s);
         dim3 grid((n - b1 + 31) / 32, SB / 32);
-        k_prep_ut<<<grid, dim3(32, 8), 0, s>>>(U, n, b0, b1, Ut);
+        k_prep_ut<<<grid, dim3(32, 8), 0, s>>>(U, n, b0, b1, Ut_hi, Ut_lo);
         GQ_LAUNCHED();
       }
-      GQ_TRY(gemm_sub(gemm_rect(W + b1, n, E, SB, Ut, SB, rows, n - b1), none, SB, nullptr,
-                      K_SWEEP_GEMM, s));
+      GQ_TRY(gemm_tc_sub(maps, tc_rect(W + b1, n, 2, 0, 0, 0, rows, n - b1), none, SB, status,
+                         status, K_SWEEP_GEMM, s));
     }
   }
-  return GPTQ_OK;
+  unsigned hs = 0;
+  GQ_CUDA(cudaMemcpyAsync(&hs, status, sizeof(unsigned), cudaMemcpyDeviceToHost, s));
+  GQ_CUDA(cudaStreamSynchronize(s));
+  return hs ? GPTQ_ERR_TIMEOUT : GPTQ_OK;
 }
 
 }  // namespace gq
