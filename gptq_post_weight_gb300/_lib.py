@@ -26,6 +26,7 @@ SIGNATURES = {
     "gptq_sweep_workspace_bytes": (_S, [_I, _I]),
     "gptq_q4tp_sweep": (_I, [_P, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _S, _P]),
     "gptq_q4tp_group": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "gptq_q4tp_sweep_noalloc": (_I, [_P, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P]),
     "gptq_group_workspace_bytes": (_S, [_I, _I]),
     "gptq_quantize_group": (_I, [_P, _I, _D, _P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _S, _P]),
     "gptq_build_equilibrated": (_I, [_P, _I, _D, _P, _P, _P, _S, _P]),
@@ -158,6 +159,23 @@ def q4tp_sweep(w, u, hw, tab, lost, ws=None, out=None, stream=None):
                                _ptr(nib), _ptr(rungs), _ptr(scales), _ptr(ws), ws.numel(),
                                _stream(torch, stream))
     _check("gptq_q4tp_sweep", code)
+    return nib, rungs, scales
+
+
+def q4tp_sweep_noalloc(w, u, hw, tab, lost, out=None, stream=None):
+    """gptq_q4tp_sweep_noalloc: the sweep with the library's own static
+    scratch instead of a workspace (for callers that cannot allocate device
+    memory).  Returns (nibbles, rungs, scales); W is consumed in place."""
+    import torch
+
+    lib = load()
+    for t, nm in ((w, "w"), (u, "u"), (hw, "hw"), (tab, "tab"), (lost, "lost")):
+        _cuda_f32(t, nm)
+    rows, n = w.shape
+    nib, rungs, scales = out if out is not None else _outs(torch, rows, n, w.device)
+    code = lib.gptq_q4tp_sweep_noalloc(_ptr(w), rows, n, _ptr(u), _ptr(hw), _ptr(tab), _ptr(lost),
+                                       _ptr(nib), _ptr(rungs), _ptr(scales), _stream(torch, stream))
+    _check("gptq_q4tp_sweep_noalloc", code)
     return nib, rungs, scales
 
 

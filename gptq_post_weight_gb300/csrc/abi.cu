@@ -21,6 +21,7 @@ gptq_status copy_dead_zeroed(const float* W, int rows, int n, const float* hdiag
 gptq_status sweep_run(float* W, int rows, int n, const float* U, const float* hw, const float* tab,
                       const float* lost, uint8_t* nib, uint8_t* rungs, float* scales, void* ws,
                       size_t ws_bytes, cudaStream_t s);
+gptq_status noalloc_scratch(void** out);
 }  // namespace gq
 
 using namespace gq;
@@ -111,6 +112,20 @@ gptq_status gptq_q4tp_sweep(float* W, int rows, int n, const float* U, const flo
   if (ws_bytes < sweep_ws_bytes(rows, n)) return GPTQ_ERR_NOMEM;
   return sweep_run(W, rows, n, U, hw, tab, lost, nibbles, rungs, scales, ws, ws_bytes,
                    as_stream(stream));
+}
+
+gptq_status gptq_q4tp_sweep_noalloc(float* W, int rows, int n, const float* U, const float* hw,
+                                    const float* tab, const float* lost, uint8_t* nibbles,
+                                    uint8_t* rungs, float* scales, void* stream) {
+  if (bad_n(n) || bad_rows(rows) || n % GPTQ_GROUP != 0) return GPTQ_ERR_SHAPE;
+  if (!ptr_ok(W) || !ptr_ok(U) || !ptr_ok(hw) || !ptr_ok(tab) || !ptr_ok(lost) ||
+      !ptr_ok(nibbles) || rungs == nullptr || !ptr_ok(scales))
+    return GPTQ_ERR_ARG;
+  if (sweep_ws_bytes(rows, n) > (size_t)GPTQ_SWEEP_NOALLOC_SCRATCH_BYTES) return GPTQ_ERR_NOMEM;
+  void* scratch = nullptr;
+  GQ_TRY(noalloc_scratch(&scratch));
+  return sweep_run(W, rows, n, U, hw, tab, lost, nibbles, rungs, scales, scratch,
+                   (size_t)GPTQ_SWEEP_NOALLOC_SCRATCH_BYTES, as_stream(stream));
 }
 
 gptq_status gptq_quantize_group(const float* H_packed, int n, double lambda, const float* W,

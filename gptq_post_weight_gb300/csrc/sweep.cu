@@ -17,6 +17,8 @@
 #include <cuda_fp16.h>
 #include <math.h>
 
+#include <mutex>
+
 namespace gq {
 namespace {
 
@@ -322,6 +324,32 @@ gptq_status copy_dead_zeroed(const float* W, int rows, int n, const float* hdiag
   GQ_PROF(K_COPY, s);
   k_copy_dz<<<152 * 8, 256, 0, s>>>(W, total, n, hdiag, out);
   GQ_LAUNCHED();
+  return GPTQ_OK;
+}
+
+// Scratch for gptq_q4tp_sweep_noalloc: a file-scope device array, so that a
+// caller that must not allocate device memory can still run the sweep.  Its
+// host-side name is only a stand-in; the device address comes from
+// cudaGetSymbolAddress, looked up once per device (on that device's first
+// call) and cached.
+namespace {
+__device__ __align__(256) unsigned char g_noalloc_scratch[GPTQ_SWEEP_NOALLOC_SCRATCH_BYTES];
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kMaxDevices] = {};
+}  // namespace
+
+gptq_status noalloc_scratch(void** out) {
+  int dev = 0;
+  GQ_CUDA(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= kMaxDevices) return GPTQ_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return GPTQ_ERR_CUDA;
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
   return GPTQ_OK;
 }
 

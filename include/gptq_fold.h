@@ -144,6 +144,35 @@ gptq_status gptq_q4tp_group(const float* tile, int rows, const float* ublk, cons
                             const float* tab, const float* lost, uint8_t* nibbles,
                             uint8_t* rungs, float* scales, float* E, void* stream);
 
+/*
+ * gptq_q4tp_sweep_noalloc -- gptq_q4tp_sweep for callers that cannot
+ * allocate device memory (no cudaMalloc, no allocator of their own, no
+ * workspace to lend): for example code that runs inside a stream that is
+ * being captured, where an allocation would break the capture, or a plugin
+ * whose host framework owns all device memory and hands it only the input and
+ * output buffers.  The pages have no counterpart; it is a packaging of the
+ * same sweep.
+ *
+ * Arguments, layouts and results are those of gptq_q4tp_sweep, without
+ * ws/ws_bytes.  Scratch lives instead in one file-scope device array of
+ * GPTQ_SWEEP_NOALLOC_SCRATCH_BYTES per GPU, which every GPU that loads the
+ * library holds until the process exits.  It fits shapes with
+ * gptq_sweep_workspace_bytes(rows, n) <= that size (about rows + n <= 24575,
+ * e.g. 5120 rows x 17408 channels); larger shapes return GPTQ_ERR_NOMEM
+ * before any work.  The call allocates nothing.
+ *
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture.  All calls share the one array and it keeps the previous call's
+ * contents (everything that must start at zero is cleared by each call), so
+ * calls whose work overlaps on the GPU -- on different streams, or from
+ * different host threads -- race on it: serialize them.
+ */
+#define GPTQ_SWEEP_NOALLOC_SCRATCH_BYTES (24u << 20)
+gptq_status gptq_q4tp_sweep_noalloc(float* W, int rows, int n, const float* U, const float* hw,
+                                    const float* tab, const float* lost, uint8_t* nibbles,
+                                    uint8_t* rungs, float* scales, void* stream);
+
 /* Workspace bytes gptq_quantize_group needs. */
 size_t gptq_group_workspace_bytes(int rows, int n);
 
