@@ -15,6 +15,7 @@ scaled to seconds per group.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import os
 import statistics
@@ -212,9 +213,9 @@ def main():
     local = int(os.environ.get("LOCAL_RANK", "0"))
     cfg = synth.config(args.config, seed=rank)
     if args.n is not None:
-        cfg = synth.config(args.config, seed=rank, n=args.n, T=2 * args.n, name=f"{args.config}_n{args.n}")
+        cfg = dataclasses.replace(cfg, n=args.n, T=2 * args.n, name=f"{args.config}_n{args.n}")
     if args.rows is not None:
-        cfg = synth.config(args.config, seed=rank, n=cfg.n, T=cfg.T, rows=args.rows, name=cfg.name)
+        cfg = dataclasses.replace(cfg, rows=args.rows)
     if args.impl == "reference":
         run_reference(args, cfg, rank)
         return
@@ -356,7 +357,7 @@ def main():
             "roofline": roof,
             "fold_tflops_algorithmic": fold_flops / (per_kind.get("fold_gemm", {}).get("ms_per_step", 0) / 1e3
                                                      + sum(per_kind.get(k, {}).get("ms_per_step", 0) / 1e3
-                                                           for k in ("build", "potrf", "trsm_panel", "trsm_inv", "diag"))
+                                                           for k in ("build", "potrf", "trsm", "diag"))
                                                      ) / 1e12 if "fold_gemm" in per_kind else None,
             "per_kernel": per_kind,
             "cpu_baseline": cpu,

@@ -37,8 +37,8 @@ constexpr int GROUP = 32;
 
 // Kernel kinds for launch accounting / per-kind timing (gptq_profile_*).
 enum Kind : int {
-  K_DIAG = 0, K_BUILD, K_POTRF, K_TRSM_PANEL, K_TRSM_INV, K_FOLD_GEMM, K_LADDER, K_SWEEP_BLOCK,
-  K_PREP_UT, K_SWEEP_GEMM, K_GROUP, K_COPY, K_NKINDS
+  K_DIAG = 0, K_BUILD, K_POTRF, K_TRSM, K_FOLD_GEMM, K_LADDER, K_SWEEP_BLOCK, K_PREP_UT,
+  K_SWEEP_GEMM, K_GROUP, K_COPY, K_NKINDS
 };
 
 // Every launch site calls prof_begin/prof_end around its <<<>>>: they count
@@ -84,38 +84,44 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 // index contiguous, leading dimension K) and given as TF32 hi/lo pairs
 // through TMA tensor maps: OperandMaps.m[a_map] / m[a_map + 1] hold A_hi /
 // A_lo, likewise for B; operand row = a_row0 + tile row (b_row0 + tile col).
+// C is reached through OperandMaps.c (an f32 tensor map); tile (ti, tj)
+// covers C[c_y0 + 128 ti ..][c_x0 + 128 tj ..], and whatever falls outside
+// the map's extent is not written (that masks ragged edges).
 // mode 0: rectangle of mt x nt tiles; mode 1: lower triangle of an mt x mt
-// tile grid (ti >= tj; inside a diagonal tile only r >= s is written).
-// Rows >= M or columns >= N are masked.
+// tile grid (ti >= tj; inside a diagonal tile only r >= s is changed).
 struct TcJob {
-  float* C;
-  long long ldc;
+  int c_x0, c_y0;
   int a_map, b_map, a_row0, b_row0;
   int mode, mt, nt, M, N, ntiles;
 };
 
 struct OperandMaps {
   CUtensorMap m[4];
+  CUtensorMap c;
 };
 
-inline TcJob tc_rect(float* C, long long ldc, int a_map, int a_row0, int b_map, int b_row0, int M,
+inline TcJob tc_rect(int c_x0, int c_y0, int a_map, int a_row0, int b_map, int b_row0, int M,
                      int N) {
   TcJob j{};
-  j.C = C; j.ldc = ldc; j.a_map = a_map; j.b_map = b_map; j.a_row0 = a_row0; j.b_row0 = b_row0;
-  j.mode = 0; j.M = M; j.N = N;
+  j.c_x0 = c_x0; j.c_y0 = c_y0; j.a_map = a_map; j.b_map = b_map; j.a_row0 = a_row0;
+  j.b_row0 = b_row0; j.mode = 0; j.M = M; j.N = N;
   j.mt = (M + 127) / 128; j.nt = (N + 127) / 128;
   j.ntiles = (M > 0 && N > 0) ? j.mt * j.nt : 0;
   return j;
 }
 
-inline TcJob tc_lower(float* C, long long ldc, int map, int row0, int M) {
+inline TcJob tc_lower(int c_x0, int c_y0, int map, int row0, int M) {
   TcJob j{};
-  j.C = C; j.ldc = ldc; j.a_map = map; j.b_map = map; j.a_row0 = row0; j.b_row0 = row0;
+  j.c_x0 = c_x0; j.c_y0 = c_y0; j.a_map = map; j.b_map = map; j.a_row0 = row0; j.b_row0 = row0;
   j.mode = 1; j.M = M; j.N = M;
   j.mt = (M + 127) / 128; j.nt = j.mt;
   j.ntiles = M > 0 ? j.mt * (j.mt + 1) / 2 : 0;
   return j;
 }
+
+// Tensor map over the f32 matrix C [rows][cols] (leading dimension ld) for
+// the GEMM's reduce-add epilogue (box 32 x 128, 128-byte swizzle).
+gptq_status make_c_map(CUtensorMap* m, float* base, long long rows, long long cols, long long ld);
 
 // Tensor map over a K-major f32 operand array [rows][K] (box 32 x 128,
 // 128-byte swizzle).  K must be a multiple of 32, base 16-byte aligned.

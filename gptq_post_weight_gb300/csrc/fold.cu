@@ -58,111 +58,177 @@ __global__ void __launch_bounds__(1024) k_diag(const float* __restrict__ hp, int
   }
 }
 
+// Per attempt: |d_k| = sqrt(H_kk + damp) (sqrt(1 + damp) for a dead channel;
+// make_u divides by it, the builder never uses it for a dead row/column) and
+// the signed D of the fold page (-sqrt(1 + damp) marks a dead channel).
+__global__ void k_dvec(int n, const float* __restrict__ hdiag, const double* __restrict__ base,
+                       double lam, float* __restrict__ Dsigned, float* __restrict__ dabs) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const double damp = lam * (*base);
+  const float h = hdiag[i];
+  const bool dead = !(h > 0.f);
+  const float d = dead ? -(float)sqrt(1.0 + damp) : (float)sqrt((double)h + damp);
+  if (Dsigned) Dsigned[i] = d;
+  dabs[i] = fabsf(d);
+}
+
 // One row i of A: lower part = equilibrated reversed damped H, upper part
 // zero (initial Y), padding rows identity.  [fold page] build_a.
 __global__ void __launch_bounds__(256) k_build(const float* __restrict__ hp, int n, int N,
                                                const float* __restrict__ hdiag,
                                                const double* __restrict__ base, double lam,
+                                               const float* __restrict__ dabs,
                                                float* __restrict__ A, long long lda,
-                                               float* __restrict__ Dsigned, float* __restrict__ dabs,
                                                int write_upper) {
   const int i = blockIdx.x;
-  const double damp = lam * (*base);
-  const float dampf = (float)damp;
   float* arow = A + (long long)i * lda;
   if (i >= n) {
     for (int j = threadIdx.x; j < N; j += blockDim.x)
       if (write_upper || j <= i) arow[j] = (j == i) ? 1.f : 0.f;
     return;
   }
+  const float dampf = (float)(lam * (*base));
   const int ii = n - 1 - i;
-  const float hii = hdiag[ii];
-  const bool dead_i = !(hii > 0.f);
-  if (threadIdx.x == 0) {
-    float d = dead_i ? -(float)sqrt(1.0 + damp) : (float)sqrt((double)hii + damp);
-    if (Dsigned) Dsigned[ii] = d;
-    dabs[ii] = fabsf(d);
-  }
-  const float di = dead_i ? 1.f : (float)sqrt((double)hii + damp);
+  const bool dead_i = !(hdiag[ii] > 0.f);
+  const float di = dabs[ii];
   const long long prow = poff(ii, n);
-  for (int j = threadIdx.x; j < N; j += blockDim.x) {
+  const int jend = write_upper ? N : i + 1;
+  for (int j = threadIdx.x; j < jend; j += blockDim.x) {
     float v = 0.f;
     if (j <= i) {
       const int jj = n - 1 - j;  // jj >= ii
-      const float hjj = hdiag[jj];
-      const bool dead_j = !(hjj > 0.f);
+      const bool dead_j = !(hdiag[jj] > 0.f);
       if (dead_i || dead_j) {
         v = (ii == jj) ? 1.f : 0.f;
       } else {
         float h = hp[prow + (jj - ii)];
         if (ii == jj) h = __fadd_rn(h, dampf);
-        const float dj = (float)sqrt((double)hjj + damp);
-        v = __fdiv_rn(h, __fmul_rn(di, dj));
+        v = __fdiv_rn(h, __fmul_rn(di, dabs[jj]));
       }
-    } else if (!write_upper) {
-      continue;
     }
     arow[j] = v;
   }
 }
 
-// Cholesky of the NB x NB diagonal block at k (lower), in shared memory:
-// 32-column sub-panels, each factored by one warp, then a triangular solve
-// of the rows below and a rank-32 update, all inside the CTA.  Pivot test of
-// the fold page's chol_diag: !(piv > 0) (NaN included) -> flag, piv := 1.
+// Cholesky of the NB x NB diagonal block at k (lower) in shared memory, in
+// 32-column panels: warp 0 factors the panel's 32 x 32 diagonal block in
+// registers (lane = row, shuffles carry the pivot column), the rows below it
+// are solved against it (one thread per row), then a rank-32 update of the
+// rest of the block (4 x 4 register tiles).  Pivot test of the fold page's
+// chol_diag: !(piv > 0) (NaN included) -> flag, piv := 1.
 // Output: Lkk (NB x NB, zeros above the diagonal).
 __global__ void __launch_bounds__(256) k_potrf(const float* __restrict__ A, long long lda, int k,
                                                float* __restrict__ Lkk, unsigned* flag) {
   if (flagged(flag)) return;
   extern __shared__ float S[];  // [NB][LDS]
+  __shared__ float rinv[32];
   __shared__ int bad;
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   if (tid == 0) bad = 0;
-  for (int e = tid; e < NB * NB; e += 256) {
-    const int r = e / NB, c = e % NB;
-    S[r * LDS + c] = (c <= r) ? A[(long long)(k + r) * lda + k + c] : 0.f;
+  // 16 float4 loads per thread, all in flight before the first store.
+  {
+    float4 v[NB * NB / 4 / 256];
+#pragma unroll
+    for (int i = 0; i < NB * NB / 4 / 256; ++i) {
+      const int e = tid + 256 * i, r = e / (NB / 4), c4 = e % (NB / 4);
+      v[i] = *reinterpret_cast<const float4*>(A + (long long)(k + r) * lda + k + 4 * c4);
+    }
+#pragma unroll
+    for (int i = 0; i < NB * NB / 4 / 256; ++i) {
+      const int e = tid + 256 * i, r = e / (NB / 4), c = 4 * (e % (NB / 4));
+      float* dst = S + r * LDS + c;
+      dst[0] = (c <= r) ? v[i].x : 0.f;
+      dst[1] = (c + 1 <= r) ? v[i].y : 0.f;
+      dst[2] = (c + 2 <= r) ? v[i].z : 0.f;
+      dst[3] = (c + 3 <= r) ? v[i].w : 0.f;
+    }
   }
   __syncthreads();
   for (int p = 0; p < NB; p += 32) {
-    if (tid < 32) {
-      const int lane = tid;
+    if (warp == 0) {
+      float a[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) a[j] = S[(p + lane) * LDS + p + j];
+#pragma unroll
       for (int c = 0; c < 32; ++c) {
-        float piv = S[(p + c) * LDS + p + c];
+        float piv = __shfl_sync(0xffffffffu, a[c], c);
         if (!(piv > 0.f)) {
           piv = 1.f;
           if (lane == 0) bad = 1;
         }
         const float l = sqrtf(piv);
-        __syncwarp();
-        if (lane == c) S[(p + c) * LDS + p + c] = l;
-        if (lane > c) S[(p + lane) * LDS + p + c] = __fdiv_rn(S[(p + lane) * LDS + p + c], l);
-        __syncwarp();
-        if (lane > c) {
-          const float lr = S[(p + lane) * LDS + p + c];
-          for (int s = c + 1; s <= lane; ++s)
-            S[(p + lane) * LDS + p + s] = fmaf(-lr, S[(p + s) * LDS + p + c], S[(p + lane) * LDS + p + s]);
+        if (lane == c) {
+          a[c] = l;
+          rinv[c] = __fdiv_rn(1.f, l);
+        } else if (lane > c) {
+          a[c] = __fdiv_rn(a[c], l);
         }
-        __syncwarp();
+        const float lic = a[c];
+#pragma unroll
+        for (int j = 1; j < 32; ++j) {
+          if (j <= c) continue;
+          const float ljc = __shfl_sync(0xffffffffu, lic, j);
+          if (lane >= j) a[j] = fmaf(-lic, ljc, a[j]);
+        }
       }
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (j <= lane) S[(p + lane) * LDS + p + j] = a[j];
     }
     __syncthreads();
-    for (int r = p + 32 + tid; r < NB; r += 256) {
+    const int r = p + 32 + tid;
+    if (r < NB) {
+      float x[32];
+#pragma unroll
+      for (int t = 0; t < 32; ++t) x[t] = S[r * LDS + p + t];
+#pragma unroll
       for (int t = 0; t < 32; ++t) {
-        float s = S[r * LDS + p + t];
-        for (int u = 0; u < t; ++u) s = fmaf(-S[r * LDS + p + u], S[(p + t) * LDS + p + u], s);
-        S[r * LDS + p + t] = __fdiv_rn(s, S[(p + t) * LDS + p + t]);
+        float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+        for (int u = 0; u + 1 < t; u += 2) {
+          a0 = fmaf(x[u], S[(p + t) * LDS + p + u], a0);
+          a1 = fmaf(x[u + 1], S[(p + t) * LDS + p + u + 1], a1);
+        }
+        if (t & 1) a0 = fmaf(x[t - 1], S[(p + t) * LDS + p + t - 1], a0);
+        x[t] = (x[t] - (a0 + a1)) * rinv[t];
       }
+#pragma unroll
+      for (int t = 0; t < 32; ++t) S[r * LDS + p + t] = x[t];
     }
     __syncthreads();
-    const int m = NB - p - 32;
-    for (int e = tid; e < m * m; e += 256) {
-      const int rr = e / m, ss = e % m;
-      if (ss > rr) continue;
-      const int r = p + 32 + rr, s2 = p + 32 + ss;
-      float acc = 0.f;
+    const int m = NB - p - 32;  // rows/cols of the remaining block
+    const int mt = m / 4;
+    const int ntile = mt * (mt + 1) / 2;
+    for (int e = tid; e < ntile; e += 256) {
+      int ti = (int)((sqrtf(8.0f * (float)e + 1.0f) - 1.0f) * 0.5f);
+      while ((ti + 1) * (ti + 2) / 2 <= e) ++ti;
+      while (ti * (ti + 1) / 2 > e) --ti;
+      const int tj = e - ti * (ti + 1) / 2;
+      const int r0 = p + 32 + 4 * ti, c0 = p + 32 + 4 * tj;
+      float acc[4][4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
 #pragma unroll 8
-      for (int t = 0; t < 32; ++t) acc = fmaf(S[r * LDS + p + t], S[s2 * LDS + p + t], acc);
-      S[r * LDS + s2] -= acc;
+      for (int t = 0; t < 32; ++t) {
+        float ra[4], rb[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          ra[i] = S[(r0 + i) * LDS + p + t];
+          rb[i] = S[(c0 + i) * LDS + p + t];
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(ra[i], rb[j], acc[i][j]);
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (c0 + j <= r0 + i) S[(r0 + i) * LDS + c0 + j] -= acc[i][j];
     }
     __syncthreads();
   }
@@ -173,30 +239,47 @@ __global__ void __launch_bounds__(256) k_potrf(const float* __restrict__ A, long
   }
 }
 
-// Forward substitution L_kk z = v for 128 row vectors per CTA (one thread
-// each, v in registers).  MODE 0 (Cholesky panel, fold page chol_panel):
-// rows i >= k+NB, v = A[i][k..k+NB), z -> P[i][*].  MODE 1 (inverse block
-// row, fold page inv_diag + inv_rows): rows c < k+NB, v = Y[c][k..k+NB)
-// (the unit vector e_{c-k} when c is in block k), z -> Yp[c][*] and the
-// finished entries of U: U[n-1-i][n-1-c] = X[i][c] / |d_{n-1-c}|
-// ([fold page] make_u), i = k + t.  z is stored as its TF32 hi/lo split,
-// the operand format of the update GEMM.
-template <int MODE>
-__global__ void __launch_bounds__(128) k_trsm(const float* __restrict__ A, long long lda, int k,
-                                              int row0, int nrows, const float* __restrict__ Lkk,
-                                              float* __restrict__ out_hi, float* __restrict__ out_lo,
-                                              const unsigned* flag,
-                                              float* __restrict__ U, const float* __restrict__ dabs,
-                                              int n) {
+constexpr int TRSM_ROWS = 64;
+
+// Forward substitutions L_kk z = v, one row vector per thread (v in
+// registers, L_kk in shared memory), for both triangular solves of step k in
+// one launch:
+//  * blocks [0, nb_panel): the Cholesky panel (fold page chol_panel), rows
+//    i >= s0 = k+NB, v = A[i][k..k+NB), z -> P[i][*];
+//  * the remaining blocks: the inverse's block row (fold page inv_diag +
+//    inv_rows), rows c < s0, v = Y[c][k..k+NB) (the unit vector e_{c-k} when
+//    c is in block k), z -> Yp[c][*], and the finished entries of U:
+//    U[n-1-i][n-1-c] = X[i][c] / |d_{n-1-c}| ([fold page] make_u), i = k+t.
+// z is stored as its TF32 hi/lo split, the operand format of the update GEMM.
+// Four partial sums per step shorten the dependent FMA chains.
+__global__ void __launch_bounds__(TRSM_ROWS) k_trsm(const float* __restrict__ A, long long lda, int k,
+                                                    int s0, int nb_panel, int N,
+                                                    const float* __restrict__ Lkk,
+                                                    float* __restrict__ P_hi, float* __restrict__ P_lo,
+                                                    float* __restrict__ Y_hi, float* __restrict__ Y_lo,
+                                                    const unsigned* flag, float* __restrict__ U,
+                                                    const float* __restrict__ dabs, int n) {
   if (flagged(flag)) return;
-  extern __shared__ __align__(16) float Ls[];  // [NB][NB]
-  for (int e = threadIdx.x; e < NB * NB / 4; e += 128)
-    reinterpret_cast<float4*>(Ls)[e] = reinterpret_cast<const float4*>(Lkk)[e];
+  extern __shared__ __align__(16) float Ls[];  // [NB][NB], then rinv[NB]
+  float* rinv = Ls + NB * NB;
+  // 64 float4 loads per thread, issued in batches of 16.
+#pragma unroll 1
+  for (int b0 = 0; b0 < NB * NB / 4; b0 += 16 * TRSM_ROWS) {
+    float4 v[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = reinterpret_cast<const float4*>(Lkk)[b0 + threadIdx.x + i * TRSM_ROWS];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) reinterpret_cast<float4*>(Ls)[b0 + threadIdx.x + i * TRSM_ROWS] = v[i];
+  }
   __syncthreads();
-  const int r = row0 + blockIdx.x * 128 + threadIdx.x;
-  if (r >= row0 + nrows) return;
+  for (int t = threadIdx.x; t < NB; t += TRSM_ROWS) rinv[t] = __fdiv_rn(1.f, Ls[t * NB + t]);
+  __syncthreads();
+  const bool panel = (int)blockIdx.x < nb_panel;
+  const int r = panel ? s0 + blockIdx.x * TRSM_ROWS + threadIdx.x
+                      : (blockIdx.x - nb_panel) * TRSM_ROWS + threadIdx.x;
+  if (r >= (panel ? N : s0)) return;
   float x[NB];
-  const int unit = (MODE == 1 && r >= k) ? r - k : -1;
+  const int unit = (!panel && r >= k) ? r - k : -1;
   if (unit >= 0) {
 #pragma unroll
     for (int t = 0; t < NB; ++t) x[t] = (t == unit) ? 1.f : 0.f;
@@ -210,27 +293,27 @@ __global__ void __launch_bounds__(128) k_trsm(const float* __restrict__ A, long 
   }
 #pragma unroll
   for (int t = 0; t < NB; ++t) {
-    float s = x[t];
     const float4* lrow = reinterpret_cast<const float4*>(Ls + t * NB);
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
     for (int u4 = 0; u4 < t / 4; ++u4) {
-      float4 l = lrow[u4];
-      s = fmaf(-l.x, x[4 * u4], s);
-      s = fmaf(-l.y, x[4 * u4 + 1], s);
-      s = fmaf(-l.z, x[4 * u4 + 2], s);
-      s = fmaf(-l.w, x[4 * u4 + 3], s);
+      const float4 l = lrow[u4];
+      a0 = fmaf(l.x, x[4 * u4], a0);
+      a1 = fmaf(l.y, x[4 * u4 + 1], a1);
+      a2 = fmaf(l.z, x[4 * u4 + 2], a2);
+      a3 = fmaf(l.w, x[4 * u4 + 3], a3);
     }
 #pragma unroll
-    for (int u = (t / 4) * 4; u < t; ++u) s = fmaf(-Ls[t * NB + u], x[u], s);
-    x[t] = __fdiv_rn(s, Ls[t * NB + t]);
+    for (int u = (t / 4) * 4; u < t; ++u) a0 = fmaf(Ls[t * NB + u], x[u], a0);
+    x[t] = (x[t] - ((a0 + a1) + (a2 + a3))) * rinv[t];
   }
   if (unit >= 0) {
 #pragma unroll
     for (int t = 0; t < NB; ++t)
       if (t < unit) x[t] = 0.f;
   }
-  float4* dh = reinterpret_cast<float4*>(out_hi + (long long)r * NB);
-  float4* dl = reinterpret_cast<float4*>(out_lo + (long long)r * NB);
+  float4* dh = reinterpret_cast<float4*>((panel ? P_hi : Y_hi) + (long long)r * NB);
+  float4* dl = reinterpret_cast<float4*>((panel ? P_lo : Y_lo) + (long long)r * NB);
 #pragma unroll
   for (int t = 0; t < NB / 4; ++t) {
     float4 h, l;
@@ -241,7 +324,7 @@ __global__ void __launch_bounds__(128) k_trsm(const float* __restrict__ A, long 
     dh[t] = h;
     dl[t] = l;
   }
-  if (MODE == 1 && r < n) {
+  if (!panel && r < n) {
     const int m = n - 1 - r;
     const float dm = dabs[m];
 #pragma unroll
@@ -296,8 +379,7 @@ static gptq_status init_attrs() {
   static bool done = false;
   if (done) return GPTQ_OK;
   GQ_CUDA(cudaFuncSetAttribute(k_potrf, cudaFuncAttributeMaxDynamicSharedMemorySize, NB * LDS * 4));
-  GQ_CUDA(cudaFuncSetAttribute(k_trsm<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, NB * NB * 4));
-  GQ_CUDA(cudaFuncSetAttribute(k_trsm<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, NB * NB * 4));
+  GQ_CUDA(cudaFuncSetAttribute(k_trsm, cudaFuncAttributeMaxDynamicSharedMemorySize, (NB * NB + NB) * 4));
   done = true;
   return GPTQ_OK;
 }
@@ -311,7 +393,9 @@ static gptq_status fold_attempt(const float* hp, const FoldWs& w, const OperandM
   GQ_CUDA(cudaMemsetAsync(w.flag, 0, sizeof(unsigned), s));
   {
     GQ_PROF(K_BUILD, s);
-    k_build<<<N, 256, 0, s>>>(hp, n, N, w.hdiag, w.base, lam, w.A, ld, D, w.dabs, 1);
+    k_dvec<<<(n + 255) / 256, 256, 0, s>>>(n, w.hdiag, w.base, lam, D, w.dabs);
+    GQ_LAUNCHED();
+    k_build<<<N, 256, 0, s>>>(hp, n, N, w.hdiag, w.base, lam, w.dabs, w.A, ld, 1);
     GQ_LAUNCHED();
   }
   for (int k = 0; k < N; k += NB) {
@@ -321,22 +405,18 @@ static gptq_status fold_attempt(const float* hp, const FoldWs& w, const OperandM
       k_potrf<<<1, 256, NB * LDS * 4, s>>>(w.A, ld, k, w.Lkk, w.flag);
       GQ_LAUNCHED();
     }
-    if (s0 < N) {
-      GQ_PROF(K_TRSM_PANEL, s);
-      k_trsm<0><<<(N - s0) / 128, 128, NB * NB * 4, s>>>(w.A, ld, k, s0, N - s0, w.Lkk, w.P_hi,
-                                                         w.P_lo, w.flag, nullptr, nullptr, n);
-      GQ_LAUNCHED();
-    }
     {
-      GQ_PROF(K_TRSM_INV, s);
-      k_trsm<1><<<s0 / 128, 128, NB * NB * 4, s>>>(w.A, ld, k, 0, s0, w.Lkk, w.Yp_hi, w.Yp_lo,
-                                                   w.flag, U, w.dabs, n);
+      GQ_PROF(K_TRSM, s);
+      const int nb_panel = (N - s0 + TRSM_ROWS - 1) / TRSM_ROWS;
+      const int nb_inv = (s0 + TRSM_ROWS - 1) / TRSM_ROWS;
+      k_trsm<<<nb_panel + nb_inv, TRSM_ROWS, (NB * NB + NB) * 4, s>>>(
+          w.A, ld, k, s0, nb_panel, N, w.Lkk, w.P_hi, w.P_lo, w.Yp_hi, w.Yp_lo, w.flag, U, w.dabs, n);
       GQ_LAUNCHED();
     }
     if (s0 < N) {
       // maps: 0/1 = P hi/lo, 2/3 = Yp hi/lo.
-      const TcJob syrk = tc_lower(w.A + (long long)s0 * ld + s0, ld, 0, s0, N - s0);
-      const TcJob inv = tc_rect(w.A + s0, ld, 2, 0, 0, s0, s0, N - s0);
+      const TcJob syrk = tc_lower(s0, s0, 0, s0, N - s0);
+      const TcJob inv = tc_rect(s0, 0, 2, 0, 0, s0, s0, N - s0);
       GQ_TRY(gemm_tc_sub(maps, syrk, inv, NB, w.flag, w.flag, K_FOLD_GEMM, s));
     }
   }
@@ -361,6 +441,7 @@ gptq_status fold_run(const float* hp, int n, double lambda, float* U, float* D, 
   GQ_TRY(make_operand_map(&maps.m[1], w.P_lo, w.N, NB));
   GQ_TRY(make_operand_map(&maps.m[2], w.Yp_hi, w.N, NB));
   GQ_TRY(make_operand_map(&maps.m[3], w.Yp_lo, w.N, NB));
+  GQ_TRY(make_c_map(&maps.c, w.A, w.N, w.N, w.N));
   double lam = lambda > 0.0 ? lambda : 0.0;
   for (;;) {
     GQ_TRY(fold_attempt(hp, w, maps, lam, U, D, s));
@@ -388,7 +469,10 @@ gptq_status build_only(const float* hp, int n, double lambda, float* A, float* D
   }
   // Rows of the caller's n x n matrix, lower triangle only.
   GQ_PROF(K_BUILD, s);
-  k_build<<<n, 256, 0, s>>>(hp, n, n, w.hdiag, w.base, lambda > 0 ? lambda : 0.0, A, n, D, w.dabs, 0);
+  const double lam = lambda > 0 ? lambda : 0.0;
+  k_dvec<<<(n + 255) / 256, 256, 0, s>>>(n, w.hdiag, w.base, lam, D, w.dabs);
+  GQ_LAUNCHED();
+  k_build<<<n, 256, 0, s>>>(hp, n, n, w.hdiag, w.base, lam, w.dabs, A, n, 0);
   GQ_LAUNCHED();
   return GPTQ_OK;
 }

@@ -15,8 +15,11 @@
 //               and issues the MMAs from one thread; tcgen05.commit frees a
 //               stage / publishes a finished accumulator;
 //   warps 2-5   epilogue: tcgen05.ld of one accumulator row per thread,
-//               C -= acc in global memory (masked), then release the buffer,
-//               so the epilogue of tile i overlaps the MMAs of tile i+1.
+//               -acc into a 128x32 swizzled staging slice (two, alternating),
+//               then one TMA reduce-add of the slice into C (the L2 does the
+//               read-modify-write, so no SM ever waits on reading C); the
+//               accumulator buffer is released after its last slice, so the
+//               epilogue of tile i overlaps the MMAs of tile i+1.
 // Every wait is bounded (about 2 s of globaltimer); on expiry the kernel
 // stops issuing, drains what it started, frees TMEM and sets bit 1 of the
 // status word.
@@ -32,7 +35,8 @@ constexpr int BM = 128, BN = 128, BK = 32, STAGES = 3;
 constexpr int TILE_A = BM * BK * 4;  // 16 KB
 constexpr int TILE_B = BN * BK * 4;  // 16 KB
 constexpr int STAGE_BYTES = 2 * TILE_A + 2 * TILE_B;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024;
+constexpr int CSLICE = BM * 32 * 4;  // 16 KB: 128 rows x 32 columns of C
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 2 * CSLICE + 1024;
 constexpr int THREADS = 192;
 constexpr uint32_t TMEM_COLS = 2 * BN;
 constexpr unsigned long long WAIT_NS = 2000000000ull;
@@ -100,6 +104,37 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// TMA reduce-add of a 128 x 32 f32 slice (128-byte swizzled in shared
+// memory) into the tensor at (x, y); completion tracked per bulk group.
+__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, uint32_t src, int x, int y) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(x), "r"(y), "r"(src)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read1() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+// Named barrier 1 over the 128 epilogue threads.
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// Same barrier, AND-reducing a predicate over the 128 threads.
+__device__ __forceinline__ bool epi_all(bool p) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred pi, po;\n setp.ne.u32 pi, %1, 0;\n bar.red.and.pred po, 1, 128, pi;\n"
+      " selp.u32 %0, 1, 0, po;\n}\n"
+      : "=r"(r)
+      : "r"((uint32_t)p)
+      : "memory");
+  return r != 0u;
+}
+
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
@@ -165,7 +200,8 @@ __device__ __forceinline__ void tile_of(const TcJob& J, int t, int& ti, int& tj)
 __global__ void __launch_bounds__(THREADS, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap m0, const __grid_constant__ CUtensorMap m1,
               const __grid_constant__ CUtensorMap m2, const __grid_constant__ CUtensorMap m3,
-              TcJob j0, TcJob j1, int K, const unsigned* flag, unsigned* status) {
+              const __grid_constant__ CUtensorMap cmap, TcJob j0, TcJob j1, int K,
+              const unsigned* flag, unsigned* status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ __align__(8) uint64_t full[STAGES], empty[STAGES], tfull[2], tempty[2], drain;
@@ -291,60 +327,55 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   } else {
     const int q = warp & 3;  // TMEM lane quarter this warp may read
-    int acc = 0;
+    const bool leader = threadIdx.x == 64;
+    uint8_t* cstage = smem + STAGES * STAGE_BYTES;
+    int acc = 0, chunk = 0;
     uint32_t aphase = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
-      // Warp-uniform wait: every lane must reach the .sync.aligned loads.
-      const bool ok = __all_sync(0xffffffffu, mbar_wait(&tfull[acc], aphase, abort));
-      if (!ok) break;
+      // All 128 epilogue threads agree before any of them reaches the
+      // .sync.aligned loads or the named barriers below.
+      if (!epi_all(mbar_wait(&tfull[acc], aphase, abort))) break;
       tc_fence_after();
       const bool second = t >= j0.ntiles;
       const TcJob& J = second ? j1 : j0;
       int ti, tj;
       tile_of(J, second ? t - j0.ntiles : t, ti, tj);
       const int rr = q * 32 + lane;  // row inside the tile
-      const int r = ti * BM + rr;
       const bool diag = (J.mode == 1) && (ti == tj);
-      float* crow = J.C + (long long)r * J.ldc + (long long)tj * BN;
       const uint32_t tbase = tmem + (uint32_t)(acc * BN) + ((uint32_t)(q * 32) << 16);
 #pragma unroll 1
       for (int cc = 0; cc < BN; cc += 32) {
-        uint32_t v0[16], v1[16];
-        __syncwarp();
-        tmem_ld16(tbase + (uint32_t)cc, v0);
-        tmem_ld16(tbase + (uint32_t)cc + 16u, v1);
+        uint32_t v[32];
+        tmem_ld16(tbase + (uint32_t)cc, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
+        tmem_ld16(tbase + (uint32_t)cc + 16u, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
         tmem_ld_wait();
-        if (r < J.M) {
-          const int s0 = tj * BN + cc;
-          const bool full_seg = (s0 + 32 <= J.N) && !(diag && cc + 31 > rr);
-          if (full_seg) {
-            float4* p = reinterpret_cast<float4*>(crow + cc);
+        uint8_t* buf = cstage + (chunk & 1) * CSLICE;
+        if (leader) bulk_wait_read1();  // the reduce that last read `buf` is done
+        epi_sync();
+        uint8_t* rowp = buf + rr * 128;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              float4 c = p[i];
-              c.x -= __uint_as_float(v0[4 * i]);
-              c.y -= __uint_as_float(v0[4 * i + 1]);
-              c.z -= __uint_as_float(v0[4 * i + 2]);
-              c.w -= __uint_as_float(v0[4 * i + 3]);
-              p[i] = c;
-            }
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              float4 c = p[4 + i];
-              c.x -= __uint_as_float(v1[4 * i]);
-              c.y -= __uint_as_float(v1[4 * i + 1]);
-              c.z -= __uint_as_float(v1[4 * i + 2]);
-              c.w -= __uint_as_float(v1[4 * i + 3]);
-              p[4 + i] = c;
-            }
-          } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              if (s0 + i < J.N && !(diag && cc + i > rr))
-                crow[cc + i] -= __uint_as_float(i < 16 ? v0[i] : v1[i - 16]);
-            }
+        for (int c4 = 0; c4 < 8; ++c4) {
+          float4 o;
+          o.x = -__uint_as_float(v[4 * c4]);
+          o.y = -__uint_as_float(v[4 * c4 + 1]);
+          o.z = -__uint_as_float(v[4 * c4 + 2]);
+          o.w = -__uint_as_float(v[4 * c4 + 3]);
+          if (diag) {  // lower triangle only: add nothing above the diagonal
+            const int c0 = cc + 4 * c4;
+            if (c0 > rr) o.x = 0.f;
+            if (c0 + 1 > rr) o.y = 0.f;
+            if (c0 + 2 > rr) o.z = 0.f;
+            if (c0 + 3 > rr) o.w = 0.f;
           }
+          *reinterpret_cast<float4*>(rowp + ((c4 ^ (rr & 7)) * 16)) = o;
         }
+        fence_proxy_async_smem();
+        epi_sync();
+        if (leader) {
+          tma_reduce_add_2d(&cmap, smem_u32(buf), J.c_x0 + tj * BN + cc, J.c_y0 + ti * BM);
+          bulk_commit();
+        }
+        ++chunk;
       }
       tc_fence_before();
       mbar_arrive(&tempty[acc]);
@@ -353,6 +384,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         aphase ^= 1u;
       }
     }
+    if (leader) bulk_wait_all();
   }
 
   __syncthreads();
@@ -415,6 +447,20 @@ gptq_status make_operand_map(CUtensorMap* m, const float* base, long long rows, 
   return r == CUDA_SUCCESS ? GPTQ_OK : GPTQ_ERR_CUDA;
 }
 
+gptq_status make_c_map(CUtensorMap* m, float* base, long long rows, long long cols, long long ld) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return GPTQ_ERR_CUDA;
+  if ((reinterpret_cast<uintptr_t>(base) & 15u) != 0 || (ld * 4) % 16 != 0) return GPTQ_ERR_ARG;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)ld * 4u};
+  cuuint32_t box[2] = {32u, (cuuint32_t)BM};
+  cuuint32_t es[2] = {1u, 1u};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? GPTQ_OK : GPTQ_ERR_CUDA;
+}
+
 gptq_status gemm_tc_sub(const OperandMaps& maps, const TcJob& j0, const TcJob& j1, int K,
                         const unsigned* flag, unsigned* status, int kind, cudaStream_t s) {
   static bool attr = false;
@@ -427,8 +473,8 @@ gptq_status gemm_tc_sub(const OperandMaps& maps, const TcJob& j0, const TcJob& j
   if (total <= 0) return GPTQ_OK;
   const int grid = total < num_sms() ? total : num_sms();
   GQ_PROF(kind, s);
-  k_gemm_tc<<<grid, THREADS, SMEM_BYTES, s>>>(maps.m[0], maps.m[1], maps.m[2], maps.m[3], j0, j1, K,
-                                              flag, status);
+  k_gemm_tc<<<grid, THREADS, SMEM_BYTES, s>>>(maps.m[0], maps.m[1], maps.m[2], maps.m[3], maps.c, j0,
+                                              j1, K, flag, status);
   GQ_LAUNCHED();
   return GPTQ_OK;
 }

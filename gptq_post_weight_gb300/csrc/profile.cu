@@ -18,8 +18,8 @@ std::vector<int> g_kind;
 int g_used = 0;
 int g_open = -1;
 
-const char* kNames[K_NKINDS] = {"diag", "build", "potrf", "trsm_panel", "trsm_inv", "fold_gemm",
-                                "ladder", "sweep_block", "prep_ut", "sweep_gemm", "group", "copy"};
+const char* kNames[K_NKINDS] = {"diag", "build", "potrf", "trsm", "fold_gemm", "ladder",
+                                "sweep_block", "prep_ut", "sweep_gemm", "group", "copy"};
 
 }  // namespace
 
