@@ -111,18 +111,24 @@ __global__ void __launch_bounds__(256) k_build(const float* __restrict__ hp, int
   }
 }
 
-// Cholesky of the NB x NB diagonal block at k (lower) in shared memory, in
-// 32-column panels: warp 0 factors the panel's 32 x 32 diagonal block in
-// registers (lane = row, shuffles carry the pivot column), the rows below it
+// Cholesky of the NB x NB diagonal block at k (lower) in shared memory, and
+// its inverse.  Factorization in 32-column panels: warp 0 factors the
+// panel's 32 x 32 diagonal block in registers (lane = row; the pivot column
+// travels by shuffles; reciprocal square root, no divisions), the rows below
 // are solved against it (one thread per row), then a rank-32 update of the
 // rest of the block (4 x 4 register tiles).  Pivot test of the fold page's
 // chol_diag: !(piv > 0) (NaN included) -> flag, piv := 1.
-// Output: Lkk (NB x NB, zeros above the diagonal).
+// Inverse ([fold page] inv_diag, blocked): the four 32 x 32 diagonal blocks
+// are inverted by four warps (lane = column), then the off-diagonal blocks
+// by block diagonals: X_ij = -X_ii sum_{j <= m < i} L_im X_mj.
+// Output: Linv (NB x NB, zeros above the diagonal).
 __global__ void __launch_bounds__(256) k_potrf(const float* __restrict__ A, long long lda, int k,
-                                               float* __restrict__ Lkk, unsigned* flag) {
+                                               float* __restrict__ Linv, unsigned* flag) {
   if (flagged(flag)) return;
-  extern __shared__ float S[];  // [NB][LDS]
-  __shared__ float rinv[32];
+  extern __shared__ float S[];  // [NB][LDS] L, then [NB][LDS] Linv, then T [NB][LDS]
+  float* Li = S + NB * LDS;
+  float* T = Li + NB * LDS;
+  __shared__ float rinv[NB];
   __shared__ int bad;
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   if (tid == 0) bad = 0;
@@ -157,14 +163,10 @@ __global__ void __launch_bounds__(256) k_potrf(const float* __restrict__ A, long
           piv = 1.f;
           if (lane == 0) bad = 1;
         }
-        const float l = sqrtf(piv);
-        if (lane == c) {
-          a[c] = l;
-          rinv[c] = __fdiv_rn(1.f, l);
-        } else if (lane > c) {
-          a[c] = __fdiv_rn(a[c], l);
-        }
-        const float lic = a[c];
+        const float rs = rsqrtf(piv);
+        const float lic = (lane == c) ? piv * rs : a[c] * rs;
+        if (lane >= c) a[c] = lic;
+        if (lane == c) rinv[p + c] = rs;
 #pragma unroll
         for (int j = 1; j < 32; ++j) {
           if (j <= c) continue;
@@ -191,7 +193,7 @@ __global__ void __launch_bounds__(256) k_potrf(const float* __restrict__ A, long
           a1 = fmaf(x[u + 1], S[(p + t) * LDS + p + u + 1], a1);
         }
         if (t & 1) a0 = fmaf(x[t - 1], S[(p + t) * LDS + p + t - 1], a0);
-        x[t] = (x[t] - (a0 + a1)) * rinv[t];
+        x[t] = (x[t] - (a0 + a1)) * rinv[p + t];
       }
 #pragma unroll
       for (int t = 0; t < 32; ++t) S[r * LDS + p + t] = x[t];
@@ -233,94 +235,147 @@ __global__ void __launch_bounds__(256) k_potrf(const float* __restrict__ A, long
     __syncthreads();
   }
   if (bad && tid == 0) atomicOr(flag, 1u);
+  // Inverse.  Diagonal blocks: warp b, lane j = column j of inv(L_bb).
+  for (int e = tid; e < NB * LDS; e += 256) Li[e] = 0.f;
+  __syncthreads();
+  if (warp < 4) {
+    const int b = warp * 32;
+    float x[32];
+#pragma unroll
+    for (int t = 0; t < 32; ++t) {
+      float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+      for (int u = 0; u + 1 < t; u += 2) {
+        a0 = fmaf(S[(b + t) * LDS + b + u], x[u], a0);
+        a1 = fmaf(S[(b + t) * LDS + b + u + 1], x[u + 1], a1);
+      }
+      if (t & 1) a0 = fmaf(S[(b + t) * LDS + b + t - 1], x[t - 1], a0);
+      x[t] = (((t == lane) ? 1.f : 0.f) - (a0 + a1)) * rinv[b + t];
+    }
+#pragma unroll
+    for (int t = 0; t < 32; ++t)
+      if (t >= lane) Li[(b + t) * LDS + b + lane] = x[t];
+  }
+  __syncthreads();
+  // Off-diagonal blocks, one block diagonal d at a time.  Each of the
+  // (4 - d) blocks has 32 x 32 outputs; thread (blk, 4 outputs).
+  for (int d = 1; d < 4; ++d) {
+    const int nblk = 4 - d;
+    // T_ij = sum_{m = j}^{i-1} L_im X_mj  (block rows i = j + d)
+    for (int o = tid; o < nblk * 1024; o += 256) {
+      const int blk = o / 1024, rr = (o % 1024) / 32, cc = o % 32;
+      const int j = blk, i = blk + d;
+      float acc = 0.f;
+      for (int mm = j * 32; mm < i * 32; ++mm) acc = fmaf(S[(i * 32 + rr) * LDS + mm], Li[mm * LDS + j * 32 + cc], acc);
+      T[(i * 32 + rr) * LDS + j * 32 + cc] = acc;
+    }
+    __syncthreads();
+    // X_ij = -X_ii T_ij
+    for (int o = tid; o < nblk * 1024; o += 256) {
+      const int blk = o / 1024, rr = (o % 1024) / 32, cc = o % 32;
+      const int j = blk, i = blk + d;
+      float acc = 0.f;
+#pragma unroll 8
+      for (int u = 0; u <= rr; ++u) acc = fmaf(Li[(i * 32 + rr) * LDS + i * 32 + u], T[(i * 32 + u) * LDS + j * 32 + cc], acc);
+      Li[(i * 32 + rr) * LDS + j * 32 + cc] = -acc;
+    }
+    __syncthreads();
+  }
   for (int e = tid; e < NB * NB; e += 256) {
     const int r = e / NB, c = e % NB;
-    Lkk[e] = (c <= r) ? S[r * LDS + c] : 0.f;
+    Linv[e] = (c <= r) ? Li[r * LDS + c] : 0.f;
   }
 }
 
-constexpr int TRSM_ROWS = 64;
+constexpr int APPLY_ROWS = 64;
 
-// Forward substitutions L_kk z = v, one row vector per thread (v in
-// registers, L_kk in shared memory), for both triangular solves of step k in
-// one launch:
-//  * blocks [0, nb_panel): the Cholesky panel (fold page chol_panel), rows
-//    i >= s0 = k+NB, v = A[i][k..k+NB), z -> P[i][*];
-//  * the remaining blocks: the inverse's block row (fold page inv_diag +
-//    inv_rows), rows c < s0, v = Y[c][k..k+NB) (the unit vector e_{c-k} when
-//    c is in block k), z -> Yp[c][*], and the finished entries of U:
+// Both triangular solves of step k as one product with the explicit inverse:
+// z = L_kk^-1 v for every row vector v, i.e. Z = V Linv^T, four threads per
+// row (thread q computes z[32q .. 32q+32) with 32 independent sums):
+//  * rows i >= s0 = k+NB: the Cholesky panel (fold page chol_panel),
+//    v = A[i][k..k+NB), z -> P[i][*];
+//  * rows c < s0: the inverse's block row (fold page inv_rows), v =
+//    Y[c][k..k+NB) (the unit vector e_{c-k} when c is in block k, so that row
+//    of Z is a column of Linv), z -> Yp[c][*], and the finished entries of U:
 //    U[n-1-i][n-1-c] = X[i][c] / |d_{n-1-c}| ([fold page] make_u), i = k+t.
 // z is stored as its TF32 hi/lo split, the operand format of the update GEMM.
-// Four partial sums per step shorten the dependent FMA chains.
-__global__ void __launch_bounds__(TRSM_ROWS) k_trsm(const float* __restrict__ A, long long lda, int k,
-                                                    int s0, int nb_panel, int N,
-                                                    const float* __restrict__ Lkk,
-                                                    float* __restrict__ P_hi, float* __restrict__ P_lo,
-                                                    float* __restrict__ Y_hi, float* __restrict__ Y_lo,
-                                                    const unsigned* flag, float* __restrict__ U,
-                                                    const float* __restrict__ dabs, int n) {
+__global__ void __launch_bounds__(APPLY_ROWS * 4) k_apply(const float* __restrict__ A, long long lda,
+                                                         int k, int s0, int N,
+                                                         const float* __restrict__ Linv,
+                                                         float* __restrict__ P_hi, float* __restrict__ P_lo,
+                                                         float* __restrict__ Y_hi, float* __restrict__ Y_lo,
+                                                         const unsigned* flag, float* __restrict__ U,
+                                                         const float* __restrict__ dabs, int n) {
   if (flagged(flag)) return;
-  extern __shared__ __align__(16) float Ls[];  // [NB][NB], then rinv[NB]
-  float* rinv = Ls + NB * NB;
-  // 64 float4 loads per thread, issued in batches of 16.
+  extern __shared__ __align__(16) float sm[];
+  float* Ls = sm;                  // [NB][NB] Linv
+  float* Vs = Ls + NB * NB;        // [APPLY_ROWS][NB + 4]
+  constexpr int LV = NB + 4;
+  const int tid = threadIdx.x;
+  const int r0 = blockIdx.x * APPLY_ROWS;
 #pragma unroll 1
-  for (int b0 = 0; b0 < NB * NB / 4; b0 += 16 * TRSM_ROWS) {
+  for (int b0 = 0; b0 < NB * NB / 4; b0 += 16 * APPLY_ROWS * 4) {
     float4 v[16];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = reinterpret_cast<const float4*>(Lkk)[b0 + threadIdx.x + i * TRSM_ROWS];
+    for (int i = 0; i < 16; ++i) v[i] = reinterpret_cast<const float4*>(Linv)[b0 + tid + i * APPLY_ROWS * 4];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) reinterpret_cast<float4*>(Ls)[b0 + threadIdx.x + i * TRSM_ROWS] = v[i];
+    for (int i = 0; i < 16; ++i) reinterpret_cast<float4*>(Ls)[b0 + tid + i * APPLY_ROWS * 4] = v[i];
   }
-  __syncthreads();
-  for (int t = threadIdx.x; t < NB; t += TRSM_ROWS) rinv[t] = __fdiv_rn(1.f, Ls[t * NB + t]);
-  __syncthreads();
-  const bool panel = (int)blockIdx.x < nb_panel;
-  const int r = panel ? s0 + blockIdx.x * TRSM_ROWS + threadIdx.x
-                      : (blockIdx.x - nb_panel) * TRSM_ROWS + threadIdx.x;
-  if (r >= (panel ? N : s0)) return;
-  float x[NB];
-  const int unit = (!panel && r >= k) ? r - k : -1;
-  if (unit >= 0) {
+  {
+    // Row vectors: 64 rows x 32 float4, 8 per thread.
+    float4 v[8];
 #pragma unroll
-    for (int t = 0; t < NB; ++t) x[t] = (t == unit) ? 1.f : 0.f;
-  } else {
-    const float4* src = reinterpret_cast<const float4*>(A + (long long)r * lda + k);
-#pragma unroll
-    for (int t = 0; t < NB / 4; ++t) {
-      float4 v = src[t];
-      x[4 * t] = v.x; x[4 * t + 1] = v.y; x[4 * t + 2] = v.z; x[4 * t + 3] = v.w;
-    }
-  }
-#pragma unroll
-  for (int t = 0; t < NB; ++t) {
-    const float4* lrow = reinterpret_cast<const float4*>(Ls + t * NB);
-    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-#pragma unroll
-    for (int u4 = 0; u4 < t / 4; ++u4) {
-      const float4 l = lrow[u4];
-      a0 = fmaf(l.x, x[4 * u4], a0);
-      a1 = fmaf(l.y, x[4 * u4 + 1], a1);
-      a2 = fmaf(l.z, x[4 * u4 + 2], a2);
-      a3 = fmaf(l.w, x[4 * u4 + 3], a3);
+    for (int i = 0; i < 8; ++i) {
+      const int e = tid + i * APPLY_ROWS * 4, rr = e / (NB / 4), c4 = e % (NB / 4);
+      const int r = r0 + rr;
+      float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (r < N) {
+        if (r >= k && r < s0) {
+          const int u = r - k;
+          x.x = (4 * c4 == u) ? 1.f : 0.f;
+          x.y = (4 * c4 + 1 == u) ? 1.f : 0.f;
+          x.z = (4 * c4 + 2 == u) ? 1.f : 0.f;
+          x.w = (4 * c4 + 3 == u) ? 1.f : 0.f;
+        } else {
+          x = *reinterpret_cast<const float4*>(A + (long long)r * lda + k + 4 * c4);
+        }
+      }
+      v[i] = x;
     }
 #pragma unroll
-    for (int u = (t / 4) * 4; u < t; ++u) a0 = fmaf(Ls[t * NB + u], x[u], a0);
-    x[t] = (x[t] - ((a0 + a1) + (a2 + a3))) * rinv[t];
+    for (int i = 0; i < 8; ++i) {
+      const int e = tid + i * APPLY_ROWS * 4, rr = e / (NB / 4), c4 = e % (NB / 4);
+      *reinterpret_cast<float4*>(Vs + rr * LV + 4 * c4) = v[i];
+    }
   }
-  if (unit >= 0) {
+  __syncthreads();
+  const int rr = tid % APPLY_ROWS, q = tid / APPLY_ROWS;  // q: which 32 outputs
+  const int r = r0 + rr;
+  if (r >= N) return;
+  float acc[32];
 #pragma unroll
-    for (int t = 0; t < NB; ++t)
-      if (t < unit) x[t] = 0.f;
+  for (int t = 0; t < 32; ++t) acc[t] = 0.f;
+  const float* vrow = Vs + rr * LV;
+  const float* lrow = Ls + (q * 32) * NB;
+#pragma unroll 2
+  for (int u4 = 0; u4 < NB / 4; ++u4) {
+    const float4 v = *reinterpret_cast<const float4*>(vrow + 4 * u4);
+#pragma unroll
+    for (int t = 0; t < 32; ++t) {
+      const float4 l = *reinterpret_cast<const float4*>(lrow + t * NB + 4 * u4);
+      acc[t] = fmaf(l.x, v.x, fmaf(l.y, v.y, fmaf(l.z, v.z, fmaf(l.w, v.w, acc[t]))));
+    }
   }
-  float4* dh = reinterpret_cast<float4*>((panel ? P_hi : Y_hi) + (long long)r * NB);
-  float4* dl = reinterpret_cast<float4*>((panel ? P_lo : Y_lo) + (long long)r * NB);
+  const bool panel = r >= s0;
+  float4* dh = reinterpret_cast<float4*>((panel ? P_hi : Y_hi) + (long long)r * NB + q * 32);
+  float4* dl = reinterpret_cast<float4*>((panel ? P_lo : Y_lo) + (long long)r * NB + q * 32);
 #pragma unroll
-  for (int t = 0; t < NB / 4; ++t) {
+  for (int t = 0; t < 8; ++t) {
     float4 h, l;
-    split_tf32(x[4 * t], h.x, l.x);
-    split_tf32(x[4 * t + 1], h.y, l.y);
-    split_tf32(x[4 * t + 2], h.z, l.z);
-    split_tf32(x[4 * t + 3], h.w, l.w);
+    split_tf32(acc[4 * t], h.x, l.x);
+    split_tf32(acc[4 * t + 1], h.y, l.y);
+    split_tf32(acc[4 * t + 2], h.z, l.z);
+    split_tf32(acc[4 * t + 3], h.w, l.w);
     dh[t] = h;
     dl[t] = l;
   }
@@ -328,9 +383,9 @@ __global__ void __launch_bounds__(TRSM_ROWS) k_trsm(const float* __restrict__ A,
     const int m = n - 1 - r;
     const float dm = dabs[m];
 #pragma unroll
-    for (int t = 0; t < NB; ++t) {
-      const int i = k + t;
-      if (i < n) U[(long long)(n - 1 - i) * n + m] = __fdiv_rn(x[t], dm);
+    for (int t = 0; t < 32; ++t) {
+      const int i = k + q * 32 + t;
+      if (i < n) U[(long long)(n - 1 - i) * n + m] = __fdiv_rn(acc[t], dm);
     }
   }
 }
@@ -344,7 +399,7 @@ struct FoldWs {
   float* P_lo;
   float* Yp_hi;   // N x NB   (Y panel of the current step, TF32 hi/lo)
   float* Yp_lo;
-  float* Lkk;     // NB x NB
+  float* Lkk;     // NB x NB: inverse of the current diagonal block of L
   float* hdiag;   // n
   float* dabs;    // n
   double* base;   // 1
@@ -375,11 +430,14 @@ size_t fold_ws_bytes(int n) {
   return c.off + 256;
 }
 
+constexpr int POTRF_SMEM = 3 * NB * LDS * 4;
+constexpr int APPLY_SMEM = (NB * NB + APPLY_ROWS * (NB + 4)) * 4;
+
 static gptq_status init_attrs() {
   static bool done = false;
   if (done) return GPTQ_OK;
-  GQ_CUDA(cudaFuncSetAttribute(k_potrf, cudaFuncAttributeMaxDynamicSharedMemorySize, NB * LDS * 4));
-  GQ_CUDA(cudaFuncSetAttribute(k_trsm, cudaFuncAttributeMaxDynamicSharedMemorySize, (NB * NB + NB) * 4));
+  GQ_CUDA(cudaFuncSetAttribute(k_potrf, cudaFuncAttributeMaxDynamicSharedMemorySize, POTRF_SMEM));
+  GQ_CUDA(cudaFuncSetAttribute(k_apply, cudaFuncAttributeMaxDynamicSharedMemorySize, APPLY_SMEM));
   done = true;
   return GPTQ_OK;
 }
@@ -402,15 +460,14 @@ static gptq_status fold_attempt(const float* hp, const FoldWs& w, const OperandM
     const int s0 = k + NB;
     {
       GQ_PROF(K_POTRF, s);
-      k_potrf<<<1, 256, NB * LDS * 4, s>>>(w.A, ld, k, w.Lkk, w.flag);
+      k_potrf<<<1, 256, POTRF_SMEM, s>>>(w.A, ld, k, w.Lkk, w.flag);
       GQ_LAUNCHED();
     }
     {
       GQ_PROF(K_TRSM, s);
-      const int nb_panel = (N - s0 + TRSM_ROWS - 1) / TRSM_ROWS;
-      const int nb_inv = (s0 + TRSM_ROWS - 1) / TRSM_ROWS;
-      k_trsm<<<nb_panel + nb_inv, TRSM_ROWS, (NB * NB + NB) * 4, s>>>(
-          w.A, ld, k, s0, nb_panel, N, w.Lkk, w.P_hi, w.P_lo, w.Yp_hi, w.Yp_lo, w.flag, U, w.dabs, n);
+      k_apply<<<N / APPLY_ROWS, APPLY_ROWS * 4, APPLY_SMEM, s>>>(w.A, ld, k, s0, N, w.Lkk, w.P_hi,
+                                                                 w.P_lo, w.Yp_hi, w.Yp_lo, w.flag,
+                                                                 U, w.dabs, n);
       GQ_LAUNCHED();
     }
     if (s0 < N) {

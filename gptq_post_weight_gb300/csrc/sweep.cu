@@ -23,33 +23,23 @@ namespace gq {
 namespace {
 
 // The rung / rounding rule of one (row, group) tile ([fold page] q4tp_group;
-// [host page] gptq_quantize_q4tp), one warp per row:
+// [host page] gptq_quantize_q4tp), one thread per row:
 //  * nominal = clamp(round_half_away((log2(amax/7) - lo) / step), 0, 31)
 //    (0 if amax == 0 or step <= 0; log2 = the f64 value rounded to f32);
 //  * rung = best of nominal-2..min(nominal+1, 31) by sum_t hw_t (w_t - q_t s)^2
-//    with q_t = clamp(rne(w_t * (1/s)), -8, 7), strict '<', s <= 0 skipped;
+//    with q_t = clamp(rne(w_t * (1/s)), -8, 7), summed in column order,
+//    strict '<' over ascending rungs, rungs with s <= 0 skipped;
 //  * per column j: q_j = clamp(rne(w_j / s), -8, 7) (0 if s <= 0), nibble
 //    q_j + 8, e_j = (w_j - q_j s) / U_jj (0 if U_jj <= 0), w_t -= e_j U_jt
 //    for t > j.
 // One rounding per operation (no contraction), so the f32 results are the
-// pages' bit for bit.
-// Lane t holds column t of the group.  Every floating-point step is taken in
-// the pages' order: the
-// candidate errors are summed sequentially over t (the terms are gathered by
-// shuffles in column order), and the feedback is applied column by column.
-// `wl` holds this lane's value of the group; `wlater[k]` its values of the
-// later groups in the same block (nl of them), which get the same per-column
-// update w -= e_j U[j][c] (one rounding for the product, one for the
-// difference), as the host page's full-row update does.  Returns the rung;
-// q, e are this lane's code and residual.
-template <int NLATER>
-__device__ __forceinline__ int q4tp_group_warp(float& wl, float (&wlater)[NLATER], int nl,
-                                               float hwl, const float* tabrow, float lo, float st,
-                                               const float* U, int ldu, int lane, float& s_out,
-                                               float& q_out, float& e_out) {
-  float amax = fabsf(wl);
+// pages' bit for bit.  The up to four candidate rungs are evaluated side by
+// side (independent sums), which changes no result.
+__device__ __forceinline__ int q4tp_pick(const float (&w)[GROUP], const float* hw,
+                                         const float* tabrow, float lo, float st) {
+  float amax = 0.f;
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  for (int t = 0; t < GROUP; ++t) amax = fmaxf(amax, fabsf(w[t]));
   int nominal = 0;
   if (amax > 0.f && st > 0.f) {
     const float x = __fdiv_rn(amax, 7.0f);
@@ -61,23 +51,25 @@ __device__ __forceinline__ int q4tp_group_warp(float& wl, float (&wlater)[NLATER
   if (amax > 0.f) {
     const int lo_c = nominal >= 2 ? nominal - 2 : 0;
     const int hi_c = nominal + 1 < 31 ? nominal + 1 : 31;
-    float term[4], err[4];
+    float sc[4], iv[4], err[4];
     bool valid[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const int cand = lo_c + k;
-      const float sc = cand <= hi_c ? tabrow[cand] : 0.f;
-      valid[k] = cand <= hi_c && sc > 0.f;
-      const float iv = __fdiv_rn(1.0f, valid[k] ? sc : 1.f);
-      const float q = fminf(fmaxf(rintf(__fmul_rn(wl, iv)), -8.f), 7.f);
-      const float d = __fsub_rn(wl, __fmul_rn(q, sc));
-      term[k] = __fmul_rn(__fmul_rn(hwl, d), d);
+      sc[k] = cand <= hi_c ? tabrow[cand] : 0.f;
+      valid[k] = cand <= hi_c && sc[k] > 0.f;
+      iv[k] = __fdiv_rn(1.0f, valid[k] ? sc[k] : 1.f);
       err[k] = 0.f;
     }
 #pragma unroll
     for (int t = 0; t < GROUP; ++t) {
+      const float h = hw[t];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) err[k] = __fadd_rn(err[k], __shfl_sync(0xffffffffu, term[k], t));
+      for (int k = 0; k < 4; ++k) {
+        const float q = fminf(fmaxf(rintf(__fmul_rn(w[t], iv[k])), -8.f), 7.f);
+        const float d = __fsub_rn(w[t], __fmul_rn(q, sc[k]));
+        err[k] = __fadd_rn(err[k], __fmul_rn(__fmul_rn(h, d), d));
+      }
     }
     float best_e = INFINITY;
 #pragma unroll
@@ -88,45 +80,28 @@ __device__ __forceinline__ int q4tp_group_warp(float& wl, float (&wlater)[NLATER
       }
     }
   }
-  const float s = tabrow[best_c];
-  float myq = 0.f, mye = 0.f;
-#pragma unroll 4
-  for (int j = 0; j < GROUP; ++j) {
-    float e = 0.f;
-    if (lane == j) {
-      float q = 0.f;
-      if (s > 0.f) q = fminf(fmaxf(rintf(__fdiv_rn(wl, s)), -8.f), 7.f);
-      const float dj = U[j * ldu + j];
-      if (dj > 0.f) e = __fdiv_rn(__fsub_rn(wl, __fmul_rn(q, s)), dj);
-      myq = q;
-      mye = e;
-    }
-    e = __shfl_sync(0xffffffffu, e, j);
-    if (e != 0.f) {
-      const float* urow = U + j * ldu;
-      if (lane > j) wl = __fsub_rn(wl, __fmul_rn(e, urow[lane]));
-#pragma unroll
-      for (int k = 0; k < NLATER; ++k)
-        if (k < nl) wlater[k] = __fsub_rn(wlater[k], __fmul_rn(e, urow[GROUP * (k + 1) + lane]));
-    }
-  }
-  s_out = s;
-  q_out = myq;
-  e_out = mye;
   return best_c;
 }
 
-// Packs the 32 codes of a warp into the tile's 4 words (byte j/2, low nibble
-// for even j) and writes them: lanes 0..3 store one word each.
-__device__ __forceinline__ void store_nibbles_warp(float q, int lane, uint32_t* dst) {
-  const uint32_t nb = (uint32_t)((int)q + 8) & 15u;
-  uint32_t word = 0u;
+__device__ __forceinline__ void q4tp_round(float (&w)[GROUP], float s, const float* U, int ldu,
+                                           uint32_t (&words)[4], float (&e)[GROUP]) {
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const uint32_t v = __shfl_sync(0xffffffffu, nb, (lane & 3) * 8 + i);
-    word |= v << (4 * i);
+  for (int i = 0; i < 4; ++i) words[i] = 0u;
+#pragma unroll
+  for (int j = 0; j < GROUP; ++j) {
+    float q = 0.f;
+    if (s > 0.f) q = fminf(fmaxf(rintf(__fdiv_rn(w[j], s)), -8.f), 7.f);
+    const uint32_t nb = (uint32_t)((int)q + 8) & 15u;
+    words[j / 8] |= nb << (4 * (j % 8));
+    const float dj = U[j * ldu + j];
+    float ej = 0.f;
+    if (dj > 0.f) ej = __fdiv_rn(__fsub_rn(w[j], __fmul_rn(q, s)), dj);
+    e[j] = ej;
+    if (ej != 0.f) {
+#pragma unroll
+      for (int t = j + 1; t < GROUP; ++t) w[t] = __fsub_rn(w[t], __fmul_rn(ej, U[j * ldu + t]));
+    }
   }
-  if (lane < 4) dst[lane] = word;
 }
 
 // Per-row ladder ([host page] gptq_quantize_q4tp_dev's tab / lost; the
@@ -197,9 +172,9 @@ __global__ void __launch_bounds__(128) k_ladder(const float* __restrict__ W, int
   }
 }
 
-// The group rule on given tiles, one warp per row (the same device code as
+// The group rule on given tiles (one thread per row; the same device code as
 // the sweep's block kernel).
-__global__ void __launch_bounds__(256) k_group(const float* __restrict__ tile, int rows,
+__global__ void __launch_bounds__(128) k_group(const float* __restrict__ tile, int rows,
                                                const float* __restrict__ ublk,
                                                const float* __restrict__ hw,
                                                const float* __restrict__ tab,
@@ -207,97 +182,124 @@ __global__ void __launch_bounds__(256) k_group(const float* __restrict__ tile, i
                                                uint8_t* __restrict__ nib, uint8_t* __restrict__ rungs,
                                                float* __restrict__ scales, float* __restrict__ E) {
   __shared__ float Us[GROUP * GROUP];
+  __shared__ float hws[GROUP];
   for (int e = threadIdx.x; e < GROUP * GROUP; e += blockDim.x) Us[e] = ublk[e];
+  if (threadIdx.x < GROUP) hws[threadIdx.x] = hw[threadIdx.x];
   __syncthreads();
-  const int lane = threadIdx.x % 32;
-  const int r = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+  const int r = blockIdx.x * blockDim.x + threadIdx.x;
   if (r >= rows) return;
-  float wl = tile[(long long)r * GROUP + lane];
-  float none[1] = {0.f};
-  float s, q, e;
-  const int c = q4tp_group_warp<1>(wl, none, 0, hw[lane], tab + (long long)r * 32, lost[2 * r],
-                                   lost[2 * r + 1], Us, GROUP, lane, s, q, e);
-  store_nibbles_warp(q, lane, reinterpret_cast<uint32_t*>(nib + (long long)r * 16));
-  if (lane == 0) {
-    rungs[r] = (uint8_t)c;
-    scales[r] = s;
-  }
-  E[(long long)r * GROUP + lane] = e;
+  float w[GROUP], e[GROUP];
+#pragma unroll
+  for (int t = 0; t < GROUP; ++t) w[t] = tile[(long long)r * GROUP + t];
+  const int c = q4tp_pick(w, hws, tab + (long long)r * 32, lost[2 * r], lost[2 * r + 1]);
+  const float s = tab[(long long)r * 32 + c];
+  uint32_t words[4];
+  q4tp_round(w, s, Us, GROUP, words, e);
+  reinterpret_cast<uint4*>(nib)[r] = make_uint4(words[0], words[1], words[2], words[3]);
+  rungs[r] = (uint8_t)c;
+  scales[r] = s;
+#pragma unroll
+  for (int t = 0; t < GROUP; ++t) E[(long long)r * GROUP + t] = e[t];
 }
 
-constexpr int SWEEP_WARPS = 16;
+constexpr int SWEEP_ROWS = 32;
+constexpr int LW = SB + 1;
 
-// One lazy block [b0, b0+B) (B <= SB): one warp per row, rows strided over
-// the grid's warps.  The block's U (B x B) and rung weights sit in shared
-// memory; each lane keeps its column of every group of the block in
-// registers.  Group by group: the rung rule, codes, residuals and the
-// per-column feedback into the rest of the group and the later groups of the
-// block; then nibbles, rung, scale and the residuals E (TF32 hi/lo, the
-// trailing GEMM's operand) go out.
-__global__ void __launch_bounds__(SWEEP_WARPS * 32) k_sweep_block(
+// One lazy block [b0, b0+B) (B <= SB) for 32 rows per CTA, one thread per
+// row: the block's U (B x B) and rung weights and the rows' block of W sit in
+// shared memory.  Group by group: the rung rule, codes, residuals and the
+// in-group feedback, then the group's residuals into the rest of the block
+// (w_c -= sum_j e_j U_jc); nibbles, rung, scale and the residuals E (TF32
+// hi/lo, the trailing GEMM's operand) go out.
+__global__ void __launch_bounds__(SWEEP_ROWS) k_sweep_block(
     const float* __restrict__ W, int rows, int n, int b0, int B, const float* __restrict__ U,
     const float* __restrict__ hw, const float* __restrict__ tab, const float* __restrict__ lost,
     uint8_t* __restrict__ nib, uint8_t* __restrict__ rungs, float* __restrict__ scales,
     float* __restrict__ E_hi, float* __restrict__ E_lo) {
   extern __shared__ __align__(16) float sm[];
-  float* Us = sm;            // [SB][SB]
-  float* hws = Us + SB * SB; // [SB]
-  // The block's U rows as float4 (B is a multiple of 32), 8 loads in flight
-  // per thread per batch.
+  float* Us = sm;                 // [SB][SB]
+  float* hws = Us + SB * SB;      // [SB]
+  float* Ws = hws + SB;           // [SWEEP_ROWS][LW]
+  const int tid = threadIdx.x;
+  const int r0 = blockIdx.x * SWEEP_ROWS;
   {
+    // U block rows as float4 (B is a multiple of 32), 16 loads in flight per
+    // thread per batch.
     const int q4 = B / 4;
     const int tot = B * q4;
 #pragma unroll 1
-    for (int b = 0; b < tot; b += 8 * SWEEP_WARPS * 32) {
-      float4 v[8];
+    for (int b = 0; b < tot; b += 16 * SWEEP_ROWS) {
+      float4 v[16];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int e = b + threadIdx.x + i * SWEEP_WARPS * 32;
+      for (int i = 0; i < 16; ++i) {
+        const int e = b + tid + i * SWEEP_ROWS;
         if (e < tot)
           v[i] = *reinterpret_cast<const float4*>(U + (long long)(b0 + e / q4) * n + b0 + 4 * (e % q4));
       }
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int e = b + threadIdx.x + i * SWEEP_WARPS * 32;
+      for (int i = 0; i < 16; ++i) {
+        const int e = b + tid + i * SWEEP_ROWS;
         if (e < tot) *reinterpret_cast<float4*>(Us + (e / q4) * SB + 4 * (e % q4)) = v[i];
       }
     }
+    // The rows' block of W, coalesced along each row.
+#pragma unroll 1
+    for (int i0 = 0; i0 < SWEEP_ROWS; i0 += 8) {
+      float v[8][SB / 32];
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int k = 0; k < SB / 32; ++k) {
+          const int rr = r0 + i0 + i, c = k * 32 + tid;
+          v[i][k] = (rr < rows && c < B) ? W[(long long)rr * n + b0 + c] : 0.f;
+        }
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int k = 0; k < SB / 32; ++k) Ws[(i0 + i) * LW + k * 32 + tid] = v[i][k];
+    }
   }
-  for (int e = threadIdx.x; e < B; e += blockDim.x) hws[e] = hw[b0 + e];
+  for (int e = tid; e < B; e += SWEEP_ROWS) hws[e] = hw[b0 + e];
   __syncthreads();
-  const int lane = threadIdx.x % 32;
-  const int ng = B / GROUP;
+  const int r = r0 + tid;
+  if (r >= rows) return;
   const int gpr = n / GROUP;
-  for (int r = blockIdx.x * SWEEP_WARPS + threadIdx.x / 32; r < rows; r += gridDim.x * SWEEP_WARPS) {
-    const float* wrow = W + (long long)r * n + b0;
-    float wv[SB / GROUP];
+  const float lo = lost[2 * r], st = lost[2 * r + 1];
+  const float* tabrow = tab + (long long)r * 32;
+  float* wrow = Ws + tid * LW;
+  for (int g = 0; g < B / GROUP; ++g) {
+    float w[GROUP], e[GROUP];
 #pragma unroll
-    for (int g = 0; g < SB / GROUP; ++g) wv[g] = g < ng ? wrow[g * GROUP + lane] : 0.f;
-    const float lo = lost[2 * r], st = lost[2 * r + 1];
-    const float* tabrow = tab + (long long)r * 32;
+    for (int t = 0; t < GROUP; ++t) w[t] = wrow[g * GROUP + t];
+    const int c = q4tp_pick(w, hws + g * GROUP, tabrow, lo, st);
+    const float s = tabrow[c];
+    uint32_t words[4];
+    q4tp_round(w, s, Us + g * GROUP * SB + g * GROUP, SB, words, e);
+    const long long tix = (long long)r * gpr + b0 / GROUP + g;
+    reinterpret_cast<uint4*>(nib)[tix] = make_uint4(words[0], words[1], words[2], words[3]);
+    rungs[tix] = (uint8_t)c;
+    scales[tix] = s;
+    float4* eh = reinterpret_cast<float4*>(E_hi + (long long)r * SB + g * GROUP);
+    float4* el = reinterpret_cast<float4*>(E_lo + (long long)r * SB + g * GROUP);
 #pragma unroll
-    for (int g = 0; g < SB / GROUP; ++g) {
-      if (g >= ng) break;
-      float later[SB / GROUP - 1];
+    for (int t = 0; t < GROUP / 4; ++t) {
+      float4 h, l;
+      split_tf32(e[4 * t], h.x, l.x);
+      split_tf32(e[4 * t + 1], h.y, l.y);
+      split_tf32(e[4 * t + 2], h.z, l.z);
+      split_tf32(e[4 * t + 3], h.w, l.w);
+      eh[t] = h;
+      el[t] = l;
+    }
+#pragma unroll 2
+    for (int col = (g + 1) * GROUP; col < B; ++col) {
+      float a0 = 0.f, a1 = 0.f;
 #pragma unroll
-      for (int k = 0; k < SB / GROUP - 1; ++k) later[k] = (g + 1 + k < SB / GROUP) ? wv[(g + 1 + k) % (SB / GROUP)] : 0.f;
-      float s, q, e;
-      const int c = q4tp_group_warp<SB / GROUP - 1>(wv[g], later, ng - g - 1, hws[g * GROUP + lane], tabrow,
-                                                    lo, st, Us + g * GROUP * SB + g * GROUP, SB, lane, s,
-                                                    q, e);
-#pragma unroll
-      for (int k = 0; k < SB / GROUP - 1; ++k)
-        if (g + 1 + k < SB / GROUP) wv[(g + 1 + k) % (SB / GROUP)] = later[k];
-      const long long tix = (long long)r * gpr + b0 / GROUP + g;
-      store_nibbles_warp(q, lane, reinterpret_cast<uint32_t*>(nib + tix * 16));
-      if (lane == 0) {
-        rungs[tix] = (uint8_t)c;
-        scales[tix] = s;
+      for (int j = 0; j < GROUP; j += 2) {
+        a0 = fmaf(e[j], Us[(g * GROUP + j) * SB + col], a0);
+        a1 = fmaf(e[j + 1], Us[(g * GROUP + j + 1) * SB + col], a1);
       }
-      float h, l;
-      split_tf32(e, h, l);
-      E_hi[(long long)r * SB + g * GROUP + lane] = h;
-      E_lo[(long long)r * SB + g * GROUP + lane] = l;
+      wrow[col] -= a0 + a1;
     }
   }
 }
@@ -346,7 +348,7 @@ static gptq_status sweep_attrs() {
   static bool done = false;
   if (done) return GPTQ_OK;
   GQ_CUDA(cudaFuncSetAttribute(k_sweep_block, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (SB * SB + SB) * 4));
+                               (SB * SB + SB + SWEEP_ROWS * LW) * 4));
   done = true;
   return GPTQ_OK;
 }
@@ -362,7 +364,7 @@ gptq_status group_run(const float* tile, int rows, const float* ublk, const floa
                       const float* tab, const float* lost, uint8_t* nib, uint8_t* rungs,
                       float* scales, float* E, cudaStream_t s) {
   GQ_PROF(K_GROUP, s);
-  k_group<<<(rows + 7) / 8, 256, 0, s>>>(tile, rows, ublk, hw, tab, lost, nib, rungs, scales, E);
+  k_group<<<(rows + 127) / 128, 128, 0, s>>>(tile, rows, ublk, hw, tab, lost, nib, rungs, scales, E);
   GQ_LAUNCHED();
   return GPTQ_OK;
 }
@@ -420,19 +422,14 @@ gptq_status sweep_run(float* W, int rows, int n, const float* U, const float* hw
   GQ_TRY(make_operand_map(&maps.m[2], E_hi, rows, SB));
   GQ_TRY(make_operand_map(&maps.m[3], E_lo, rows, SB));
   GQ_TRY(make_c_map(&maps.c, W, rows, n, n));
-  const int smem = (SB * SB + SB) * 4;
+  const int smem = (SB * SB + SB + SWEEP_ROWS * LW) * 4;
   const TcJob none{};
-  int sms = 0, dev = 0;
-  GQ_CUDA(cudaGetDevice(&dev));
-  GQ_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
-  const int want = (rows + SWEEP_WARPS - 1) / SWEEP_WARPS;
-  const int blocks = want < 2 * sms ? want : 2 * sms;
   for (int b0 = 0; b0 < n; b0 += SB) {
     const int B = (n - b0) < SB ? (n - b0) : SB;
     const int b1 = b0 + B;
     {
       GQ_PROF(K_SWEEP_BLOCK, s);
-      k_sweep_block<<<blocks, SWEEP_WARPS * 32, smem, s>>>(
+      k_sweep_block<<<(rows + SWEEP_ROWS - 1) / SWEEP_ROWS, SWEEP_ROWS, smem, s>>>(
           W, rows, n, b0, B, U, hw, tab, lost, nib, rungs, scales, E_hi, E_lo);
       GQ_LAUNCHED();
     }
