@@ -57,16 +57,26 @@ def workload_desc(cfg):
 
 
 def fold_gemm_flops(n, NB=128):
-    """Useful flops of the fold's update GEMM launches (SYRK lower tiles +
-    inverse rectangle) over one fold, on the padded size."""
+    """Useful flops of the fold's update GEMM launches over one fold, on the
+    padded size, following the library's schedule: steps in pairs (a thin
+    K = NB strip update of the next block column between them, then one
+    K = 2 NB trailing update), a last unpaired step with K = NB."""
     N = (n + NB - 1) // NB * NB
     tot = 0
-    for k in range(0, N, NB):
-        s0 = k + NB
-        m = N - s0
-        if m <= 0:
-            continue
-        tot += 2 * NB * (m * (m + 1) // 2) + 2 * NB * s0 * m
+    k = 0
+    while k < N:
+        if k + 2 * NB <= N:
+            k1, s1 = k + NB, k + 2 * NB
+            tot += 2 * NB * ((N - k1 - NB) * NB + NB * (NB + 1) // 2)  # SYRK strip
+            tot += 2 * NB * k1 * NB  # inverse strip
+            m = N - s1
+            tot += 2 * (2 * NB) * (m * (m + 1) // 2) + 2 * (2 * NB) * s1 * m
+            k = s1
+        else:
+            s0 = k + NB
+            m = N - s0
+            tot += 2 * NB * (m * (m + 1) // 2) + 2 * NB * s0 * m
+            k = s0
     return tot
 
 

@@ -88,7 +88,9 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 // covers C[c_y0 + 128 ti ..][c_x0 + 128 tj ..], and whatever falls outside
 // the map's extent is not written (that masks ragged edges).
 // mode 0: rectangle of mt x nt tiles; mode 1: lower triangle of an mt x mt
-// tile grid (ti >= tj; inside a diagonal tile only r >= s is changed).
+// tile grid (ti >= tj; inside a diagonal tile only r >= s is changed);
+// mode 2: rectangle whose tiles with ti == tj are diagonal tiles (a strip
+// of a lower triangle starting at its diagonal).
 struct TcJob {
   int c_x0, c_y0;
   int a_map, b_map, a_row0, b_row0;
@@ -107,6 +109,13 @@ inline TcJob tc_rect(int c_x0, int c_y0, int a_map, int a_row0, int b_map, int b
   j.b_row0 = b_row0; j.mode = 0; j.M = M; j.N = N;
   j.mt = (M + 127) / 128; j.nt = (N + 127) / 128;
   j.ntiles = (M > 0 && N > 0) ? j.mt * j.nt : 0;
+  return j;
+}
+
+inline TcJob tc_strip(int c_x0, int c_y0, int a_map, int a_row0, int b_map, int b_row0, int M,
+                      int N) {
+  TcJob j = tc_rect(c_x0, c_y0, a_map, a_row0, b_map, b_row0, M, N);
+  j.mode = 2;
   return j;
 }
 

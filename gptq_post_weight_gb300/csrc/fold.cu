@@ -288,6 +288,9 @@ __global__ void __launch_bounds__(256) k_potrf(const float* __restrict__ A, long
 }
 
 constexpr int APPLY_ROWS = 64;
+// Panel buffers hold two steps side by side (columns [0, NB) and [NB, 2NB)),
+// so that a pair of steps updates the trailing matrix once with K = 2 NB.
+constexpr int PW = 2 * NB;
 
 // Both triangular solves of step k as one product with the explicit inverse:
 // z = L_kk^-1 v for every row vector v, i.e. Z = V Linv^T, four threads per
@@ -298,9 +301,11 @@ constexpr int APPLY_ROWS = 64;
 //    Y[c][k..k+NB) (the unit vector e_{c-k} when c is in block k, so that row
 //    of Z is a column of Linv), z -> Yp[c][*], and the finished entries of U:
 //    U[n-1-i][n-1-c] = X[i][c] / |d_{n-1-c}| ([fold page] make_u), i = k+t.
-// z is stored as its TF32 hi/lo split, the operand format of the update GEMM.
+// z is stored as its TF32 hi/lo split, the operand format of the update GEMM,
+// in columns [col0, col0 + NB) of the 2 NB-wide panel buffers; panel rows
+// below zero_end also clear their Yp entries there (see fold_attempt).
 __global__ void __launch_bounds__(APPLY_ROWS * 4) k_apply(const float* __restrict__ A, long long lda,
-                                                         int k, int s0, int N,
+                                                         int k, int s0, int N, int col0, int zero_end,
                                                          const float* __restrict__ Linv,
                                                          float* __restrict__ P_hi, float* __restrict__ P_lo,
                                                          float* __restrict__ Y_hi, float* __restrict__ Y_lo,
@@ -367,8 +372,19 @@ __global__ void __launch_bounds__(APPLY_ROWS * 4) k_apply(const float* __restric
     }
   }
   const bool panel = r >= s0;
-  float4* dh = reinterpret_cast<float4*>((panel ? P_hi : Y_hi) + (long long)r * NB + q * 32);
-  float4* dl = reinterpret_cast<float4*>((panel ? P_lo : Y_lo) + (long long)r * NB + q * 32);
+  const long long off = (long long)r * PW + col0 + q * 32;
+  float4* dh = reinterpret_cast<float4*>((panel ? P_hi : Y_hi) + off);
+  float4* dl = reinterpret_cast<float4*>((panel ? P_lo : Y_lo) + off);
+  if (panel && r < zero_end) {
+    // Rows of the next block: their part of Yp in this half is X[block k][r] = 0.
+    float4* zh = reinterpret_cast<float4*>(Y_hi + off);
+    float4* zl = reinterpret_cast<float4*>(Y_lo + off);
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+      zh[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+      zl[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
 #pragma unroll
   for (int t = 0; t < 8; ++t) {
     float4 h, l;
@@ -395,9 +411,9 @@ __global__ void __launch_bounds__(APPLY_ROWS * 4) k_apply(const float* __restric
 struct FoldWs {
   int n, N;
   float* A;       // N x N
-  float* P_hi;    // N x NB   (L panel of the current step, TF32 hi/lo)
+  float* P_hi;    // N x PW   (L panels of the current pair of steps, TF32 hi/lo)
   float* P_lo;
-  float* Yp_hi;   // N x NB   (Y panel of the current step, TF32 hi/lo)
+  float* Yp_hi;   // N x PW   (Y panels of the current pair of steps, TF32 hi/lo)
   float* Yp_lo;
   float* Lkk;     // NB x NB: inverse of the current diagonal block of L
   float* hdiag;   // n
@@ -411,10 +427,10 @@ static bool carve_fold(Carve& c, int n, FoldWs& w) {
   w.N = (int)round_up((size_t)n, NB);
   const size_t N = (size_t)w.N;
   w.A = c.take<float>(N * N);
-  w.P_hi = c.take<float>(N * NB);
-  w.P_lo = c.take<float>(N * NB);
-  w.Yp_hi = c.take<float>(N * NB);
-  w.Yp_lo = c.take<float>(N * NB);
+  w.P_hi = c.take<float>(N * PW);
+  w.P_lo = c.take<float>(N * PW);
+  w.Yp_hi = c.take<float>(N * PW);
+  w.Yp_lo = c.take<float>(N * PW);
   w.Lkk = c.take<float>((size_t)NB * NB);
   w.hdiag = c.take<float>((size_t)n);
   w.dabs = c.take<float>((size_t)n);
@@ -456,25 +472,55 @@ static gptq_status fold_attempt(const float* hp, const FoldWs& w, const OperandM
     k_build<<<N, 256, 0, s>>>(hp, n, N, w.hdiag, w.base, lam, w.dabs, w.A, ld, 1);
     GQ_LAUNCHED();
   }
-  for (int k = 0; k < N; k += NB) {
+  // Steps go in pairs (k, k + NB) while two blocks remain:
+  //   potrf(k); apply(k) -> panel columns [0, NB);
+  //   thin update of block column k + NB only (K = NB): SYRK strip and the
+  //   inverse's strip, so that block k + NB is current;
+  //   potrf(k + NB); apply(k + NB) -> panel columns [NB, 2 NB);
+  //   one trailing update with K = 2 NB (both panels) for everything right
+  //   of / below block k + NB.
+  // A last unpaired block runs as a single step (K = NB).
+  auto step = [&](int k, int col0, int zero_end) -> gptq_status {
     const int s0 = k + NB;
     {
       GQ_PROF(K_POTRF, s);
       k_potrf<<<1, 256, POTRF_SMEM, s>>>(w.A, ld, k, w.Lkk, w.flag);
       GQ_LAUNCHED();
     }
-    {
-      GQ_PROF(K_TRSM, s);
-      k_apply<<<N / APPLY_ROWS, APPLY_ROWS * 4, APPLY_SMEM, s>>>(w.A, ld, k, s0, N, w.Lkk, w.P_hi,
-                                                                 w.P_lo, w.Yp_hi, w.Yp_lo, w.flag,
-                                                                 U, w.dabs, n);
-      GQ_LAUNCHED();
-    }
-    if (s0 < N) {
-      // maps: 0/1 = P hi/lo, 2/3 = Yp hi/lo.
-      const TcJob syrk = tc_lower(s0, s0, 0, s0, N - s0);
-      const TcJob inv = tc_rect(s0, 0, 2, 0, 0, s0, s0, N - s0);
-      GQ_TRY(gemm_tc_sub(maps, syrk, inv, NB, w.flag, w.flag, K_FOLD_GEMM, s));
+    GQ_PROF(K_TRSM, s);
+    k_apply<<<N / APPLY_ROWS, APPLY_ROWS * 4, APPLY_SMEM, s>>>(w.A, ld, k, s0, N, col0, zero_end,
+                                                               w.Lkk, w.P_hi, w.P_lo, w.Yp_hi,
+                                                               w.Yp_lo, w.flag, U, w.dabs, n);
+    GQ_LAUNCHED();
+    return GPTQ_OK;
+  };
+  // maps: 0/1 = P hi/lo, 2/3 = Yp hi/lo (K = 2 NB wide).
+  int k = 0;
+  while (k < N) {
+    if (k + 2 * NB <= N) {
+      const int k1 = k + NB, s1 = k + 2 * NB;
+      GQ_TRY(step(k, 0, s1));
+      {
+        const TcJob syrk = tc_strip(k1, k1, 0, k1, 0, k1, N - k1, NB);
+        const TcJob inv = tc_rect(k1, 0, 2, 0, 0, k1, k1, NB);
+        GQ_TRY(gemm_tc_sub(maps, syrk, inv, NB, w.flag, w.flag, K_FOLD_GEMM, s));
+      }
+      GQ_TRY(step(k1, NB, 0));
+      if (s1 < N) {
+        const TcJob syrk = tc_lower(s1, s1, 0, s1, N - s1);
+        const TcJob inv = tc_rect(s1, 0, 2, 0, 0, s1, s1, N - s1);
+        GQ_TRY(gemm_tc_sub(maps, syrk, inv, 2 * NB, w.flag, w.flag, K_FOLD_GEMM, s));
+      }
+      k = s1;
+    } else {
+      const int s0 = k + NB;
+      GQ_TRY(step(k, 0, 0));
+      if (s0 < N) {
+        const TcJob syrk = tc_lower(s0, s0, 0, s0, N - s0);
+        const TcJob inv = tc_rect(s0, 0, 2, 0, 0, s0, s0, N - s0);
+        GQ_TRY(gemm_tc_sub(maps, syrk, inv, NB, w.flag, w.flag, K_FOLD_GEMM, s));
+      }
+      k = s0;
     }
   }
   return GPTQ_OK;
@@ -494,10 +540,10 @@ gptq_status fold_run(const float* hp, int n, double lambda, float* U, float* D, 
   if (hdiag) GQ_CUDA(cudaMemcpyAsync(hdiag, w.hdiag, (size_t)n * 4, cudaMemcpyDeviceToDevice, s));
   GQ_CUDA(cudaMemsetAsync(U, 0, (size_t)n * n * 4, s));
   OperandMaps maps;
-  GQ_TRY(make_operand_map(&maps.m[0], w.P_hi, w.N, NB));
-  GQ_TRY(make_operand_map(&maps.m[1], w.P_lo, w.N, NB));
-  GQ_TRY(make_operand_map(&maps.m[2], w.Yp_hi, w.N, NB));
-  GQ_TRY(make_operand_map(&maps.m[3], w.Yp_lo, w.N, NB));
+  GQ_TRY(make_operand_map(&maps.m[0], w.P_hi, w.N, PW));
+  GQ_TRY(make_operand_map(&maps.m[1], w.P_lo, w.N, PW));
+  GQ_TRY(make_operand_map(&maps.m[2], w.Yp_hi, w.N, PW));
+  GQ_TRY(make_operand_map(&maps.m[3], w.Yp_lo, w.N, PW));
   GQ_TRY(make_c_map(&maps.c, w.A, w.N, w.N, w.N));
   double lam = lambda > 0.0 ? lambda : 0.0;
   for (;;) {

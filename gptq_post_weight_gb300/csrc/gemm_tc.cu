@@ -341,7 +341,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       int ti, tj;
       tile_of(J, second ? t - j0.ntiles : t, ti, tj);
       const int rr = q * 32 + lane;  // row inside the tile
-      const bool diag = (J.mode == 1) && (ti == tj);
+      const bool diag = (J.mode != 0) && (ti == tj);
       const uint32_t tbase = tmem + (uint32_t)(acc * BN) + ((uint32_t)(q * 32) << 16);
 #pragma unroll 1
       for (int cc = 0; cc < BN; cc += 32) {

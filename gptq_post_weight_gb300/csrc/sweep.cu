@@ -3,12 +3,15 @@
 // host page's gptq_quantize_q4tp).
 //
 // Lazy blocks of SB = 128 columns (4 groups): one kernel runs the four
-// groups of a block for 64 rows per CTA out of shared memory (rung choice,
-// rounding, in-group feedback, then the group's residuals into the rest of
-// the block), then one GEMM applies the block's residuals to every later
-// column: W[:, b1:] -= E_blk U[b0:b1, b1:].  With SB = 32 this is the fold
-// page's per-group q4tp_trail; a wider block is the same mathematics with
-// the residual sums taken in a different order.
+// groups of a block out of shared memory (rung choice, rounding, in-group
+// feedback, then the group's residuals into the rest of the block), and
+// GEMMs apply the residuals to every later column:
+// W[:, b1:] -= E_blk U[b0:b1, b1:].  Blocks go in pairs: after the first
+// block a thin update (K = 128) brings the second block's columns up to
+// date, and after the second one update with K = 256 (both blocks'
+// residuals) covers everything to the right.  With SB = 32 and no pairing
+// this is the fold page's per-group q4tp_trail; the wider blocks are the
+// same mathematics with the residual sums taken in a different order.
 //
 // The per-group rule uses one rounding per operation (no contraction) so it
 // reproduces the pages' f32 arithmetic bit for bit.
@@ -203,24 +206,28 @@ __global__ void __launch_bounds__(128) k_group(const float* __restrict__ tile, i
 }
 
 constexpr int SWEEP_ROWS = 32;
+constexpr int SWEEP_THREADS = 128;
 constexpr int LW = SB + 1;
+constexpr int EW = 2 * SB;  // residual / U-stripe buffers hold a pair of blocks
 
-// One lazy block [b0, b0+B) (B <= SB) for 32 rows per CTA, one thread per
-// row: the block's U (B x B) and rung weights and the rows' block of W sit in
-// shared memory.  Group by group: the rung rule, codes, residuals and the
-// in-group feedback, then the group's residuals into the rest of the block
-// (w_c -= sum_j e_j U_jc); nibbles, rung, scale and the residuals E (TF32
-// hi/lo, the trailing GEMM's operand) go out.
-__global__ void __launch_bounds__(SWEEP_ROWS) k_sweep_block(
+// One lazy block [b0, b0+B) (B <= SB) for 32 rows per CTA: the block's U
+// (B x B), rung weights and the rows' block of W sit in shared memory.  Group
+// by group, warp 0 runs the rung / rounding rule (one thread per row) and
+// writes nibbles, rung, scale and the residuals E (TF32 hi/lo, the trailing
+// GEMM's operand); then all four warps push the group's residuals into the
+// rest of the block (w_c -= sum_j e_j U_jc), each warp a quarter of the
+// columns.
+__global__ void __launch_bounds__(SWEEP_THREADS) k_sweep_block(
     const float* __restrict__ W, int rows, int n, int b0, int B, const float* __restrict__ U,
     const float* __restrict__ hw, const float* __restrict__ tab, const float* __restrict__ lost,
     uint8_t* __restrict__ nib, uint8_t* __restrict__ rungs, float* __restrict__ scales,
-    float* __restrict__ E_hi, float* __restrict__ E_lo) {
+    float* __restrict__ E_hi, float* __restrict__ E_lo, int ecol0) {
   extern __shared__ __align__(16) float sm[];
   float* Us = sm;                 // [SB][SB]
   float* hws = Us + SB * SB;      // [SB]
   float* Ws = hws + SB;           // [SWEEP_ROWS][LW]
-  const int tid = threadIdx.x;
+  float* Es = Ws + SWEEP_ROWS * LW;  // [SWEEP_ROWS][GROUP + 1]
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   const int r0 = blockIdx.x * SWEEP_ROWS;
   {
     // U block rows as float4 (B is a multiple of 32), 16 loads in flight per
@@ -228,84 +235,98 @@ __global__ void __launch_bounds__(SWEEP_ROWS) k_sweep_block(
     const int q4 = B / 4;
     const int tot = B * q4;
 #pragma unroll 1
-    for (int b = 0; b < tot; b += 16 * SWEEP_ROWS) {
+    for (int b = 0; b < tot; b += 16 * SWEEP_THREADS) {
       float4 v[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
-        const int e = b + tid + i * SWEEP_ROWS;
+        const int e = b + tid + i * SWEEP_THREADS;
         if (e < tot)
           v[i] = *reinterpret_cast<const float4*>(U + (long long)(b0 + e / q4) * n + b0 + 4 * (e % q4));
       }
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
-        const int e = b + tid + i * SWEEP_ROWS;
+        const int e = b + tid + i * SWEEP_THREADS;
         if (e < tot) *reinterpret_cast<float4*>(Us + (e / q4) * SB + 4 * (e % q4)) = v[i];
       }
     }
-    // The rows' block of W, coalesced along each row.
-#pragma unroll 1
-    for (int i0 = 0; i0 < SWEEP_ROWS; i0 += 8) {
-      float v[8][SB / 32];
+    // The rows' block of W, coalesced along each row (warp w: rows w, w+4, ...).
+    float v[SWEEP_ROWS / 4][SB / 32];
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
+    for (int i = 0; i < SWEEP_ROWS / 4; ++i)
 #pragma unroll
-        for (int k = 0; k < SB / 32; ++k) {
-          const int rr = r0 + i0 + i, c = k * 32 + tid;
-          v[i][k] = (rr < rows && c < B) ? W[(long long)rr * n + b0 + c] : 0.f;
-        }
-#pragma unroll
-      for (int i = 0; i < 8; ++i)
-#pragma unroll
-        for (int k = 0; k < SB / 32; ++k) Ws[(i0 + i) * LW + k * 32 + tid] = v[i][k];
-    }
-  }
-  for (int e = tid; e < B; e += SWEEP_ROWS) hws[e] = hw[b0 + e];
-  __syncthreads();
-  const int r = r0 + tid;
-  if (r >= rows) return;
-  const int gpr = n / GROUP;
-  const float lo = lost[2 * r], st = lost[2 * r + 1];
-  const float* tabrow = tab + (long long)r * 32;
-  float* wrow = Ws + tid * LW;
-  for (int g = 0; g < B / GROUP; ++g) {
-    float w[GROUP], e[GROUP];
-#pragma unroll
-    for (int t = 0; t < GROUP; ++t) w[t] = wrow[g * GROUP + t];
-    const int c = q4tp_pick(w, hws + g * GROUP, tabrow, lo, st);
-    const float s = tabrow[c];
-    uint32_t words[4];
-    q4tp_round(w, s, Us + g * GROUP * SB + g * GROUP, SB, words, e);
-    const long long tix = (long long)r * gpr + b0 / GROUP + g;
-    reinterpret_cast<uint4*>(nib)[tix] = make_uint4(words[0], words[1], words[2], words[3]);
-    rungs[tix] = (uint8_t)c;
-    scales[tix] = s;
-    float4* eh = reinterpret_cast<float4*>(E_hi + (long long)r * SB + g * GROUP);
-    float4* el = reinterpret_cast<float4*>(E_lo + (long long)r * SB + g * GROUP);
-#pragma unroll
-    for (int t = 0; t < GROUP / 4; ++t) {
-      float4 h, l;
-      split_tf32(e[4 * t], h.x, l.x);
-      split_tf32(e[4 * t + 1], h.y, l.y);
-      split_tf32(e[4 * t + 2], h.z, l.z);
-      split_tf32(e[4 * t + 3], h.w, l.w);
-      eh[t] = h;
-      el[t] = l;
-    }
-#pragma unroll 2
-    for (int col = (g + 1) * GROUP; col < B; ++col) {
-      float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-      for (int j = 0; j < GROUP; j += 2) {
-        a0 = fmaf(e[j], Us[(g * GROUP + j) * SB + col], a0);
-        a1 = fmaf(e[j + 1], Us[(g * GROUP + j + 1) * SB + col], a1);
+      for (int kq = 0; kq < SB / 32; ++kq) {
+        const int rr = r0 + warp + 4 * i, c = kq * 32 + lane;
+        v[i][kq] = (rr < rows && c < B) ? W[(long long)rr * n + b0 + c] : 0.f;
       }
-      wrow[col] -= a0 + a1;
+#pragma unroll
+    for (int i = 0; i < SWEEP_ROWS / 4; ++i)
+#pragma unroll
+      for (int kq = 0; kq < SB / 32; ++kq) Ws[(warp + 4 * i) * LW + kq * 32 + lane] = v[i][kq];
+  }
+  for (int e = tid; e < B; e += SWEEP_THREADS) hws[e] = hw[b0 + e];
+  __syncthreads();
+  const int r = r0 + lane;
+  const bool live = r < rows;
+  const int gpr = n / GROUP;
+  float* wrow = Ws + lane * LW;
+  for (int g = 0; g < B / GROUP; ++g) {
+    if (warp == 0 && live) {
+      const float lo = lost[2 * r], st = lost[2 * r + 1];
+      const float* tabrow = tab + (long long)r * 32;
+      float w[GROUP], e[GROUP];
+#pragma unroll
+      for (int t = 0; t < GROUP; ++t) w[t] = wrow[g * GROUP + t];
+      const int c = q4tp_pick(w, hws + g * GROUP, tabrow, lo, st);
+      const float s = tabrow[c];
+      uint32_t words[4];
+      q4tp_round(w, s, Us + g * GROUP * SB + g * GROUP, SB, words, e);
+      const long long tix = (long long)r * gpr + b0 / GROUP + g;
+      reinterpret_cast<uint4*>(nib)[tix] = make_uint4(words[0], words[1], words[2], words[3]);
+      rungs[tix] = (uint8_t)c;
+      scales[tix] = s;
+      float4* eh = reinterpret_cast<float4*>(E_hi + (long long)r * EW + ecol0 + g * GROUP);
+      float4* el = reinterpret_cast<float4*>(E_lo + (long long)r * EW + ecol0 + g * GROUP);
+#pragma unroll
+      for (int t = 0; t < GROUP / 4; ++t) {
+        float4 h, l;
+        split_tf32(e[4 * t], h.x, l.x);
+        split_tf32(e[4 * t + 1], h.y, l.y);
+        split_tf32(e[4 * t + 2], h.z, l.z);
+        split_tf32(e[4 * t + 3], h.w, l.w);
+        eh[t] = h;
+        el[t] = l;
+      }
+#pragma unroll
+      for (int t = 0; t < GROUP; ++t) Es[lane * (GROUP + 1) + t] = e[t];
     }
+    __syncthreads();
+    const int rest = B - (g + 1) * GROUP;  // later columns of the block
+    if (rest > 0 && live) {
+      float e[GROUP];
+#pragma unroll
+      for (int t = 0; t < GROUP; ++t) e[t] = Es[lane * (GROUP + 1) + t];
+      const int per = rest / 4;  // multiple of 8
+      const int c0 = (g + 1) * GROUP + warp * per;
+#pragma unroll 2
+      for (int col = c0; col < c0 + per; ++col) {
+        float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+        for (int j = 0; j < GROUP; j += 2) {
+          a0 = fmaf(e[j], Us[(g * GROUP + j) * SB + col], a0);
+          a1 = fmaf(e[j + 1], Us[(g * GROUP + j + 1) * SB + col], a1);
+        }
+        wrow[col] -= a0 + a1;
+      }
+    }
+    __syncthreads();
   }
 }
 
-// Ut[c][t] = U[b0 + t][b1 + c]: the block row of U, K-major for the GEMM,
-// stored as its TF32 hi/lo split.
+// Ut[c][t] = U[b0 + t][b1 + c], t < kt (one or two blocks' rows of U),
+// c < n - b1: the block rows of U to the right of the first block, K-major
+// for the GEMM, stored as their TF32 hi/lo split.  Rows b1 + c of U below
+// the diagonal are zero, so the same stripe serves the thin update of the
+// second block (c < SB, first SB of t) and the pair's trailing update.
 __global__ void k_prep_ut(const float* __restrict__ U, int n, int b0, int b1,
                           float* __restrict__ Ut_hi, float* __restrict__ Ut_lo) {
   __shared__ float tile[32][33];
@@ -321,8 +342,8 @@ __global__ void k_prep_ut(const float* __restrict__ U, int n, int b0, int b1,
     if (c < ncol) {
       float h, l;
       split_tf32(tile[threadIdx.x][i], h, l);
-      Ut_hi[(long long)c * SB + t0 + threadIdx.x] = h;
-      Ut_lo[(long long)c * SB + t0 + threadIdx.x] = l;
+      Ut_hi[(long long)c * EW + t0 + threadIdx.x] = h;
+      Ut_lo[(long long)c * EW + t0 + threadIdx.x] = l;
     }
   }
 }
@@ -341,14 +362,14 @@ __global__ void k_copy_dz(const float* __restrict__ W, long long total, int n,
 }  // namespace
 
 size_t sweep_ws_bytes(int rows, int n) {
-  return 2 * round_up((size_t)rows * SB * 4, 256) + 2 * round_up((size_t)n * SB * 4, 256) + 1024;
+  return 2 * round_up((size_t)rows * EW * 4, 256) + 2 * round_up((size_t)n * EW * 4, 256) + 1024;
 }
 
 static gptq_status sweep_attrs() {
   static bool done = false;
   if (done) return GPTQ_OK;
   GQ_CUDA(cudaFuncSetAttribute(k_sweep_block, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (SB * SB + SB + SWEEP_ROWS * LW) * 4));
+                               (SB * SB + SB + SWEEP_ROWS * LW + SWEEP_ROWS * (GROUP + 1)) * 4));
   done = true;
   return GPTQ_OK;
 }
@@ -409,39 +430,60 @@ gptq_status sweep_run(float* W, int rows, int n, const float* U, const float* hw
                       size_t ws_bytes, cudaStream_t s) {
   GQ_TRY(sweep_attrs());
   Carve c(ws, ws_bytes);
-  float* E_hi = c.take<float>((size_t)rows * SB);
-  float* E_lo = c.take<float>((size_t)rows * SB);
-  float* Ut_hi = c.take<float>((size_t)n * SB);
-  float* Ut_lo = c.take<float>((size_t)n * SB);
+  float* E_hi = c.take<float>((size_t)rows * EW);
+  float* E_lo = c.take<float>((size_t)rows * EW);
+  float* Ut_hi = c.take<float>((size_t)n * EW);
+  float* Ut_lo = c.take<float>((size_t)n * EW);
   unsigned* status = c.take<unsigned>(4);
   if (!c.ok) return GPTQ_ERR_NOMEM;
   GQ_CUDA(cudaMemsetAsync(status, 0, sizeof(unsigned), s));
   OperandMaps maps;  // 0/1 = Ut hi/lo, 2/3 = E hi/lo
-  GQ_TRY(make_operand_map(&maps.m[0], Ut_hi, n, SB));
-  GQ_TRY(make_operand_map(&maps.m[1], Ut_lo, n, SB));
-  GQ_TRY(make_operand_map(&maps.m[2], E_hi, rows, SB));
-  GQ_TRY(make_operand_map(&maps.m[3], E_lo, rows, SB));
+  GQ_TRY(make_operand_map(&maps.m[0], Ut_hi, n, EW));
+  GQ_TRY(make_operand_map(&maps.m[1], Ut_lo, n, EW));
+  GQ_TRY(make_operand_map(&maps.m[2], E_hi, rows, EW));
+  GQ_TRY(make_operand_map(&maps.m[3], E_lo, rows, EW));
   GQ_TRY(make_c_map(&maps.c, W, rows, n, n));
-  const int smem = (SB * SB + SB + SWEEP_ROWS * LW) * 4;
+  const int smem = (SB * SB + SB + SWEEP_ROWS * LW + SWEEP_ROWS * (GROUP + 1)) * 4;
   const TcJob none{};
-  for (int b0 = 0; b0 < n; b0 += SB) {
-    const int B = (n - b0) < SB ? (n - b0) : SB;
-    const int b1 = b0 + B;
-    {
-      GQ_PROF(K_SWEEP_BLOCK, s);
-      k_sweep_block<<<(rows + SWEEP_ROWS - 1) / SWEEP_ROWS, SWEEP_ROWS, smem, s>>>(
-          W, rows, n, b0, B, U, hw, tab, lost, nib, rungs, scales, E_hi, E_lo);
-      GQ_LAUNCHED();
-    }
-    if (b1 < n) {
-      {
-        GQ_PROF(K_PREP_UT, s);
-        dim3 grid((n - b1 + 31) / 32, SB / 32);
-        k_prep_ut<<<grid, dim3(32, 8), 0, s>>>(U, n, b0, b1, Ut_hi, Ut_lo);
-        GQ_LAUNCHED();
+  const int grid_rows = (rows + SWEEP_ROWS - 1) / SWEEP_ROWS;
+  auto block = [&](int b0, int B, int ecol0) -> gptq_status {
+    GQ_PROF(K_SWEEP_BLOCK, s);
+    k_sweep_block<<<grid_rows, SWEEP_THREADS, smem, s>>>(W, rows, n, b0, B, U, hw, tab, lost, nib,
+                                                         rungs, scales, E_hi, E_lo, ecol0);
+    GQ_LAUNCHED();
+    return GPTQ_OK;
+  };
+  auto prep = [&](int b0, int b1, int kt) -> gptq_status {
+    GQ_PROF(K_PREP_UT, s);
+    dim3 grid((n - b1 + 31) / 32, kt / 32);
+    k_prep_ut<<<grid, dim3(32, 8), 0, s>>>(U, n, b0, b1, Ut_hi, Ut_lo);
+    GQ_LAUNCHED();
+    return GPTQ_OK;
+  };
+  // maps: 0/1 = Ut hi/lo, 2/3 = E hi/lo (K up to 2 SB).
+  int b0 = 0;
+  while (b0 < n) {
+    if (b0 + 2 * SB <= n) {
+      const int b1 = b0 + SB, b2 = b0 + 2 * SB;
+      GQ_TRY(block(b0, SB, 0));
+      GQ_TRY(prep(b0, b1, 2 * SB));
+      GQ_TRY(gemm_tc_sub(maps, tc_rect(b1, 0, 2, 0, 0, 0, rows, SB), none, SB, status, status,
+                         K_SWEEP_GEMM, s));
+      GQ_TRY(block(b1, SB, SB));
+      if (b2 < n)
+        GQ_TRY(gemm_tc_sub(maps, tc_rect(b2, 0, 2, 0, 0, SB, rows, n - b2), none, 2 * SB, status,
+                           status, K_SWEEP_GEMM, s));
+      b0 = b2;
+    } else {
+      const int B = (n - b0) < SB ? (n - b0) : SB;
+      const int b1 = b0 + B;
+      GQ_TRY(block(b0, B, 0));
+      if (b1 < n) {
+        GQ_TRY(prep(b0, b1, SB));
+        GQ_TRY(gemm_tc_sub(maps, tc_rect(b1, 0, 2, 0, 0, 0, rows, n - b1), none, SB, status,
+                           status, K_SWEEP_GEMM, s));
       }
-      GQ_TRY(gemm_tc_sub(maps, tc_rect(b1, 0, 2, 0, 0, 0, rows, n - b1), none, SB, status,
-                         status, K_SWEEP_GEMM, s));
+      b0 = b1;
     }
   }
   unsigned hs = 0;

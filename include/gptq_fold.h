@@ -168,7 +168,7 @@ gptq_status gptq_q4tp_group(const float* tile, int rows, const float* ublk, cons
  * calls whose work overlaps on the GPU -- on different streams, or from
  * different host threads -- race on it: serialize them.
  */
-#define GPTQ_SWEEP_NOALLOC_SCRATCH_BYTES (24u << 20)
+#define GPTQ_SWEEP_NOALLOC_SCRATCH_BYTES (48u << 20)
 gptq_status gptq_q4tp_sweep_noalloc(float* W, int rows, int n, const float* U, const float* hw,
                                     const float* tab, const float* lost, uint8_t* nibbles,
                                     uint8_t* rungs, float* scales, void* stream);

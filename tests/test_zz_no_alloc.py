@@ -45,7 +45,7 @@ def test_noalloc_sweep_matches_workspace_sweep(lib):
 def test_noalloc_sweep_rejects_oversize(lib):
     from gptq_post_weight_gb300 import _lib
 
-    limit = 24 << 20
+    limit = 48 << 20
     assert lib.gptq_sweep_workspace_bytes(5120, 17408) <= limit
     rows, n = 4096, 24576
     assert lib.gptq_sweep_workspace_bytes(rows, n) > limit
