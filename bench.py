@@ -201,6 +201,89 @@ def run_reference(args, cfg, rank):
     print(json.dumps(line), flush=True)
 
 
+def aggregate(t_local: float, steps: int, world: int, pg=None):
+    """Whole-job seconds per group: the slowest rank's time for `steps` steps
+    (max over ranks), divided by the groups all ranks processed (one group
+    per rank per step).  Returns (t_max, value)."""
+    t = float(t_local)
+    if pg is not None and world > 1:
+        import torch
+
+        tt = torch.tensor([t], dtype=torch.float64)
+        if pg.get_backend() == "nccl":
+            tt = tt.cuda()
+        pg.all_reduce(tt, op=pg.ReduceOp.MAX)
+        t = float(tt.item())
+    return t, t / (steps * world)
+
+
+def run_batch(args, rank, world, dev, lib, _lib, torch, synth):
+    """11 independent n = 17408 groups (seeds 0..10) back to back on one GPU:
+    `--streams` host threads, each with its own CUDA stream and workspace,
+    take groups in turn.  Device-timed from one event that every stream
+    waits on to one event that waits on every stream."""
+    import concurrent.futures as cf
+
+    ngroups = 11
+    cfgs = [synth.config("n17408", seed=i) for i in range(ngroups)]
+    probs = [synth.make_problem(c, dev) for c in cfgs]
+    n, rows = cfgs[0].n, cfgs[0].rows
+    gpr = n // 32
+    S = max(1, args.streams)
+    streams = [torch.cuda.Stream(dev) for _ in range(S)]
+    wss = [_lib.workspace(lib.gptq_group_workspace_bytes(rows, n), dev) for _ in range(S)]
+    outs = [(torch.empty(rows * n // 2, dtype=torch.uint8, device=dev),
+             torch.empty(rows * gpr, dtype=torch.uint8, device=dev),
+             torch.empty(rows * gpr, dtype=torch.float32, device=dev)) for _ in range(S)]
+
+    def lane(i):
+        with torch.cuda.stream(streams[i]):
+            for g in range(i, ngroups, S):
+                hp, w = probs[g]
+                _lib.quantize_group(hp, n, w, cfgs[g].lam, ws=wss[i], want_u=False, stream=streams[i],
+                                    out=outs[i])
+
+    def one_pass(pool):
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        cur = torch.cuda.current_stream(dev)
+        start.record(cur)
+        for st in streams:
+            st.wait_event(start)
+        list(pool.map(lane, range(S)))
+        for st in streams:
+            ev = torch.cuda.Event()
+            ev.record(st)
+            cur.wait_event(ev)
+        end.record(cur)
+        return start, end
+
+    with cf.ThreadPoolExecutor(S) as pool:
+        for _ in range(max(args.warmup, 0)):
+            one_pass(pool)
+        torch.cuda.synchronize()
+        sampler = ClockSampler(dev.index or 0)
+        sampler.start()
+        time.sleep(0.3)
+        l0 = _lib.launch_count()
+        marks = [one_pass(pool) for _ in range(args.steps)]
+        torch.cuda.synchronize()
+        launches = _lib.launch_count() - l0
+        clocks = sampler.stop()
+    t = sum(s.elapsed_time(e) for s, e in marks) / 1e3
+    t_max, value = aggregate(t / ngroups, args.steps, world, None)
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": t / args.steps * 1e3, "higher_is_better": False,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+                "config": {"workload": f"batch: {ngroups} independent groups, each " + workload_desc(cfgs[0]).split(": ", 1)[1]
+                           + f"; seeds 0..{ngroups - 1}; {S} streams", "groups_per_step": ngroups,
+                           "groups_per_s": ngroups * args.steps / t,
+                           "l2": "inputs larger than L2; no flush"},
+                "gpu_launches": launches, "clocks": clocks}
+        print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -214,6 +297,7 @@ def main():
     ap.add_argument("--ref-rows", type=int, default=8)
     ap.add_argument("--n", type=int, default=None, help="override n (T = 2n) for small profiling cases")
     ap.add_argument("--rows", type=int, default=None)
+    ap.add_argument("--streams", type=int, default=2, help="host threads / streams for --config batch")
     args = ap.parse_args()
 
     import synth
@@ -221,7 +305,7 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
-    cfg = synth.config(args.config, seed=rank)
+    cfg = synth.config("n17408" if args.config == "batch" else args.config, seed=rank)
     if args.n is not None:
         cfg = dataclasses.replace(cfg, n=args.n, T=2 * args.n, name=f"{args.config}_n{args.n}")
     if args.rows is not None:
@@ -246,6 +330,9 @@ def main():
         dist.init_process_group("nccl", device_id=dev)
         pg = dist
     lib = _lib.load()
+    if args.config == "batch":
+        run_batch(args, rank, world, dev, lib, _lib, torch, synth)
+        return
 
     hp, w = synth.make_problem(cfg, dev)
     n, rows = cfg.n, cfg.rows
@@ -286,12 +373,7 @@ def main():
     prof = _lib.profile_stop()
     launches = _lib.launch_count() - launches0
     clocks = sampler.stop()
-    t_dev = e0.elapsed_time(e1) / 1e3  # s for K steps on this rank
-    if pg is not None:
-        tt = torch.tensor([t_dev], device=dev, dtype=torch.float64)
-        pg.all_reduce(tt, op=pg.ReduceOp.MAX)
-        t_dev = float(tt.item())
-    value = t_dev / (args.steps * world)
+    t_dev, value = aggregate(e0.elapsed_time(e1) / 1e3, args.steps, world, pg)
 
     # End to end through the public call with host buffers: H2D of the
     # group's inputs from pinned memory, the call, D2H of its outputs.
@@ -316,12 +398,8 @@ def main():
         for _ in range(args.steps):
             e2e_step()
         torch.cuda.synchronize()
-        t_e2e = time.perf_counter() - t0
-        if pg is not None:
-            tt = torch.tensor([t_e2e], device=dev, dtype=torch.float64)
-            pg.all_reduce(tt, op=pg.ReduceOp.MAX)
-            t_e2e = float(tt.item())
-        e2e = {"value": t_e2e / (args.steps * world), "unit": UNIT,
+        t_e2e, v_e2e = aggregate(time.perf_counter() - t0, args.steps, world, pg)
+        e2e = {"value": v_e2e, "unit": UNIT,
                "h2d_bytes_per_step": hp.numel() * 4 + w.numel() * 4,
                "d2h_bytes_per_step": sum(o.numel() * o.element_size() for o in outs)}
 

@@ -30,6 +30,8 @@ SIGNATURES = {
     "gptq_group_workspace_bytes": (_S, [_I, _I]),
     "gptq_quantize_group": (_I, [_P, _I, _D, _P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _S, _P]),
     "gptq_build_equilibrated": (_I, [_P, _I, _D, _P, _P, _P, _S, _P]),
+    "gptq_gram_workspace_bytes": (_S, [_I]),
+    "gptq_gram_add": (_I, [_P, _I, _P, _I, _P, _S, _P]),
     "gptq_launch_count": (ctypes.c_longlong, []),
     "gptq_kernel_kinds": (_I, []),
     "gptq_kernel_kind_name": (ctypes.c_char_p, [_I]),
@@ -245,3 +247,18 @@ def profile_stop():
     if r == -2:
         out["_truncated"] = (0.0, 1)
     return out
+
+
+def gram_add(h_packed, x, ws=None, stream=None):
+    """H_packed += X^T X in place (X [T, n] f32); returns h_packed."""
+    import torch
+
+    lib = load()
+    _cuda_f32(h_packed, "h_packed")
+    _cuda_f32(x, "x")
+    t, n = x.shape
+    if ws is None:
+        ws = workspace(lib.gptq_gram_workspace_bytes(n), x.device)
+    code = lib.gptq_gram_add(_ptr(h_packed), n, _ptr(x), t, _ptr(ws), ws.numel(), _stream(torch, stream))
+    _check("gptq_gram_add", code)
+    return h_packed

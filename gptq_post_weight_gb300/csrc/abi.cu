@@ -22,6 +22,9 @@ gptq_status sweep_run(float* W, int rows, int n, const float* U, const float* hw
                       const float* lost, uint8_t* nib, uint8_t* rungs, float* scales, void* ws,
                       size_t ws_bytes, cudaStream_t s);
 gptq_status noalloc_scratch(void** out);
+size_t gram_ws_bytes(int n);
+gptq_status gram_run(float* Hp, int n, const float* X, int T, void* ws, size_t ws_bytes,
+                     cudaStream_t s);
 }  // namespace gq
 
 using namespace gq;
@@ -156,6 +159,17 @@ gptq_status gptq_quantize_group(const float* H_packed, int n, double lambda, con
   GQ_TRY(copy_dead_zeroed(W, rows, n, hd, wz, s));
   GQ_TRY(ladder_run(wz, rows, n, tb, ls, s));
   return sweep_run(wz, rows, n, u, hd, tb, ls, nibbles, rungs, scales, rest, rest_bytes, s);
+}
+
+size_t gptq_gram_workspace_bytes(int n) { return bad_n(n) ? 0 : gram_ws_bytes(n); }
+
+gptq_status gptq_gram_add(float* H_packed, int n, const float* X, int T, void* ws,
+                          size_t ws_bytes, void* stream) {
+  if (bad_n(n) || T < 0) return GPTQ_ERR_SHAPE;
+  if (!ptr_ok(H_packed) || (T > 0 && !ptr_ok(X)) || ws == nullptr) return GPTQ_ERR_ARG;
+  if (ws_bytes < gram_ws_bytes(n)) return GPTQ_ERR_NOMEM;
+  if (T == 0) return GPTQ_OK;
+  return gram_run(H_packed, n, X, T, ws, ws_bytes, as_stream(stream));
 }
 
 }  // extern "C"

@@ -38,7 +38,7 @@ constexpr int GROUP = 32;
 // Kernel kinds for launch accounting / per-kind timing (gptq_profile_*).
 enum Kind : int {
   K_DIAG = 0, K_BUILD, K_POTRF, K_TRSM, K_FOLD_GEMM, K_LADDER, K_SWEEP_BLOCK, K_PREP_UT,
-  K_SWEEP_GEMM, K_GROUP, K_COPY, K_NKINDS
+  K_SWEEP_GEMM, K_GROUP, K_COPY, K_GRAM_PREP, K_GRAM_GEMM, K_NKINDS
 };
 
 // Every launch site calls prof_begin/prof_end around its <<<>>>: they count
@@ -95,6 +95,7 @@ struct TcJob {
   int c_x0, c_y0;
   int a_map, b_map, a_row0, b_row0;
   int mode, mt, nt, M, N, ntiles;
+  int add;  // 0: C -= A B^T; 1: C += A B^T
 };
 
 struct OperandMaps {
@@ -136,11 +137,24 @@ gptq_status make_c_map(CUtensorMap* m, float* base, long long rows, long long co
 // 128-byte swizzle).  K must be a multiple of 32, base 16-byte aligned.
 gptq_status make_operand_map(CUtensorMap* m, const float* base, long long rows, int K);
 
+// Diagonal-block step fused into an update (fold only): the block at (k, k)
+// of the N x N matrix A (leading dimension lda) must be tile 0 of job 0; its
+// Cholesky inverse goes to Linv and a bad pivot to bit 0 of the status word.
+struct FusedPotrf {
+  const float* A;
+  long long lda;
+  int k;
+  float* Linv;
+  int on;
+};
+
 // Enqueue C -= A B^T for up to two jobs in one persistent launch.
 // `flag`: skip everything when non-zero (may be null).  `status`: bit 1 is
 // set if a device-side wait timed out.
+// kseg > 0: drain the accumulator to C every kseg (multiple of 32) of K.
 gptq_status gemm_tc_sub(const OperandMaps& maps, const TcJob& j0, const TcJob& j1, int K,
-                        const unsigned* flag, unsigned* status, int kind, cudaStream_t s);
+                        const unsigned* flag, unsigned* status, int kind, cudaStream_t s,
+                        const FusedPotrf& fp = FusedPotrf{}, int kseg = 0);
 
 // TF32 split: hi = x rounded to TF32 (10-bit mantissa, nearest, ties away),
 // lo = (x - hi) rounded to TF32; x - hi is exact in f32.

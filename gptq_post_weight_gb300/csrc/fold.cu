@@ -19,13 +19,13 @@
 // A pivot that is not positive (or NaN) sets a device flag; every later
 // kernel of the attempt returns at once, and the host raises lambda.
 #include "common.cuh"
+#include "potrf.cuh"
 
 #include <math.h>
 
 namespace gq {
 namespace {
 
-constexpr int LDS = NB + 1;
 
 __device__ __forceinline__ long long poff(long long r, long long n) { return r * (2 * n - r + 1) / 2; }
 
@@ -111,180 +111,12 @@ __global__ void __launch_bounds__(256) k_build(const float* __restrict__ hp, int
   }
 }
 
-// Cholesky of the NB x NB diagonal block at k (lower) in shared memory, and
-// its inverse.  Factorization in 32-column panels: warp 0 factors the
-// panel's 32 x 32 diagonal block in registers (lane = row; the pivot column
-// travels by shuffles; reciprocal square root, no divisions), the rows below
-// are solved against it (one thread per row), then a rank-32 update of the
-// rest of the block (4 x 4 register tiles).  Pivot test of the fold page's
-// chol_diag: !(piv > 0) (NaN included) -> flag, piv := 1.
-// Inverse ([fold page] inv_diag, blocked): the four 32 x 32 diagonal blocks
-// are inverted by four warps (lane = column), then the off-diagonal blocks
-// by block diagonals: X_ij = -X_ii sum_{j <= m < i} L_im X_mj.
-// Output: Linv (NB x NB, zeros above the diagonal).
+// Standalone launch of the diagonal-block step (the first block of a fold).
 __global__ void __launch_bounds__(256) k_potrf(const float* __restrict__ A, long long lda, int k,
                                                float* __restrict__ Linv, unsigned* flag) {
   if (flagged(flag)) return;
-  extern __shared__ float S[];  // [NB][LDS] L, then [NB][LDS] Linv, then T [NB][LDS]
-  float* Li = S + NB * LDS;
-  float* T = Li + NB * LDS;
-  __shared__ float rinv[NB];
-  __shared__ int bad;
-  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
-  if (tid == 0) bad = 0;
-  // 16 float4 loads per thread, all in flight before the first store.
-  {
-    float4 v[NB * NB / 4 / 256];
-#pragma unroll
-    for (int i = 0; i < NB * NB / 4 / 256; ++i) {
-      const int e = tid + 256 * i, r = e / (NB / 4), c4 = e % (NB / 4);
-      v[i] = *reinterpret_cast<const float4*>(A + (long long)(k + r) * lda + k + 4 * c4);
-    }
-#pragma unroll
-    for (int i = 0; i < NB * NB / 4 / 256; ++i) {
-      const int e = tid + 256 * i, r = e / (NB / 4), c = 4 * (e % (NB / 4));
-      float* dst = S + r * LDS + c;
-      dst[0] = (c <= r) ? v[i].x : 0.f;
-      dst[1] = (c + 1 <= r) ? v[i].y : 0.f;
-      dst[2] = (c + 2 <= r) ? v[i].z : 0.f;
-      dst[3] = (c + 3 <= r) ? v[i].w : 0.f;
-    }
-  }
-  __syncthreads();
-  for (int p = 0; p < NB; p += 32) {
-    if (warp == 0) {
-      float a[32];
-#pragma unroll
-      for (int j = 0; j < 32; ++j) a[j] = S[(p + lane) * LDS + p + j];
-#pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        float piv = __shfl_sync(0xffffffffu, a[c], c);
-        if (!(piv > 0.f)) {
-          piv = 1.f;
-          if (lane == 0) bad = 1;
-        }
-        const float rs = rsqrtf(piv);
-        const float lic = (lane == c) ? piv * rs : a[c] * rs;
-        if (lane >= c) a[c] = lic;
-        if (lane == c) rinv[p + c] = rs;
-#pragma unroll
-        for (int j = 1; j < 32; ++j) {
-          if (j <= c) continue;
-          const float ljc = __shfl_sync(0xffffffffu, lic, j);
-          if (lane >= j) a[j] = fmaf(-lic, ljc, a[j]);
-        }
-      }
-#pragma unroll
-      for (int j = 0; j < 32; ++j)
-        if (j <= lane) S[(p + lane) * LDS + p + j] = a[j];
-    }
-    __syncthreads();
-    const int r = p + 32 + tid;
-    if (r < NB) {
-      float x[32];
-#pragma unroll
-      for (int t = 0; t < 32; ++t) x[t] = S[r * LDS + p + t];
-#pragma unroll
-      for (int t = 0; t < 32; ++t) {
-        float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-        for (int u = 0; u + 1 < t; u += 2) {
-          a0 = fmaf(x[u], S[(p + t) * LDS + p + u], a0);
-          a1 = fmaf(x[u + 1], S[(p + t) * LDS + p + u + 1], a1);
-        }
-        if (t & 1) a0 = fmaf(x[t - 1], S[(p + t) * LDS + p + t - 1], a0);
-        x[t] = (x[t] - (a0 + a1)) * rinv[p + t];
-      }
-#pragma unroll
-      for (int t = 0; t < 32; ++t) S[r * LDS + p + t] = x[t];
-    }
-    __syncthreads();
-    const int m = NB - p - 32;  // rows/cols of the remaining block
-    const int mt = m / 4;
-    const int ntile = mt * (mt + 1) / 2;
-    for (int e = tid; e < ntile; e += 256) {
-      int ti = (int)((sqrtf(8.0f * (float)e + 1.0f) - 1.0f) * 0.5f);
-      while ((ti + 1) * (ti + 2) / 2 <= e) ++ti;
-      while (ti * (ti + 1) / 2 > e) --ti;
-      const int tj = e - ti * (ti + 1) / 2;
-      const int r0 = p + 32 + 4 * ti, c0 = p + 32 + 4 * tj;
-      float acc[4][4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
-#pragma unroll 8
-      for (int t = 0; t < 32; ++t) {
-        float ra[4], rb[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          ra[i] = S[(r0 + i) * LDS + p + t];
-          rb[i] = S[(c0 + i) * LDS + p + t];
-        }
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-          for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(ra[i], rb[j], acc[i][j]);
-      }
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          if (c0 + j <= r0 + i) S[(r0 + i) * LDS + c0 + j] -= acc[i][j];
-    }
-    __syncthreads();
-  }
-  if (bad && tid == 0) atomicOr(flag, 1u);
-  // Inverse.  Diagonal blocks: warp b, lane j = column j of inv(L_bb).
-  for (int e = tid; e < NB * LDS; e += 256) Li[e] = 0.f;
-  __syncthreads();
-  if (warp < 4) {
-    const int b = warp * 32;
-    float x[32];
-#pragma unroll
-    for (int t = 0; t < 32; ++t) {
-      float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-      for (int u = 0; u + 1 < t; u += 2) {
-        a0 = fmaf(S[(b + t) * LDS + b + u], x[u], a0);
-        a1 = fmaf(S[(b + t) * LDS + b + u + 1], x[u + 1], a1);
-      }
-      if (t & 1) a0 = fmaf(S[(b + t) * LDS + b + t - 1], x[t - 1], a0);
-      x[t] = (((t == lane) ? 1.f : 0.f) - (a0 + a1)) * rinv[b + t];
-    }
-#pragma unroll
-    for (int t = 0; t < 32; ++t)
-      if (t >= lane) Li[(b + t) * LDS + b + lane] = x[t];
-  }
-  __syncthreads();
-  // Off-diagonal blocks, one block diagonal d at a time.  Each of the
-  // (4 - d) blocks has 32 x 32 outputs; thread (blk, 4 outputs).
-  for (int d = 1; d < 4; ++d) {
-    const int nblk = 4 - d;
-    // T_ij = sum_{m = j}^{i-1} L_im X_mj  (block rows i = j + d)
-    for (int o = tid; o < nblk * 1024; o += 256) {
-      const int blk = o / 1024, rr = (o % 1024) / 32, cc = o % 32;
-      const int j = blk, i = blk + d;
-      float acc = 0.f;
-      for (int mm = j * 32; mm < i * 32; ++mm) acc = fmaf(S[(i * 32 + rr) * LDS + mm], Li[mm * LDS + j * 32 + cc], acc);
-      T[(i * 32 + rr) * LDS + j * 32 + cc] = acc;
-    }
-    __syncthreads();
-    // X_ij = -X_ii T_ij
-    for (int o = tid; o < nblk * 1024; o += 256) {
-      const int blk = o / 1024, rr = (o % 1024) / 32, cc = o % 32;
-      const int j = blk, i = blk + d;
-      float acc = 0.f;
-#pragma unroll 8
-      for (int u = 0; u <= rr; ++u) acc = fmaf(Li[(i * 32 + rr) * LDS + i * 32 + u], T[(i * 32 + u) * LDS + j * 32 + cc], acc);
-      Li[(i * 32 + rr) * LDS + j * 32 + cc] = -acc;
-    }
-    __syncthreads();
-  }
-  for (int e = tid; e < NB * NB; e += 256) {
-    const int r = e / NB, c = e % NB;
-    Linv[e] = (c <= r) ? Li[r * LDS + c] : 0.f;
-  }
+  extern __shared__ float S[];
+  potrf_inverse_block(A + (long long)k * lda + k, lda, Linv, flag, S);
 }
 
 constexpr int APPLY_ROWS = 64;
@@ -446,7 +278,7 @@ size_t fold_ws_bytes(int n) {
   return c.off + 256;
 }
 
-constexpr int POTRF_SMEM = 3 * NB * LDS * 4;
+constexpr int POTRF_SMEM = POTRF_SMEM_BYTES;
 constexpr int APPLY_SMEM = (NB * NB + APPLY_ROWS * (NB + 4)) * 4;
 
 static gptq_status init_attrs() {
@@ -480,45 +312,48 @@ static gptq_status fold_attempt(const float* hp, const FoldWs& w, const OperandM
   //   one trailing update with K = 2 NB (both panels) for everything right
   //   of / below block k + NB.
   // A last unpaired block runs as a single step (K = NB).
-  auto step = [&](int k, int col0, int zero_end) -> gptq_status {
-    const int s0 = k + NB;
-    {
-      GQ_PROF(K_POTRF, s);
-      k_potrf<<<1, 256, POTRF_SMEM, s>>>(w.A, ld, k, w.Lkk, w.flag);
-      GQ_LAUNCHED();
-    }
+  // The diagonal-block step (Cholesky + inverse of block k) of the first
+  // block runs alone; every later one rides in the update GEMM that finishes
+  // its block (tile 0 of that GEMM is exactly that block).
+  auto apply = [&](int k, int col0, int zero_end) -> gptq_status {
     GQ_PROF(K_TRSM, s);
-    k_apply<<<N / APPLY_ROWS, APPLY_ROWS * 4, APPLY_SMEM, s>>>(w.A, ld, k, s0, N, col0, zero_end,
+    k_apply<<<N / APPLY_ROWS, APPLY_ROWS * 4, APPLY_SMEM, s>>>(w.A, ld, k, k + NB, N, col0, zero_end,
                                                                w.Lkk, w.P_hi, w.P_lo, w.Yp_hi,
                                                                w.Yp_lo, w.flag, U, w.dabs, n);
     GQ_LAUNCHED();
     return GPTQ_OK;
   };
+  auto fused = [&](int k) { return FusedPotrf{w.A, ld, k, w.Lkk, 1}; };
+  {
+    GQ_PROF(K_POTRF, s);
+    k_potrf<<<1, 256, POTRF_SMEM, s>>>(w.A, ld, 0, w.Lkk, w.flag);
+    GQ_LAUNCHED();
+  }
   // maps: 0/1 = P hi/lo, 2/3 = Yp hi/lo (K = 2 NB wide).
   int k = 0;
   while (k < N) {
     if (k + 2 * NB <= N) {
       const int k1 = k + NB, s1 = k + 2 * NB;
-      GQ_TRY(step(k, 0, s1));
+      GQ_TRY(apply(k, 0, s1));
       {
         const TcJob syrk = tc_strip(k1, k1, 0, k1, 0, k1, N - k1, NB);
         const TcJob inv = tc_rect(k1, 0, 2, 0, 0, k1, k1, NB);
-        GQ_TRY(gemm_tc_sub(maps, syrk, inv, NB, w.flag, w.flag, K_FOLD_GEMM, s));
+        GQ_TRY(gemm_tc_sub(maps, syrk, inv, NB, w.flag, w.flag, K_FOLD_GEMM, s, fused(k1)));
       }
-      GQ_TRY(step(k1, NB, 0));
+      GQ_TRY(apply(k1, NB, 0));
       if (s1 < N) {
         const TcJob syrk = tc_lower(s1, s1, 0, s1, N - s1);
         const TcJob inv = tc_rect(s1, 0, 2, 0, 0, s1, s1, N - s1);
-        GQ_TRY(gemm_tc_sub(maps, syrk, inv, 2 * NB, w.flag, w.flag, K_FOLD_GEMM, s));
+        GQ_TRY(gemm_tc_sub(maps, syrk, inv, 2 * NB, w.flag, w.flag, K_FOLD_GEMM, s, fused(s1)));
       }
       k = s1;
     } else {
       const int s0 = k + NB;
-      GQ_TRY(step(k, 0, 0));
+      GQ_TRY(apply(k, 0, 0));
       if (s0 < N) {
         const TcJob syrk = tc_lower(s0, s0, 0, s0, N - s0);
         const TcJob inv = tc_rect(s0, 0, 2, 0, 0, s0, s0, N - s0);
-        GQ_TRY(gemm_tc_sub(maps, syrk, inv, NB, w.flag, w.flag, K_FOLD_GEMM, s));
+        GQ_TRY(gemm_tc_sub(maps, syrk, inv, NB, w.flag, w.flag, K_FOLD_GEMM, s, fused(s0)));
       }
       k = s0;
     }

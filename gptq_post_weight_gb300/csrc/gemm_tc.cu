@@ -23,7 +23,13 @@
 // Every wait is bounded (about 2 s of globaltimer); on expiry the kernel
 // stops issuing, drains what it started, frees TMEM and sets bit 1 of the
 // status word.
+// Fused diagonal-block step: in the fold every update's first tile is the
+// next 128 x 128 diagonal block.  With `fp.on`, CTA 0 computes only that
+// tile (the other CTAs share the rest), waits for its reduce-add to land,
+// then factors and inverts the block in its own shared memory while the
+// other CTAs finish the update.
 #include "common.cuh"
+#include "potrf.cuh"
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -200,8 +206,8 @@ __device__ __forceinline__ void tile_of(const TcJob& J, int t, int& ti, int& tj)
 __global__ void __launch_bounds__(THREADS, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap m0, const __grid_constant__ CUtensorMap m1,
               const __grid_constant__ CUtensorMap m2, const __grid_constant__ CUtensorMap m3,
-              const __grid_constant__ CUtensorMap cmap, TcJob j0, TcJob j1, int K,
-              const unsigned* flag, unsigned* status) {
+              const __grid_constant__ CUtensorMap cmap, TcJob j0, TcJob j1, int K, int kseg,
+              const unsigned* flag, unsigned* status, FusedPotrf fp) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ __align__(8) uint64_t full[STAGES], empty[STAGES], tfull[2], tempty[2], drain;
@@ -217,6 +223,20 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int total = j0.ntiles + j1.ntiles;
   const int nk = K / BK;
+  // Split-K within a tile: the accumulator is drained to C (reduce-add,
+  // round-to-nearest in L2) every `segc` chunks, which bounds how many MMAs
+  // accumulate into one f32 TMEM value before it is rounded properly.
+  const int segc = (kseg > 0 && kseg / BK < nk) ? kseg / BK : nk;
+  const int nseg = (nk + segc - 1) / segc;
+  // Tile sequence of this CTA: t0, t0 + tstride, ...
+  int t0 = blockIdx.x, tstride = gridDim.x;
+  if (fp.on) {
+    if (blockIdx.x == 0) {
+      tstride = total;  // tile 0 only
+    } else {
+      tstride = gridDim.x - 1;
+    }
+  }
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
@@ -250,7 +270,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       const CUtensorMap* maps[4] = {&m0, &m1, &m2, &m3};
       int stage = 0, issued = 0;
       uint32_t phase = 0;
-      for (int t = blockIdx.x; t < total && !*abort; t += gridDim.x) {
+      for (int t = t0; t < total && !*abort; t += tstride) {
         const bool second = t >= j0.ntiles;
         const TcJob& J = second ? j1 : j0;
         int ti, tj;
@@ -281,39 +301,46 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (lane == 0) {
       int stage = 0, acc = 0, consumed = 0;
       uint32_t phase = 0, aphase = 0;
-      for (int t = blockIdx.x; t < total && !*abort; t += gridDim.x) {
-        if (!mbar_wait(&tempty[acc], aphase ^ 1u, abort)) break;
-        tc_fence_after();
-        const uint32_t d = tmem + (uint32_t)(acc * BN);
+      for (int t = t0; t < total && !*abort; t += tstride) {
         bool ok = true;
-        for (int c = 0; c < nk; ++c) {
-          if (!mbar_wait(&full[stage], phase, abort)) {
+        for (int sg = 0; sg < nseg && ok; ++sg) {
+          if (!mbar_wait(&tempty[acc], aphase ^ 1u, abort)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t a_hi = smem_u32(smem + stage * STAGE_BYTES);
-          const uint32_t a_lo = a_hi + TILE_A, b_hi = a_hi + 2 * TILE_A, b_lo = b_hi + TILE_B;
+          const uint32_t d = tmem + (uint32_t)(acc * BN);
+          const int cend = (sg + 1) * segc < nk ? (sg + 1) * segc : nk;
+          for (int c = sg * segc; c < cend; ++c) {
+            if (!mbar_wait(&full[stage], phase, abort)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t a_hi = smem_u32(smem + stage * STAGE_BYTES);
+            const uint32_t a_lo = a_hi + TILE_A, b_hi = a_hi + 2 * TILE_A, b_lo = b_hi + TILE_B;
 #pragma unroll
-          for (int kk = 0; kk < BK / 8; ++kk) {
-            const uint32_t off = (uint32_t)kk * 32u;
-            mma_tf32(d, sdesc(a_lo + off), sdesc(b_hi + off), (c | kk) ? 1u : 0u);
-            mma_tf32(d, sdesc(a_hi + off), sdesc(b_lo + off), 1u);
-            mma_tf32(d, sdesc(a_hi + off), sdesc(b_hi + off), 1u);
+            for (int kk = 0; kk < BK / 8; ++kk) {
+              const uint32_t off = (uint32_t)kk * 32u;
+              mma_tf32(d, sdesc(a_lo + off), sdesc(b_hi + off), (c > sg * segc || kk) ? 1u : 0u);
+              mma_tf32(d, sdesc(a_hi + off), sdesc(b_lo + off), 1u);
+              mma_tf32(d, sdesc(a_hi + off), sdesc(b_hi + off), 1u);
+            }
+            mma_commit(&empty[stage]);
+            ++consumed;
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
           }
-          mma_commit(&empty[stage]);
-          ++consumed;
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
+          if (!ok) break;
+          mma_commit(&tfull[acc]);
+          if (++acc == 2) {
+            acc = 0;
+            aphase ^= 1u;
           }
         }
         if (!ok) break;
-        mma_commit(&tfull[acc]);
-        if (++acc == 2) {
-          acc = 0;
-          aphase ^= 1u;
-        }
       }
       consumed_sh = consumed;
       // Every MMA this thread issued has completed once `drain` flips.
@@ -331,10 +358,15 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint8_t* cstage = smem + STAGES * STAGE_BYTES;
     int acc = 0, chunk = 0;
     uint32_t aphase = 0;
-    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+    bool go = true;
+    for (int w = t0 * nseg; go && w < total * nseg; w += (w % nseg == nseg - 1) ? (tstride - 1) * nseg + 1 : 1) {
+      const int t = w / nseg;
       // All 128 epilogue threads agree before any of them reaches the
       // .sync.aligned loads or the named barriers below.
-      if (!epi_all(mbar_wait(&tfull[acc], aphase, abort))) break;
+      if (!epi_all(mbar_wait(&tfull[acc], aphase, abort))) {
+        go = false;
+        break;
+      }
       tc_fence_after();
       const bool second = t >= j0.ntiles;
       const TcJob& J = second ? j1 : j0;
@@ -356,10 +388,10 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
         for (int c4 = 0; c4 < 8; ++c4) {
           float4 o;
-          o.x = -__uint_as_float(v[4 * c4]);
-          o.y = -__uint_as_float(v[4 * c4 + 1]);
-          o.z = -__uint_as_float(v[4 * c4 + 2]);
-          o.w = -__uint_as_float(v[4 * c4 + 3]);
+          o.x = J.add ? __uint_as_float(v[4 * c4]) : -__uint_as_float(v[4 * c4]);
+          o.y = J.add ? __uint_as_float(v[4 * c4 + 1]) : -__uint_as_float(v[4 * c4 + 1]);
+          o.z = J.add ? __uint_as_float(v[4 * c4 + 2]) : -__uint_as_float(v[4 * c4 + 2]);
+          o.w = J.add ? __uint_as_float(v[4 * c4 + 3]) : -__uint_as_float(v[4 * c4 + 3]);
           if (diag) {  // lower triangle only: add nothing above the diagonal
             const int c0 = cc + 4 * c4;
             if (c0 > rr) o.x = 0.f;
@@ -404,6 +436,16 @@ __global__ void __launch_bounds__(THREADS, 1)
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS)
                  : "memory");
+  }
+  if (fp.on && blockIdx.x == 0 && !abort_sh) {
+    // The epilogue leader waited for its reduce-adds (wait_group 0); make
+    // the tensor core's global writes visible to plain loads, then run the
+    // diagonal-block step on the finished tile (shared memory is free: every
+    // load has landed and every MMA has retired).
+    if (threadIdx.x == 64) asm volatile("fence.proxy.async.global;" ::: "memory");
+    __syncthreads();
+    potrf_inverse_block(fp.A + (long long)fp.k * fp.lda + fp.k, fp.lda, fp.Linv, status,
+                        reinterpret_cast<float*>(smem));
   }
 }
 
@@ -462,7 +504,8 @@ gptq_status make_c_map(CUtensorMap* m, float* base, long long rows, long long co
 }
 
 gptq_status gemm_tc_sub(const OperandMaps& maps, const TcJob& j0, const TcJob& j1, int K,
-                        const unsigned* flag, unsigned* status, int kind, cudaStream_t s) {
+                        const unsigned* flag, unsigned* status, int kind, cudaStream_t s,
+                        const FusedPotrf& fp, int kseg) {
   static bool attr = false;
   if (!attr) {
     GQ_CUDA(cudaFuncSetAttribute(k_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES));
@@ -474,7 +517,7 @@ gptq_status gemm_tc_sub(const OperandMaps& maps, const TcJob& j0, const TcJob& j
   const int grid = total < num_sms() ? total : num_sms();
   GQ_PROF(kind, s);
   k_gemm_tc<<<grid, THREADS, SMEM_BYTES, s>>>(maps.m[0], maps.m[1], maps.m[2], maps.m[3], maps.c, j0,
-                                              j1, K, flag, status);
+                                              j1, K, kseg, flag, status, fp);
   GQ_LAUNCHED();
   return GPTQ_OK;
 }

@@ -1,0 +1,195 @@
+// Cholesky factor and inverse of one NB x NB diagonal block (the fold's
+// diagonal-block step), shared by the standalone kernel (first block) and
+// the update GEMM, which runs it on the block its first tile just finished.
+#pragma once
+
+#include "common.cuh"
+
+namespace gq {
+
+constexpr int LDS = NB + 1;
+constexpr int POTRF_SMEM_BYTES = 3 * NB * LDS * 4;
+
+// Cholesky of the NB x NB diagonal block at k (lower) in shared memory, and
+// its inverse.  Factorization in 32-column panels: warp 0 factors the
+// panel's 32 x 32 diagonal block in registers (lane = row; the pivot column
+// travels by shuffles; reciprocal square root, no divisions), the rows below
+// are solved against it (one thread per row), then a rank-32 update of the
+// rest of the block (4 x 4 register tiles).  Pivot test of the fold page's
+// chol_diag: !(piv > 0) (NaN included) -> flag, piv := 1.
+// Inverse ([fold page] inv_diag, blocked): the four 32 x 32 diagonal blocks
+// are inverted by four warps (lane = column), then the off-diagonal blocks
+// by block diagonals: X_ij = -X_ii sum_{j <= m < i} L_im X_mj.
+// Output: Linv (NB x NB, zeros above the diagonal).
+// Runs on the whole CTA (any multiple of 32 threads >= 128); S is at least
+// POTRF_SMEM_BYTES of shared memory.  The block starts at Ablk (leading
+// dimension lda); it is read with L1-bypassing loads.
+static __device__ __noinline__ void potrf_inverse_block(const float* __restrict__ Ablk, long long lda,
+                                                 float* __restrict__ Linv, unsigned* flag, float* S) {
+  float* Li = S + NB * LDS;
+  float* T = Li + NB * LDS;
+  __shared__ float rinv[NB];
+  __shared__ int bad;
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  const int NT = blockDim.x;
+  if (tid == 0) bad = 0;
+  // 16 float4 loads per thread, all in flight before the first store.
+  {
+#pragma unroll 1
+    for (int b0 = 0; b0 < NB * NB / 4; b0 += 8 * NT) {
+      float4 v[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int e = b0 + tid + NT * i, r = e / (NB / 4), c4 = e % (NB / 4);
+        if (e < NB * NB / 4) v[i] = __ldcg(reinterpret_cast<const float4*>(Ablk + (long long)r * lda + 4 * c4));
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int e = b0 + tid + NT * i, r = e / (NB / 4), c = 4 * (e % (NB / 4));
+        if (e >= NB * NB / 4) continue;
+        float* dst = S + r * LDS + c;
+        dst[0] = (c <= r) ? v[i].x : 0.f;
+        dst[1] = (c + 1 <= r) ? v[i].y : 0.f;
+        dst[2] = (c + 2 <= r) ? v[i].z : 0.f;
+        dst[3] = (c + 3 <= r) ? v[i].w : 0.f;
+      }
+    }
+  }
+  __syncthreads();
+  for (int p = 0; p < NB; p += 32) {
+    if (warp == 0) {
+      float a[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) a[j] = S[(p + lane) * LDS + p + j];
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        float piv = __shfl_sync(0xffffffffu, a[c], c);
+        if (!(piv > 0.f)) {
+          piv = 1.f;
+          if (lane == 0) bad = 1;
+        }
+        const float rs = rsqrtf(piv);
+        const float lic = (lane == c) ? piv * rs : a[c] * rs;
+        if (lane >= c) a[c] = lic;
+        if (lane == c) rinv[p + c] = rs;
+#pragma unroll
+        for (int j = 1; j < 32; ++j) {
+          if (j <= c) continue;
+          const float ljc = __shfl_sync(0xffffffffu, lic, j);
+          if (lane >= j) a[j] = fmaf(-lic, ljc, a[j]);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (j <= lane) S[(p + lane) * LDS + p + j] = a[j];
+    }
+    __syncthreads();
+    for (int r = p + 32 + tid; r < NB; r += NT) {
+      float x[32];
+#pragma unroll
+      for (int t = 0; t < 32; ++t) x[t] = S[r * LDS + p + t];
+#pragma unroll
+      for (int t = 0; t < 32; ++t) {
+        float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+        for (int u = 0; u + 1 < t; u += 2) {
+          a0 = fmaf(x[u], S[(p + t) * LDS + p + u], a0);
+          a1 = fmaf(x[u + 1], S[(p + t) * LDS + p + u + 1], a1);
+        }
+        if (t & 1) a0 = fmaf(x[t - 1], S[(p + t) * LDS + p + t - 1], a0);
+        x[t] = (x[t] - (a0 + a1)) * rinv[p + t];
+      }
+#pragma unroll
+      for (int t = 0; t < 32; ++t) S[r * LDS + p + t] = x[t];
+    }
+    __syncthreads();
+    const int m = NB - p - 32;  // rows/cols of the remaining block
+    const int mt = m / 4;
+    const int ntile = mt * (mt + 1) / 2;
+    for (int e = tid; e < ntile; e += NT) {
+      int ti = (int)((sqrtf(8.0f * (float)e + 1.0f) - 1.0f) * 0.5f);
+      while ((ti + 1) * (ti + 2) / 2 <= e) ++ti;
+      while (ti * (ti + 1) / 2 > e) --ti;
+      const int tj = e - ti * (ti + 1) / 2;
+      const int r0 = p + 32 + 4 * ti, c0 = p + 32 + 4 * tj;
+      float acc[4][4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+#pragma unroll 8
+      for (int t = 0; t < 32; ++t) {
+        float ra[4], rb[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          ra[i] = S[(r0 + i) * LDS + p + t];
+          rb[i] = S[(c0 + i) * LDS + p + t];
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(ra[i], rb[j], acc[i][j]);
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (c0 + j <= r0 + i) S[(r0 + i) * LDS + c0 + j] -= acc[i][j];
+    }
+    __syncthreads();
+  }
+  if (bad && tid == 0) atomicOr(flag, 1u);
+  // Inverse.  Diagonal blocks: warp b, lane j = column j of inv(L_bb).
+  for (int e = tid; e < NB * LDS; e += NT) Li[e] = 0.f;
+  __syncthreads();
+  if (warp < 4) {
+    const int b = warp * 32;
+    float x[32];
+#pragma unroll
+    for (int t = 0; t < 32; ++t) {
+      float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+      for (int u = 0; u + 1 < t; u += 2) {
+        a0 = fmaf(S[(b + t) * LDS + b + u], x[u], a0);
+        a1 = fmaf(S[(b + t) * LDS + b + u + 1], x[u + 1], a1);
+      }
+      if (t & 1) a0 = fmaf(S[(b + t) * LDS + b + t - 1], x[t - 1], a0);
+      x[t] = (((t == lane) ? 1.f : 0.f) - (a0 + a1)) * rinv[b + t];
+    }
+#pragma unroll
+    for (int t = 0; t < 32; ++t)
+      if (t >= lane) Li[(b + t) * LDS + b + lane] = x[t];
+  }
+  __syncthreads();
+  // Off-diagonal blocks, one block diagonal d at a time.  Each of the
+  // (4 - d) blocks has 32 x 32 outputs; thread (blk, 4 outputs).
+  for (int d = 1; d < 4; ++d) {
+    const int nblk = 4 - d;
+    // T_ij = sum_{m = j}^{i-1} L_im X_mj  (block rows i = j + d)
+    for (int o = tid; o < nblk * 1024; o += NT) {
+      const int blk = o / 1024, rr = (o % 1024) / 32, cc = o % 32;
+      const int j = blk, i = blk + d;
+      float acc = 0.f;
+      for (int mm = j * 32; mm < i * 32; ++mm) acc = fmaf(S[(i * 32 + rr) * LDS + mm], Li[mm * LDS + j * 32 + cc], acc);
+      T[(i * 32 + rr) * LDS + j * 32 + cc] = acc;
+    }
+    __syncthreads();
+    // X_ij = -X_ii T_ij
+    for (int o = tid; o < nblk * 1024; o += NT) {
+      const int blk = o / 1024, rr = (o % 1024) / 32, cc = o % 32;
+      const int j = blk, i = blk + d;
+      float acc = 0.f;
+#pragma unroll 8
+      for (int u = 0; u <= rr; ++u) acc = fmaf(Li[(i * 32 + rr) * LDS + i * 32 + u], T[(i * 32 + u) * LDS + j * 32 + cc], acc);
+      Li[(i * 32 + rr) * LDS + j * 32 + cc] = -acc;
+    }
+    __syncthreads();
+  }
+  for (int e = tid; e < NB * NB; e += NT) {
+    const int r = e / NB, c = e % NB;
+    Linv[e] = (c <= r) ? Li[r * LDS + c] : 0.f;
+  }
+}
+
+
+}  // namespace gq

@@ -19,7 +19,8 @@ int g_used = 0;
 int g_open = -1;
 
 const char* kNames[K_NKINDS] = {"diag", "build", "potrf", "trsm", "fold_gemm", "ladder",
-                                "sweep_block", "prep_ut", "sweep_gemm", "group", "copy"};
+                                "sweep_block", "prep_ut", "sweep_gemm", "group", "copy",
+                                "gram_prep", "gram_gemm"};
 
 }  // namespace
 

@@ -199,6 +199,23 @@ gptq_status gptq_build_equilibrated(const float* H_packed, int n, double lambda,
                                     float* D, void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * gptq_gram_add -- calibration Hessian accumulation H += X^T X for one window
+ * of tokens ([host page] calibration pass: gram_alloc / gram_add_dev, one
+ * accumulator per linear input; [fold page] poff: the packed layout).  The
+ * pages sum over tokens and keep the token count apart: no normalization.
+ *
+ *   H_packed in/out f32 n(n+1)/2, upper triangle by rows (as gptq_fold reads).
+ *   X        in     f32 T*n row-major (token t, channel i at X[t*n + i]).
+ *   T >= 0 tokens (T == 0: nothing to do).  ws >= gptq_gram_workspace_bytes(n)
+ *   (a dense n x n scratch plus two n x 4096 operand slices).
+ * Products on the tensor cores with the 3xTF32 split, f32 accumulation;
+ * reads back a 4-byte status word (stream synchronisation) at the end.
+ */
+size_t gptq_gram_workspace_bytes(int n);
+gptq_status gptq_gram_add(float* H_packed, int n, const float* X, int T, void* ws,
+                          size_t ws_bytes, void* stream);
+
+/*
  * Tracing: launch accounting and per-kernel timing.  Every kernel launch of
  * the library is counted; between gptq_profile_start and gptq_profile_stop
  * each launch is also bracketed by a pair of CUDA events recorded on the

@@ -19,6 +19,8 @@ item):
   full-row update ``w[j+1..] -= e * U[j, j+1..]`` right after each column).
 * ``cortiq-engine src/gpu_wgpu/gptq_dev.rs``, ``build_a``: the equilibrated,
   reversed, damped matrix (only to check the library's builder step).
+* ``cortiq-cli src/gptq.rs``, the calibration pass (``gram_add_dev``): the
+  Hessian accumulator H += X^T X over a window of tokens, packed upper.
 
 Readings of points the pages leave open are stated where they are used
 (``ladder`` for the missing converter ladder, ``nominal_rung`` for the f32
@@ -44,3 +46,4 @@ from .q4tp import (  # noqa: F401
     output_error,
     nibbles_to_codes,
 )
+from .gram import gram_add, pack_upper  # noqa: F401,E402

@@ -274,3 +274,26 @@ def test_full_size_group(lib, name):
     assert agree >= 0.999, agree
     assert rung_agree >= 0.999, rung_agree
     assert abs(e_dev - e_or) <= 0.01 * e_or, (e_dev, e_or)
+
+
+@pytest.mark.slow
+def test_full_size_rank_deficient_retry(lib):
+    """The n = 17408 group drawn from T = n/2 samples (rank n/2) with
+    lambda = 0: the first factorization must fail and the damping rise
+    (0 -> 1e-4 -> x10); the device may need one x10 step more than the f64
+    oracle, never less.  U is compared with the oracle at the damping the
+    device used."""
+    from gptq_post_weight_gb300 import _lib
+
+    cfg = synth.rank_deficient(synth.config("n17408"))
+    hpd = synth.make_h_packed(cfg, DEV)
+    u, d, hd, lam = _lib.fold(hpd, cfg.n, 0.0)
+    hp = np_(hpd)
+    del hpd
+    lamo = oracle.fold(hp, cfg.n, 0.0)[3]
+    assert lam >= 1e-4
+    assert lamo <= lam <= 10 * lamo * (1 + 1e-12)
+    uo = oracle.fold(hp, cfg.n, lam)[0]
+    err = rel_fro(np_(u), uo)
+    print(f"rank-deficient n={cfg.n}: lambda device {lam:g}, oracle {lamo:g}, U rel err {err:.2e}")
+    assert err <= 1e-4
