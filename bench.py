@@ -284,6 +284,57 @@ def run_batch(args, rank, world, dev, lib, _lib, torch, synth):
         print(json.dumps(line), flush=True)
 
 
+def run_gram(args, rank, world, dev, lib, _lib, torch, synth):
+    """The calibration step in front of the fold: H += X^T X for one window
+    of T = 32768 tokens at n = 17408 (X = the group's activations as
+    [tokens, channels]), into a packed H resident in HBM."""
+    cfg = synth.config("n17408", seed=rank)
+    n, T = cfg.n, cfg.T
+    x = synth.make_x(cfg, dev).T.contiguous()  # [T, n]
+    hp = torch.zeros(n * (n + 1) // 2, dtype=torch.float32, device=dev)
+    ws = _lib.workspace(lib.gptq_gram_workspace_bytes(n), dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(max(args.warmup, 0)):
+        _lib.gram_add(hp, x, ws=ws, stream=stream)
+    torch.cuda.synchronize()
+    sampler = ClockSampler(dev.index or 0)
+    sampler.start()
+    time.sleep(0.3)
+    l0 = _lib.launch_count()
+    _lib.profile_start(100000)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        _lib.gram_add(hp, x, ws=ws, stream=stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    prof = _lib.profile_stop()
+    launches = _lib.launch_count() - l0
+    clocks = sampler.stop()
+    t, value = aggregate(e0.elapsed_time(e1) / 1e3, args.steps, world, None)
+    flops = n * (n + 1) // 2 * 2 * T
+    pk, src = peaks()
+    peak = pk.get("bf16_tflops_sustained", pk.get("bf16_tflops")) * TF32_PER_BF16 / 3.0
+    ms_g, cnt_g = prof.get("gram_gemm", (0.0, 0))
+    ach = flops * args.steps / (ms_g / 1e3) / 1e12 if ms_g > 0 else None
+    if rank == 0:
+        line = {"metric": "s per calibration window: H += X^T X at n=17408, T=32768 tokens", "value": value,
+                "unit": "s/window", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": t / args.steps * 1e3, "higher_is_better": False, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+                "config": {"workload": f"Gram accumulation, X [{T}, {n}] f32 (the n17408 group's activations), "
+                                       "H packed upper f32", "l2": "inputs larger than L2; no flush"},
+                "roofline": {"bound": "tensor", "kernel": "gram_gemm", "achieved": ach, "peak": peak,
+                             "unit": "TFLOP/s", "frac": (ach / peak) if ach else None, "traffic": None,
+                             "flop_per_launch": flops * args.steps / max(cnt_g, 1)},
+                "tflops_whole_call": flops / (t / args.steps) / 1e12,
+                "per_kernel": {k: {"ms_per_step": v[0] / args.steps, "launches_per_step": v[1] / args.steps}
+                               for k, v in prof.items() if not k.startswith("_") and v[1] > 0},
+                "gpu_launches": launches, "clocks": clocks}
+        print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -305,7 +356,7 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
-    cfg = synth.config("n17408" if args.config == "batch" else args.config, seed=rank)
+    cfg = synth.config("n17408" if args.config in ("batch", "gram") else args.config, seed=rank)
     if args.n is not None:
         cfg = dataclasses.replace(cfg, n=args.n, T=2 * args.n, name=f"{args.config}_n{args.n}")
     if args.rows is not None:
@@ -332,6 +383,9 @@ def main():
     lib = _lib.load()
     if args.config == "batch":
         run_batch(args, rank, world, dev, lib, _lib, torch, synth)
+        return
+    if args.config == "gram":
+        run_gram(args, rank, world, dev, lib, _lib, torch, synth)
         return
 
     hp, w = synth.make_problem(cfg, dev)

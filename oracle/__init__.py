@@ -21,6 +21,8 @@ item):
   reversed, damped matrix (only to check the library's builder step).
 * ``cortiq-cli src/gptq.rs``, the calibration pass (``gram_add_dev``): the
   Hessian accumulator H += X^T X over a window of tokens, packed upper.
+* ``cortiq-cli src/gptq.rs``, ``act_order_perm`` / ``permute_sym`` /
+  ``gptq_quantize_q4tp_act_order``: act-order with static groups.
 
 Readings of points the pages leave open are stated where they are used
 (``ladder`` for the missing converter ladder, ``nominal_rung`` for the f32
@@ -47,3 +49,10 @@ from .q4tp import (  # noqa: F401
     nibbles_to_codes,
 )
 from .gram import gram_add, pack_upper  # noqa: F401,E402
+from .actorder import (  # noqa: F401,E402
+    act_order_perm,
+    converter_rungs,
+    permute_packed,
+    sweep_q4tp_act_order,
+    total_cmp_key,
+)
