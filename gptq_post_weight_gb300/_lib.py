@@ -30,6 +30,13 @@ SIGNATURES = {
     "gptq_group_workspace_bytes": (_S, [_I, _I]),
     "gptq_quantize_group": (_I, [_P, _I, _D, _P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _S, _P]),
     "gptq_build_equilibrated": (_I, [_P, _I, _D, _P, _P, _P, _S, _P]),
+    "gptq_act_order_perm": (_I, [_P, _I, _P, _P]),
+    "gptq_fold_permuted": (_I, [_P, _I, _D, _P, _P, _P, _P, _P, _P, _S, _P]),
+    "gptq_static_rungs": (_I, [_P, _I, _I, _P, _P, _P, _P, _P]),
+    "gptq_sweep_act_order_workspace_bytes": (_S, [_I, _I]),
+    "gptq_q4tp_sweep_act_order": (_I, [_P, _I, _I, _P, _P, _P, _P, _P, _P, _S, _P]),
+    "gptq_group_act_order_workspace_bytes": (_S, [_I, _I]),
+    "gptq_quantize_group_act_order": (_I, [_P, _I, _D, _P, _I, _P, _P, _P, _P, _P, _P, _P, _S, _P]),
     "gptq_gram_workspace_bytes": (_S, [_I]),
     "gptq_gram_add": (_I, [_P, _I, _P, _I, _P, _S, _P]),
     "gptq_launch_count": (ctypes.c_longlong, []),
@@ -262,3 +269,79 @@ def gram_add(h_packed, x, ws=None, stream=None):
     code = lib.gptq_gram_add(_ptr(h_packed), n, _ptr(x), t, _ptr(ws), ws.numel(), _stream(torch, stream))
     _check("gptq_gram_add", code)
     return h_packed
+
+
+def act_order_perm(hdiag):
+    import torch
+
+    lib = load()
+    _cuda_f32(hdiag, "hdiag")
+    n = hdiag.numel()
+    perm = torch.empty(n, dtype=torch.int32, device=hdiag.device)
+    _check("gptq_act_order_perm", lib.gptq_act_order_perm(_ptr(hdiag), n, _ptr(perm), _stream(torch)))
+    return perm
+
+
+def fold_permuted(h_packed, n, perm, lam=0.01):
+    """U, D, hdiag (permuted order), lambda_used of H[perm][perm]."""
+    import torch
+
+    lib = load()
+    dev = h_packed.device
+    u = torch.empty(n, n, dtype=torch.float32, device=dev)
+    d = torch.empty(n, dtype=torch.float32, device=dev)
+    hd = torch.empty(n, dtype=torch.float32, device=dev)
+    ws = workspace(lib.gptq_fold_workspace_bytes(n), dev)
+    lam_used = ctypes.c_double(0.0)
+    code = lib.gptq_fold_permuted(_ptr(h_packed), n, float(lam), _ptr(perm), _ptr(u), _ptr(d), _ptr(hd),
+                                  ctypes.byref(lam_used), _ptr(ws), ws.numel(), _stream(torch))
+    _check("gptq_fold_permuted", code)
+    return u, d, hd, lam_used.value
+
+
+def static_rungs(w, tab, lost):
+    import torch
+
+    lib = load()
+    rows, n = w.shape
+    rungs = torch.empty(rows * (n // 32), dtype=torch.uint8, device=w.device)
+    scales = torch.empty(rows * (n // 32), dtype=torch.float32, device=w.device)
+    code = lib.gptq_static_rungs(_ptr(w), rows, n, _ptr(tab), _ptr(lost), _ptr(rungs), _ptr(scales),
+                                 _stream(torch))
+    _check("gptq_static_rungs", code)
+    return rungs, scales
+
+
+def q4tp_sweep_act_order(w, u, perm, tab, rungs):
+    import torch
+
+    lib = load()
+    rows, n = w.shape
+    nib = torch.empty(rows * n // 2, dtype=torch.uint8, device=w.device)
+    ws = workspace(lib.gptq_sweep_act_order_workspace_bytes(rows, n), w.device)
+    code = lib.gptq_q4tp_sweep_act_order(_ptr(w), rows, n, _ptr(u), _ptr(perm), _ptr(tab), _ptr(rungs),
+                                         _ptr(nib), _ptr(ws), ws.numel(), _stream(torch))
+    _check("gptq_q4tp_sweep_act_order", code)
+    return nib
+
+
+def quantize_group_act_order(h_packed, n, w, lam=0.01, ws=None, want_u=True, stream=None):
+    import torch
+
+    lib = load()
+    _cuda_f32(h_packed, "h_packed")
+    _cuda_f32(w, "w")
+    rows = w.shape[0]
+    dev = w.device
+    nib, rungs, scales = _outs(torch, rows, n, dev)
+    perm = torch.empty(n, dtype=torch.int32, device=dev)
+    u = torch.empty(n, n, dtype=torch.float32, device=dev) if want_u else None
+    if ws is None:
+        ws = workspace(lib.gptq_group_act_order_workspace_bytes(rows, n), dev)
+    lam_used = ctypes.c_double(0.0)
+    code = lib.gptq_quantize_group_act_order(_ptr(h_packed), n, float(lam), _ptr(w), rows, _ptr(nib),
+                                             _ptr(rungs), _ptr(scales), _ptr(perm), _ptr(u),
+                                             ctypes.byref(lam_used), _ptr(ws), ws.numel(),
+                                             _stream(torch, stream))
+    _check("gptq_quantize_group_act_order", code)
+    return dict(nibbles=nib, rungs=rungs, scales=scales, perm=perm, u=u, lam=lam_used.value)

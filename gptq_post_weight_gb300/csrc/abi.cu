@@ -9,7 +9,16 @@ namespace gq {
 size_t fold_ws_bytes(int n);
 size_t sweep_ws_bytes(int rows, int n);
 gptq_status fold_run(const float* hp, int n, double lambda, float* U, float* D, float* hdiag,
-                     double* lambda_used, void* ws, size_t ws_bytes, cudaStream_t s);
+                     double* lambda_used, void* ws, size_t ws_bytes, cudaStream_t s,
+                     const int* perm = nullptr);
+gptq_status perm_run(const float* hdiag, int n, int* perm, cudaStream_t s);
+gptq_status diag_run(const float* hp, int n, float* hdiag, cudaStream_t s);
+size_t sweep_act_ws_bytes(int rows, int n);
+gptq_status static_rungs_run(const float* W, int rows, int n, const float* tab, const float* lost,
+                             uint8_t* rungs, float* scales, cudaStream_t s);
+gptq_status sweep_act_run(const float* W, int rows, int n, const float* Up, const int* perm,
+                          const float* tab, const uint8_t* srungs, uint8_t* nib, void* ws,
+                          size_t ws_bytes, cudaStream_t s);
 gptq_status build_only(const float* hp, int n, double lambda, float* A, float* D, void* ws,
                        size_t ws_bytes, cudaStream_t s);
 gptq_status ladder_run(const float* W, int rows, int n, float* tab, float* lost, cudaStream_t s);
@@ -170,6 +179,92 @@ gptq_status gptq_gram_add(float* H_packed, int n, const float* X, int T, void* w
   if (ws_bytes < gram_ws_bytes(n)) return GPTQ_ERR_NOMEM;
   if (T == 0) return GPTQ_OK;
   return gram_run(H_packed, n, X, T, ws, ws_bytes, as_stream(stream));
+}
+
+gptq_status gptq_act_order_perm(const float* hdiag, int n, int* perm, void* stream) {
+  if (bad_n(n)) return GPTQ_ERR_SHAPE;
+  if (!ptr_ok(hdiag) || !ptr_ok(perm)) return GPTQ_ERR_ARG;
+  return perm_run(hdiag, n, perm, as_stream(stream));
+}
+
+gptq_status gptq_fold_permuted(const float* H_packed, int n, double lambda, const int* perm,
+                               float* U, float* D, float* hdiag, double* lambda_used, void* ws,
+                               size_t ws_bytes, void* stream) {
+  if (bad_n(n)) return GPTQ_ERR_SHAPE;
+  if (!ptr_ok(H_packed) || !ptr_ok(perm) || !ptr_ok(U) || !opt_ok(D) || !opt_ok(hdiag) ||
+      ws == nullptr)
+    return GPTQ_ERR_ARG;
+  if (!isfinite(lambda)) return GPTQ_ERR_ARG;
+  if (ws_bytes < fold_ws_bytes(n)) return GPTQ_ERR_NOMEM;
+  return fold_run(H_packed, n, lambda, U, D, hdiag, lambda_used, ws, ws_bytes, as_stream(stream),
+                  perm);
+}
+
+gptq_status gptq_static_rungs(const float* W, int rows, int n, const float* tab, const float* lost,
+                              uint8_t* rungs, float* scales, void* stream) {
+  if (bad_n(n) || bad_rows(rows) || n % GPTQ_GROUP != 0) return GPTQ_ERR_SHAPE;
+  if (!ptr_ok(W) || !ptr_ok(tab) || !ptr_ok(lost) || rungs == nullptr || !ptr_ok(scales))
+    return GPTQ_ERR_ARG;
+  return static_rungs_run(W, rows, n, tab, lost, rungs, scales, as_stream(stream));
+}
+
+size_t gptq_sweep_act_order_workspace_bytes(int rows, int n) {
+  if (bad_n(n) || bad_rows(rows)) return 0;
+  return sweep_act_ws_bytes(rows, n);
+}
+
+gptq_status gptq_q4tp_sweep_act_order(const float* W, int rows, int n, const float* U,
+                                      const int* perm, const float* tab, const uint8_t* rungs,
+                                      uint8_t* nibbles, void* ws, size_t ws_bytes, void* stream) {
+  if (bad_n(n) || bad_rows(rows) || n % GPTQ_GROUP != 0) return GPTQ_ERR_SHAPE;
+  if (!ptr_ok(W) || !ptr_ok(U) || !ptr_ok(perm) || !ptr_ok(tab) || rungs == nullptr ||
+      !ptr_ok(nibbles) || ws == nullptr)
+    return GPTQ_ERR_ARG;
+  if (ws_bytes < sweep_act_ws_bytes(rows, n)) return GPTQ_ERR_NOMEM;
+  return sweep_act_run(W, rows, n, U, perm, tab, rungs, nibbles, ws, ws_bytes, as_stream(stream));
+}
+
+size_t gptq_group_act_order_workspace_bytes(int rows, int n) {
+  if (bad_n(n) || bad_rows(rows)) return 0;
+  const size_t f = fold_ws_bytes(n), sw = sweep_act_ws_bytes(rows, n);
+  const size_t own = round_up((size_t)n * n * 4, 256) + 4 * round_up((size_t)n * 4, 256) +
+                     round_up((size_t)rows * n * 4, 256) + round_up((size_t)rows * 32 * 4, 256) +
+                     round_up((size_t)rows * 2 * 4, 256) + 1024;
+  return own + (f > sw ? f : sw);
+}
+
+gptq_status gptq_quantize_group_act_order(const float* H_packed, int n, double lambda,
+                                          const float* W, int rows, uint8_t* nibbles,
+                                          uint8_t* rungs, float* scales, int* perm_out, float* U,
+                                          double* lambda_used, void* ws, size_t ws_bytes,
+                                          void* stream) {
+  if (bad_n(n) || bad_rows(rows) || n % GPTQ_GROUP != 0) return GPTQ_ERR_SHAPE;
+  if (!ptr_ok(H_packed) || !ptr_ok(W) || !ptr_ok(nibbles) || rungs == nullptr ||
+      !ptr_ok(scales) || !opt_ok(perm_out) || !opt_ok(U) || ws == nullptr)
+    return GPTQ_ERR_ARG;
+  if (!isfinite(lambda)) return GPTQ_ERR_ARG;
+  if (ws_bytes < gptq_group_act_order_workspace_bytes(rows, n)) return GPTQ_ERR_NOMEM;
+  cudaStream_t s = as_stream(stream);
+  Carve c(ws, ws_bytes);
+  float* u = U ? U : c.take<float>((size_t)n * n);
+  int* perm = perm_out ? perm_out : c.take<int>((size_t)n);
+  float* hraw = c.take<float>((size_t)n);
+  float* hperm = c.take<float>((size_t)n);
+  float* d = c.take<float>((size_t)n);
+  float* wz = c.take<float>((size_t)rows * n);
+  float* tb = c.take<float>((size_t)rows * 32);
+  float* ls = c.take<float>((size_t)rows * 2);
+  if (!c.ok) return GPTQ_ERR_NOMEM;
+  const size_t off = round_up(c.off, 256);
+  void* rest = static_cast<char*>(ws) + off;
+  const size_t rest_bytes = ws_bytes - off;
+  GQ_TRY(diag_run(H_packed, n, hraw, s));
+  GQ_TRY(perm_run(hraw, n, perm, s));
+  GQ_TRY(fold_run(H_packed, n, lambda, u, d, hperm, lambda_used, rest, rest_bytes, s, perm));
+  GQ_TRY(copy_dead_zeroed(W, rows, n, hraw, wz, s));
+  GQ_TRY(ladder_run(wz, rows, n, tb, ls, s));
+  GQ_TRY(static_rungs_run(wz, rows, n, tb, ls, rungs, scales, s));
+  return sweep_act_run(wz, rows, n, u, perm, tb, rungs, nibbles, rest, rest_bytes, s);
 }
 
 }  // extern "C"

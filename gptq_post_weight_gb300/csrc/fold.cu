@@ -36,13 +36,16 @@ __device__ __forceinline__ bool flagged(const unsigned* flag) {
 // Raw diagonal, dead mask and base = max(mean(diag with dead := 1), 1e-12)
 // in f64 with a fixed summation order (one CTA).  [fold page] diag_get and
 // fold_inner's host lines; [host page] gptq_fold_operator_par.
+// With a permutation (act order), position i holds channel perm[i].
 __global__ void __launch_bounds__(1024) k_diag(const float* __restrict__ hp, int n,
+                                               const int* __restrict__ perm,
                                                float* __restrict__ hdiag,
                                                double* __restrict__ base_out) {
   __shared__ double part[1024];
   double acc = 0.0;
   for (int i = threadIdx.x; i < n; i += 1024) {
-    float h = hp[poff(i, n)];
+    const int ch = perm ? perm[i] : i;
+    float h = hp[poff(ch, n)];
     hdiag[i] = h;
     acc += (h > 0.f) ? (double)h : 1.0;
   }
@@ -74,8 +77,11 @@ __global__ void k_dvec(int n, const float* __restrict__ hdiag, const double* __r
 }
 
 // One row i of A: lower part = equilibrated reversed damped H, upper part
-// zero (initial Y), padding rows identity.  [fold page] build_a.
+// zero (initial Y), padding rows identity.  [fold page] build_a.  With a
+// permutation (act order, host page's permute_sym) the matrix is
+// H[perm][perm]: its entries are gathered from the packed triangle.
 __global__ void __launch_bounds__(256) k_build(const float* __restrict__ hp, int n, int N,
+                                               const int* __restrict__ perm,
                                                const float* __restrict__ hdiag,
                                                const double* __restrict__ base, double lam,
                                                const float* __restrict__ dabs,
@@ -102,7 +108,14 @@ __global__ void __launch_bounds__(256) k_build(const float* __restrict__ hp, int
       if (dead_i || dead_j) {
         v = (ii == jj) ? 1.f : 0.f;
       } else {
-        float h = hp[prow + (jj - ii)];
+        float h;
+        if (perm) {
+          const int pa = perm[ii], pb = perm[jj];
+          const int a = pa < pb ? pa : pb, b = pa < pb ? pb : pa;
+          h = hp[poff(a, n) + (b - a)];
+        } else {
+          h = hp[prow + (jj - ii)];
+        }
         if (ii == jj) h = __fadd_rn(h, dampf);
         v = __fdiv_rn(h, __fmul_rn(di, dabs[jj]));
       }
@@ -238,7 +251,58 @@ __global__ void __launch_bounds__(APPLY_ROWS * 4) k_apply(const float* __restric
   }
 }
 
+// Act-order channel order ([host page] act_order_perm): descending H_ii in
+// Rust's total order on f32 (NaN and -0.0 ordered), ties by ascending index.
+// Each thread ranks one channel against all others (keys staged in shared
+// memory) and writes perm[rank] = channel.
+__device__ __forceinline__ int total_key(float x) {
+  const int b = __float_as_int(x);
+  return b < 0 ? (b ^ 0x7FFFFFFF) : b;
+}
+
+__global__ void __launch_bounds__(256) k_perm_rank(const float* __restrict__ hdiag, int n,
+                                                   int* __restrict__ perm) {
+  __shared__ int keys[2048];
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  const int ki = i < n ? total_key(hdiag[i]) : 0;
+  int rank = 0;
+  for (int base = 0; base < n; base += 2048) {
+    const int m = (n - base) < 2048 ? (n - base) : 2048;
+    __syncthreads();
+    for (int e = threadIdx.x; e < m; e += blockDim.x) keys[e] = total_key(hdiag[base + e]);
+    __syncthreads();
+    if (i < n) {
+      for (int e = 0; e < m; ++e) {
+        const int kj = keys[e], j = base + e;
+        rank += (kj > ki) || (kj == ki && j < i);
+      }
+    }
+  }
+  if (i < n) perm[rank] = i;
+}
+
 }  // namespace
+
+namespace {
+__global__ void k_hdiag(const float* __restrict__ hp, int n, float* __restrict__ hdiag) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) hdiag[i] = hp[poff(i, n)];
+}
+}  // namespace
+
+gptq_status diag_run(const float* hp, int n, float* hdiag, cudaStream_t s) {
+  GQ_PROF(K_DIAG, s);
+  k_hdiag<<<(n + 255) / 256, 256, 0, s>>>(hp, n, hdiag);
+  GQ_LAUNCHED();
+  return GPTQ_OK;
+}
+
+gptq_status perm_run(const float* hdiag, int n, int* perm, cudaStream_t s) {
+  GQ_PROF(K_COPY, s);
+  k_perm_rank<<<(n + 255) / 256, 256, 0, s>>>(hdiag, n, perm);
+  GQ_LAUNCHED();
+  return GPTQ_OK;
+}
 
 struct FoldWs {
   int n, N;
@@ -293,7 +357,7 @@ static gptq_status init_attrs() {
 // One factorisation attempt at damping lam: build, interleaved Cholesky +
 // inverse, U.  The pivot flag is left on the device.
 static gptq_status fold_attempt(const float* hp, const FoldWs& w, const OperandMaps& maps,
-                                double lam, float* U, float* D, cudaStream_t s) {
+                                double lam, float* U, float* D, cudaStream_t s, const int* perm) {
   const int n = w.n, N = w.N;
   const long long ld = N;
   GQ_CUDA(cudaMemsetAsync(w.flag, 0, sizeof(unsigned), s));
@@ -301,7 +365,7 @@ static gptq_status fold_attempt(const float* hp, const FoldWs& w, const OperandM
     GQ_PROF(K_BUILD, s);
     k_dvec<<<(n + 255) / 256, 256, 0, s>>>(n, w.hdiag, w.base, lam, D, w.dabs);
     GQ_LAUNCHED();
-    k_build<<<N, 256, 0, s>>>(hp, n, N, w.hdiag, w.base, lam, w.dabs, w.A, ld, 1);
+    k_build<<<N, 256, 0, s>>>(hp, n, N, perm, w.hdiag, w.base, lam, w.dabs, w.A, ld, 1);
     GQ_LAUNCHED();
   }
   // Steps go in pairs (k, k + NB) while two blocks remain:
@@ -362,14 +426,15 @@ static gptq_status fold_attempt(const float* hp, const FoldWs& w, const OperandM
 }
 
 gptq_status fold_run(const float* hp, int n, double lambda, float* U, float* D, float* hdiag,
-                     double* lambda_used, void* ws, size_t ws_bytes, cudaStream_t s) {
+                     double* lambda_used, void* ws, size_t ws_bytes, cudaStream_t s,
+                     const int* perm) {
   GQ_TRY(init_attrs());
   Carve c(ws, ws_bytes);
   FoldWs w;
   if (!carve_fold(c, n, w)) return GPTQ_ERR_NOMEM;
   {
     GQ_PROF(K_DIAG, s);
-    k_diag<<<1, 1024, 0, s>>>(hp, n, w.hdiag, w.base);
+    k_diag<<<1, 1024, 0, s>>>(hp, n, perm, w.hdiag, w.base);
     GQ_LAUNCHED();
   }
   if (hdiag) GQ_CUDA(cudaMemcpyAsync(hdiag, w.hdiag, (size_t)n * 4, cudaMemcpyDeviceToDevice, s));
@@ -382,7 +447,7 @@ gptq_status fold_run(const float* hp, int n, double lambda, float* U, float* D, 
   GQ_TRY(make_c_map(&maps.c, w.A, w.N, w.N, w.N));
   double lam = lambda > 0.0 ? lambda : 0.0;
   for (;;) {
-    GQ_TRY(fold_attempt(hp, w, maps, lam, U, D, s));
+    GQ_TRY(fold_attempt(hp, w, maps, lam, U, D, s, perm));
     unsigned hflag = 0;
     GQ_CUDA(cudaMemcpyAsync(&hflag, w.flag, sizeof(unsigned), cudaMemcpyDeviceToHost, s));
     GQ_CUDA(cudaStreamSynchronize(s));
@@ -402,7 +467,7 @@ gptq_status build_only(const float* hp, int n, double lambda, float* A, float* D
   if (!carve_fold(c, n, w)) return GPTQ_ERR_NOMEM;
   {
     GQ_PROF(K_DIAG, s);
-    k_diag<<<1, 1024, 0, s>>>(hp, n, w.hdiag, w.base);
+    k_diag<<<1, 1024, 0, s>>>(hp, n, nullptr, w.hdiag, w.base);
     GQ_LAUNCHED();
   }
   // Rows of the caller's n x n matrix, lower triangle only.
@@ -410,7 +475,7 @@ gptq_status build_only(const float* hp, int n, double lambda, float* A, float* D
   const double lam = lambda > 0 ? lambda : 0.0;
   k_dvec<<<(n + 255) / 256, 256, 0, s>>>(n, w.hdiag, w.base, lam, D, w.dabs);
   GQ_LAUNCHED();
-  k_build<<<n, 256, 0, s>>>(hp, n, n, w.hdiag, w.base, lam, w.dabs, A, n, 0);
+  k_build<<<n, 256, 0, s>>>(hp, n, n, nullptr, w.hdiag, w.base, lam, w.dabs, A, n, 0);
   GQ_LAUNCHED();
   return GPTQ_OK;
 }

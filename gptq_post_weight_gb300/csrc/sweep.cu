@@ -107,6 +107,29 @@ __device__ __forceinline__ void q4tp_round(float (&w)[GROUP], float s, const flo
   }
 }
 
+// Act-order rounding of 32 consecutive (permuted) columns with per-column
+// scales ([host page] gptq_quantize_q4tp_act_order): q_j = clamp(rne(w_j /
+// s_j), -8, 7) (0 if s_j <= 0), e_j = (w_j - q_j s_j) / U_jj (0 if
+// U_jj <= 0), w_t -= e_j U_jt for t > j; one rounding per operation.
+__device__ __forceinline__ void q4tp_round_cols(float (&w)[GROUP], const float (&s)[GROUP],
+                                                const float* U, int ldu, int (&q8)[GROUP],
+                                                float (&e)[GROUP]) {
+#pragma unroll
+  for (int j = 0; j < GROUP; ++j) {
+    float q = 0.f;
+    if (s[j] > 0.f) q = fminf(fmaxf(rintf(__fdiv_rn(w[j], s[j])), -8.f), 7.f);
+    q8[j] = (int)q;
+    const float dj = U[j * ldu + j];
+    float ej = 0.f;
+    if (dj > 0.f) ej = __fdiv_rn(__fsub_rn(w[j], __fmul_rn(q, s[j])), dj);
+    e[j] = ej;
+    if (ej != 0.f) {
+#pragma unroll
+      for (int t = j + 1; t < GROUP; ++t) w[t] = __fsub_rn(w[t], __fmul_rn(ej, U[j * ldu + t]));
+    }
+  }
+}
+
 // Per-row ladder ([host page] gptq_quantize_q4tp_dev's tab / lost; the
 // converter itself is not on the pages -- reading in the header).
 __global__ void __launch_bounds__(128) k_ladder(const float* __restrict__ W, int n,
@@ -217,11 +240,17 @@ constexpr int EW = 2 * SB;  // residual / U-stripe buffers hold a pair of blocks
 // GEMM's operand); then all four warps push the group's residuals into the
 // rest of the block (w_c -= sum_j e_j U_jc), each warp a quarter of the
 // columns.
+// ACT (act order): W and U are in permuted channel order, the rungs are
+// given (static, per original group) and each column takes the scale of its
+// original group; codes go to `codes` (int8, permuted order) instead of the
+// nibble plane.
+template <bool ACT>
 __global__ void __launch_bounds__(SWEEP_THREADS) k_sweep_block(
     const float* __restrict__ W, int rows, int n, int b0, int B, const float* __restrict__ U,
     const float* __restrict__ hw, const float* __restrict__ tab, const float* __restrict__ lost,
     uint8_t* __restrict__ nib, uint8_t* __restrict__ rungs, float* __restrict__ scales,
-    float* __restrict__ E_hi, float* __restrict__ E_lo, int ecol0) {
+    float* __restrict__ E_hi, float* __restrict__ E_lo, int ecol0, const int* __restrict__ perm,
+    int8_t* __restrict__ codes) {
   extern __shared__ __align__(16) float sm[];
   float* Us = sm;                 // [SB][SB]
   float* hws = Us + SB * SB;      // [SB]
@@ -263,7 +292,7 @@ __global__ void __launch_bounds__(SWEEP_THREADS) k_sweep_block(
 #pragma unroll
       for (int kq = 0; kq < SB / 32; ++kq) Ws[(warp + 4 * i) * LW + kq * 32 + lane] = v[i][kq];
   }
-  for (int e = tid; e < B; e += SWEEP_THREADS) hws[e] = hw[b0 + e];
+  for (int e = tid; e < B; e += SWEEP_THREADS) hws[e] = ACT ? 0.f : hw[b0 + e];
   __syncthreads();
   const int r = r0 + lane;
   const bool live = r < rows;
@@ -271,19 +300,36 @@ __global__ void __launch_bounds__(SWEEP_THREADS) k_sweep_block(
   float* wrow = Ws + lane * LW;
   for (int g = 0; g < B / GROUP; ++g) {
     if (warp == 0 && live) {
-      const float lo = lost[2 * r], st = lost[2 * r + 1];
       const float* tabrow = tab + (long long)r * 32;
       float w[GROUP], e[GROUP];
 #pragma unroll
       for (int t = 0; t < GROUP; ++t) w[t] = wrow[g * GROUP + t];
-      const int c = q4tp_pick(w, hws + g * GROUP, tabrow, lo, st);
-      const float s = tabrow[c];
-      uint32_t words[4];
-      q4tp_round(w, s, Us + g * GROUP * SB + g * GROUP, SB, words, e);
-      const long long tix = (long long)r * gpr + b0 / GROUP + g;
-      reinterpret_cast<uint4*>(nib)[tix] = make_uint4(words[0], words[1], words[2], words[3]);
-      rungs[tix] = (uint8_t)c;
-      scales[tix] = s;
+      if (ACT) {
+        float sc[GROUP];
+        int q8[GROUP];
+#pragma unroll
+        for (int t = 0; t < GROUP; ++t)
+          sc[t] = tabrow[rungs[(long long)r * gpr + perm[b0 + g * GROUP + t] / GROUP]];
+        q4tp_round_cols(w, sc, Us + g * GROUP * SB + g * GROUP, SB, q8, e);
+        uint32_t pk[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          pk[i] = (uint32_t)(q8[4 * i] & 255) | ((uint32_t)(q8[4 * i + 1] & 255) << 8) |
+                  ((uint32_t)(q8[4 * i + 2] & 255) << 16) | ((uint32_t)(q8[4 * i + 3] & 255) << 24);
+        uint4* dst = reinterpret_cast<uint4*>(codes + (long long)r * n + b0 + g * GROUP);
+        dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+      } else {
+        const float lo = lost[2 * r], st = lost[2 * r + 1];
+        const int c = q4tp_pick(w, hws + g * GROUP, tabrow, lo, st);
+        const float s = tabrow[c];
+        uint32_t words[4];
+        q4tp_round(w, s, Us + g * GROUP * SB + g * GROUP, SB, words, e);
+        const long long tix = (long long)r * gpr + b0 / GROUP + g;
+        reinterpret_cast<uint4*>(nib)[tix] = make_uint4(words[0], words[1], words[2], words[3]);
+        rungs[tix] = (uint8_t)c;
+        scales[tix] = s;
+      }
       float4* eh = reinterpret_cast<float4*>(E_hi + (long long)r * EW + ecol0 + g * GROUP);
       float4* el = reinterpret_cast<float4*>(E_lo + (long long)r * EW + ecol0 + g * GROUP);
 #pragma unroll
@@ -368,7 +414,9 @@ size_t sweep_ws_bytes(int rows, int n) {
 static gptq_status sweep_attrs() {
   static bool done = false;
   if (done) return GPTQ_OK;
-  GQ_CUDA(cudaFuncSetAttribute(k_sweep_block, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  GQ_CUDA(cudaFuncSetAttribute(k_sweep_block<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (SB * SB + SB + SWEEP_ROWS * LW + SWEEP_ROWS * (GROUP + 1)) * 4));
+  GQ_CUDA(cudaFuncSetAttribute(k_sweep_block<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (SB * SB + SB + SWEEP_ROWS * LW + SWEEP_ROWS * (GROUP + 1)) * 4));
   done = true;
   return GPTQ_OK;
@@ -425,9 +473,10 @@ gptq_status noalloc_scratch(void** out) {
   return GPTQ_OK;
 }
 
-gptq_status sweep_run(float* W, int rows, int n, const float* U, const float* hw, const float* tab,
-                      const float* lost, uint8_t* nib, uint8_t* rungs, float* scales, void* ws,
-                      size_t ws_bytes, cudaStream_t s) {
+static gptq_status sweep_core(float* W, int rows, int n, const float* U, const float* hw,
+                              const float* tab, const float* lost, uint8_t* nib, uint8_t* rungs,
+                              float* scales, void* ws, size_t ws_bytes, cudaStream_t s,
+                              const int* perm, int8_t* codes) {
   GQ_TRY(sweep_attrs());
   Carve c(ws, ws_bytes);
   float* E_hi = c.take<float>((size_t)rows * EW);
@@ -448,8 +497,14 @@ gptq_status sweep_run(float* W, int rows, int n, const float* U, const float* hw
   const int grid_rows = (rows + SWEEP_ROWS - 1) / SWEEP_ROWS;
   auto block = [&](int b0, int B, int ecol0) -> gptq_status {
     GQ_PROF(K_SWEEP_BLOCK, s);
-    k_sweep_block<<<grid_rows, SWEEP_THREADS, smem, s>>>(W, rows, n, b0, B, U, hw, tab, lost, nib,
-                                                         rungs, scales, E_hi, E_lo, ecol0);
+    if (perm)
+      k_sweep_block<true><<<grid_rows, SWEEP_THREADS, smem, s>>>(W, rows, n, b0, B, U, hw, tab, lost,
+                                                                 nib, rungs, scales, E_hi, E_lo, ecol0,
+                                                                 perm, codes);
+    else
+      k_sweep_block<false><<<grid_rows, SWEEP_THREADS, smem, s>>>(W, rows, n, b0, B, U, hw, tab, lost,
+                                                                  nib, rungs, scales, E_hi, E_lo,
+                                                                  ecol0, nullptr, nullptr);
     GQ_LAUNCHED();
     return GPTQ_OK;
   };
@@ -490,6 +545,121 @@ gptq_status sweep_run(float* W, int rows, int n, const float* U, const float* hw
   GQ_CUDA(cudaMemcpyAsync(&hs, status, sizeof(unsigned), cudaMemcpyDeviceToHost, s));
   GQ_CUDA(cudaStreamSynchronize(s));
   return hs ? GPTQ_ERR_TIMEOUT : GPTQ_OK;
+}
+
+gptq_status sweep_run(float* W, int rows, int n, const float* U, const float* hw, const float* tab,
+                      const float* lost, uint8_t* nib, uint8_t* rungs, float* scales, void* ws,
+                      size_t ws_bytes, cudaStream_t s) {
+  return sweep_core(W, rows, n, U, hw, tab, lost, nib, rungs, scales, ws, ws_bytes, s, nullptr,
+                    nullptr);
+}
+
+namespace {
+
+// Static rung of every (row, group): the rung rule with unit weights on the
+// (dead-zeroed) original weights -- the reading of the converter's own
+// choice that act order keeps fixed.
+__global__ void k_static_rungs(const float* __restrict__ W, int rows, int n,
+                               const float* __restrict__ tab, const float* __restrict__ lost,
+                               uint8_t* __restrict__ rungs, float* __restrict__ scales) {
+  __shared__ float ones[GROUP];
+  if (threadIdx.x < GROUP) ones[threadIdx.x] = 1.f;
+  __syncthreads();
+  const int gpr = n / GROUP;
+  const long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+  if (idx >= (long long)rows * gpr) return;
+  const int r = (int)(idx / gpr), g = (int)(idx % gpr);
+  float w[GROUP];
+  const float4* src = reinterpret_cast<const float4*>(W + (long long)r * n + g * GROUP);
+#pragma unroll
+  for (int q = 0; q < GROUP / 4; ++q) {
+    const float4 v = src[q];
+    w[4 * q] = v.x; w[4 * q + 1] = v.y; w[4 * q + 2] = v.z; w[4 * q + 3] = v.w;
+  }
+  const float* tabrow = tab + (long long)r * 32;
+  const int c = q4tp_pick(w, ones, tabrow, lost[2 * r], lost[2 * r + 1]);
+  rungs[idx] = (uint8_t)c;
+  scales[idx] = tabrow[c];
+}
+
+// Wp[r][a] = W[r][perm[a]].
+__global__ void k_gather_cols(const float* __restrict__ W, int rows, int n, const int* __restrict__ perm,
+                              float* __restrict__ Wp) {
+  const long long total = (long long)rows * n;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+       i += (long long)gridDim.x * blockDim.x) {
+    const long long r = i / n;
+    const int a = (int)(i % n);
+    Wp[i] = W[r * n + perm[a]];
+  }
+}
+
+__global__ void k_invperm(const int* __restrict__ perm, int n, int* __restrict__ inv) {
+  const int a = blockIdx.x * blockDim.x + threadIdx.x;
+  if (a < n) inv[perm[a]] = a;
+}
+
+// Nibble tile (r, g) from the permuted codes: column c of the group is
+// channel c, found at permuted position inv[c].
+__global__ void k_pack_nibbles(const int8_t* __restrict__ codes, int rows, int n,
+                               const int* __restrict__ inv, uint8_t* __restrict__ nib) {
+  const int gpr = n / GROUP;
+  const long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+  if (idx >= (long long)rows * gpr) return;
+  const long long r = idx / gpr;
+  const int g = (int)(idx % gpr);
+  uint32_t words[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+  for (int j = 0; j < GROUP; ++j) {
+    const int q = codes[r * n + inv[g * GROUP + j]];
+    words[j / 8] |= ((uint32_t)(q + 8) & 15u) << (4 * (j % 8));
+  }
+  reinterpret_cast<uint4*>(nib)[idx] = make_uint4(words[0], words[1], words[2], words[3]);
+}
+
+}  // namespace
+
+size_t sweep_act_ws_bytes(int rows, int n) {
+  return sweep_ws_bytes(rows, n) + round_up((size_t)rows * n * 4, 256) +
+         round_up((size_t)rows * n, 256) + round_up((size_t)n * 4, 256) + 1024;
+}
+
+gptq_status static_rungs_run(const float* W, int rows, int n, const float* tab, const float* lost,
+                             uint8_t* rungs, float* scales, cudaStream_t s) {
+  const long long tot = (long long)rows * (n / GROUP);
+  GQ_PROF(K_LADDER, s);
+  k_static_rungs<<<(unsigned)((tot + 127) / 128), 128, 0, s>>>(W, rows, n, tab, lost, rungs, scales);
+  GQ_LAUNCHED();
+  return GPTQ_OK;
+}
+
+// The act-order sweep ([host page] gptq_quantize_q4tp_act_order): W (original
+// order, dead columns zeroed) is gathered into permuted order, swept against
+// the permuted operator with the static rungs, and the codes are packed back
+// into the original nibble plane.
+gptq_status sweep_act_run(const float* W, int rows, int n, const float* Up, const int* perm,
+                          const float* tab, const uint8_t* srungs, uint8_t* nib, void* ws,
+                          size_t ws_bytes, cudaStream_t s) {
+  Carve c(ws, ws_bytes);
+  float* Wp = c.take<float>((size_t)rows * n);
+  int8_t* codes = c.take<int8_t>((size_t)rows * n);
+  int* inv = c.take<int>((size_t)n);
+  if (!c.ok) return GPTQ_ERR_NOMEM;
+  const size_t off = round_up(c.off, 256);
+  {
+    GQ_PROF(K_COPY, s);
+    k_gather_cols<<<152 * 8, 256, 0, s>>>(W, rows, n, perm, Wp);
+    GQ_LAUNCHED();
+    k_invperm<<<(n + 255) / 256, 256, 0, s>>>(perm, n, inv);
+    GQ_LAUNCHED();
+  }
+  GQ_TRY(sweep_core(Wp, rows, n, Up, nullptr, tab, nullptr, nullptr, const_cast<uint8_t*>(srungs),
+                    nullptr, static_cast<char*>(ws) + off, ws_bytes - off, s, perm, codes));
+  const long long tot = (long long)rows * (n / GROUP);
+  GQ_PROF(K_COPY, s);
+  k_pack_nibbles<<<(unsigned)((tot + 127) / 128), 128, 0, s>>>(codes, rows, n, inv, nib);
+  GQ_LAUNCHED();
+  return GPTQ_OK;
 }
 
 }  // namespace gq

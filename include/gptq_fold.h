@@ -199,6 +199,45 @@ gptq_status gptq_build_equilibrated(const float* H_packed, int n, double lambda,
                                     float* D, void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * Act order ([host page] act_order_perm, permute_sym,
+ * gptq_quantize_q4tp_act_order): channels are eliminated in descending H_ii
+ * order (Rust total order on f32, ties by index), against the fold operator
+ * of H[perm][perm]; every tile's rung is fixed up front ("static groups")
+ * and only the codes move.  The static rung is read here as the q4tp rung
+ * rule with unit weights on the dead-zeroed original weights (the pages
+ * call the converter for it, which they do not show).
+ *
+ * gptq_act_order_perm   perm (int32 n, out): position a holds channel
+ *                       perm[a]; hdiag = raw H_ii (n).
+ * gptq_fold_permuted    gptq_fold of H[perm][perm] (entries gathered from
+ *                       the packed H): U, D, hdiag in permuted order.
+ * gptq_static_rungs     rungs (u8 rows*n/32) and scales (f32) of every
+ *                       (row, group) from the dead-zeroed W and its ladder.
+ * gptq_q4tp_sweep_act_order  the sweep: W (rows*n, original order, dead
+ *                       columns zeroed; not modified), U of the permuted H,
+ *                       perm, tab, static rungs -> nibble plane (original
+ *                       layout, as gptq_q4tp_sweep writes it).
+ * gptq_quantize_group_act_order  all of the above for one group; perm_out
+ *                       and U may be NULL.
+ */
+gptq_status gptq_act_order_perm(const float* hdiag, int n, int* perm, void* stream);
+gptq_status gptq_fold_permuted(const float* H_packed, int n, double lambda, const int* perm,
+                               float* U, float* D, float* hdiag, double* lambda_used, void* ws,
+                               size_t ws_bytes, void* stream);
+gptq_status gptq_static_rungs(const float* W, int rows, int n, const float* tab, const float* lost,
+                              uint8_t* rungs, float* scales, void* stream);
+size_t gptq_sweep_act_order_workspace_bytes(int rows, int n);
+gptq_status gptq_q4tp_sweep_act_order(const float* W, int rows, int n, const float* U,
+                                      const int* perm, const float* tab, const uint8_t* rungs,
+                                      uint8_t* nibbles, void* ws, size_t ws_bytes, void* stream);
+size_t gptq_group_act_order_workspace_bytes(int rows, int n);
+gptq_status gptq_quantize_group_act_order(const float* H_packed, int n, double lambda,
+                                          const float* W, int rows, uint8_t* nibbles,
+                                          uint8_t* rungs, float* scales, int* perm_out, float* U,
+                                          double* lambda_used, void* ws, size_t ws_bytes,
+                                          void* stream);
+
+/*
  * gptq_gram_add -- calibration Hessian accumulation H += X^T X for one window
  * of tokens ([host page] calibration pass: gram_alloc / gram_add_dev, one
  * accumulator per linear input; [fold page] poff: the packed layout).  The
