@@ -56,6 +56,9 @@ struct ProfScope {
 
 inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Streaming multiprocessors of the current device (queried once).
+int num_sms();
+
 // Bump allocator over the caller's workspace (256-byte aligned pieces).
 struct Carve {
   char* base;
@@ -139,12 +142,13 @@ gptq_status make_operand_map(CUtensorMap* m, const float* base, long long rows, 
 
 // Diagonal-block step fused into an update (fold only): the block at (k, k)
 // of the N x N matrix A (leading dimension lda) must be tile 0 of job 0; its
-// Cholesky inverse goes to Linv and a bad pivot to bit 0 of the status word.
+// Cholesky inverse goes, transposed, to LinvT and a bad pivot to bit 0 of
+// the status word.
 struct FusedPotrf {
   const float* A;
   long long lda;
   int k;
-  float* Linv;
+  float* LinvT;
   int on;
 };
 
@@ -163,6 +167,17 @@ __device__ __forceinline__ float tf32_rna(float x) {
   asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
   return __uint_as_float(r);
 }
+// 16-byte global -> shared copy that bypasses registers (both addresses
+// 16-byte aligned); completion: cp_async_wait_all() in the issuing thread,
+// then a barrier before other threads read it.
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  const unsigned sa = (unsigned)__cvta_generic_to_shared(smem);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
+}
+
 __device__ __forceinline__ void split_tf32(float x, float& hi, float& lo) {
   hi = tf32_rna(x);
   lo = tf32_rna(x - hi);

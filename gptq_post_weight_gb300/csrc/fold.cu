@@ -126,20 +126,21 @@ __global__ void __launch_bounds__(256) k_build(const float* __restrict__ hp, int
 
 // Standalone launch of the diagonal-block step (the first block of a fold).
 __global__ void __launch_bounds__(256) k_potrf(const float* __restrict__ A, long long lda, int k,
-                                               float* __restrict__ Linv, unsigned* flag) {
+                                               float* __restrict__ LinvT, unsigned* flag) {
   if (flagged(flag)) return;
   extern __shared__ float S[];
-  potrf_inverse_block(A + (long long)k * lda + k, lda, Linv, flag, S);
+  potrf_inverse_block(A + (long long)k * lda + k, lda, LinvT, flag, S);
 }
 
-constexpr int APPLY_ROWS = 64;
+constexpr int APPLY_ROWS = 32;     // rows per tile
+constexpr int APPLY_THREADS = 256;
+constexpr int LV = NB + 4;  // row stride of the row-vector tiles (float4 rows)
 // Panel buffers hold two steps side by side (columns [0, NB) and [NB, 2NB)),
 // so that a pair of steps updates the trailing matrix once with K = 2 NB.
 constexpr int PW = 2 * NB;
 
 // Both triangular solves of step k as one product with the explicit inverse:
-// z = L_kk^-1 v for every row vector v, i.e. Z = V Linv^T, four threads per
-// row (thread q computes z[32q .. 32q+32) with 32 independent sums):
+// z = L_kk^-1 v for every row vector v, i.e. Z = V Linv^T:
 //  * rows i >= s0 = k+NB: the Cholesky panel (fold page chol_panel),
 //    v = A[i][k..k+NB), z -> P[i][*];
 //  * rows c < s0: the inverse's block row (fold page inv_rows), v =
@@ -149,106 +150,152 @@ constexpr int PW = 2 * NB;
 // z is stored as its TF32 hi/lo split, the operand format of the update GEMM,
 // in columns [col0, col0 + NB) of the 2 NB-wide panel buffers; panel rows
 // below zero_end also clear their Yp entries there (see fold_attempt).
-__global__ void __launch_bounds__(APPLY_ROWS * 4) k_apply(const float* __restrict__ A, long long lda,
-                                                         int k, int s0, int N, int col0, int zero_end,
-                                                         const float* __restrict__ Linv,
-                                                         float* __restrict__ P_hi, float* __restrict__ P_lo,
-                                                         float* __restrict__ Y_hi, float* __restrict__ Y_lo,
-                                                         const unsigned* flag, float* __restrict__ U,
-                                                         const float* __restrict__ dabs, int n) {
+// Persistent: a CTA keeps L_kk^-T in shared memory and walks tiles of 32
+// rows, the next tile's vectors arriving (asynchronous copies) while the
+// current one is multiplied.  The sums stop at the diagonal of Linv (z_c
+// needs v_u for u <= c only); warp w owns the 8-column blocks w and 15 - w,
+// so every warp does the same number of multiply-adds.  Thread (l % 16,
+// l / 16): rows l % 16 and l % 16 + 16, 4 columns of each block.  Z goes
+// back through shared memory for row-contiguous stores.
+__global__ void __launch_bounds__(APPLY_THREADS, 1) k_apply(const float* __restrict__ A, long long lda,
+                                                           int k, int s0, int N, int col0, int zero_end,
+                                                           const float* __restrict__ LinvT,
+                                                           float* __restrict__ P_hi, float* __restrict__ P_lo,
+                                                           float* __restrict__ Y_hi, float* __restrict__ Y_lo,
+                                                           const unsigned* flag, float* __restrict__ U,
+                                                           const float* __restrict__ dabs, int n) {
   if (flagged(flag)) return;
   extern __shared__ __align__(16) float sm[];
-  float* Ls = sm;                  // [NB][NB] Linv
-  float* Vs = Ls + NB * NB;        // [APPLY_ROWS][NB + 4]
-  constexpr int LV = NB + 4;
+  float* Lt = sm;                         // [NB][NB]: Lt[u][c] = Linv[c][u]
+  float* Vb = Lt + NB * NB;               // 2 x [APPLY_ROWS][LV]: row vectors
+  float* Zs = Vb + 2 * APPLY_ROWS * LV;   // [APPLY_ROWS][LV]: results
   const int tid = threadIdx.x;
-  const int r0 = blockIdx.x * APPLY_ROWS;
-#pragma unroll 1
-  for (int b0 = 0; b0 < NB * NB / 4; b0 += 16 * APPLY_ROWS * 4) {
-    float4 v[16];
+  const int ntiles = N / APPLY_ROWS;
+  // Vectors of tile t into buffer b: copies for rows of A, plain stores for
+  // the unit rows of block k (rows past N do not occur: N is a multiple of
+  // the tile).
+  auto fetch = [&](int t, float* buf) {
+    const int r0 = t * APPLY_ROWS;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = reinterpret_cast<const float4*>(Linv)[b0 + tid + i * APPLY_ROWS * 4];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) reinterpret_cast<float4*>(Ls)[b0 + tid + i * APPLY_ROWS * 4] = v[i];
-  }
-  {
-    // Row vectors: 64 rows x 32 float4, 8 per thread.
-    float4 v[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int e = tid + i * APPLY_ROWS * 4, rr = e / (NB / 4), c4 = e % (NB / 4);
+    for (int i = 0; i < APPLY_ROWS * NB / 4 / APPLY_THREADS; ++i) {
+      const int e = tid + i * APPLY_THREADS, rr = e / (NB / 4), c4 = e % (NB / 4);
       const int r = r0 + rr;
-      float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (r < N) {
-        if (r >= k && r < s0) {
-          const int u = r - k;
-          x.x = (4 * c4 == u) ? 1.f : 0.f;
-          x.y = (4 * c4 + 1 == u) ? 1.f : 0.f;
-          x.z = (4 * c4 + 2 == u) ? 1.f : 0.f;
-          x.w = (4 * c4 + 3 == u) ? 1.f : 0.f;
-        } else {
-          x = *reinterpret_cast<const float4*>(A + (long long)r * lda + k + 4 * c4);
+      float* dst = buf + rr * LV + 4 * c4;
+      if (!(r >= k && r < s0)) {
+        cp_async16(dst, A + (long long)r * lda + k + 4 * c4);
+      } else {
+        const int u = r - k;
+        *reinterpret_cast<float4*>(dst) = make_float4(4 * c4 == u ? 1.f : 0.f, 4 * c4 + 1 == u ? 1.f : 0.f,
+                                                      4 * c4 + 2 == u ? 1.f : 0.f, 4 * c4 + 3 == u ? 1.f : 0.f);
+      }
+    }
+  };
+  const int t0 = blockIdx.x;
+  if (t0 >= ntiles) return;
+#pragma unroll 4
+  for (int e = tid; e < NB * NB / 4; e += APPLY_THREADS) cp_async16(Lt + 4 * e, LinvT + 4 * e);
+  fetch(t0, Vb);
+  asm volatile("cp.async.commit_group;" ::: "memory");
+  const int warp = tid / 32, lane = tid % 32;
+  const int lr = lane & 15, h = lane >> 4;
+  const int c1 = 8 * warp + 4 * h;          // block w
+  const int c2 = 8 * (15 - warp) + 4 * h;   // block 15 - w
+  const int ua = 8 * warp + 8;              // u bound of block w
+  const int ub = 8 * (16 - warp);           // u bound of block 15 - w
+  int it = 0;
+  for (int t = t0; t < ntiles; t += gridDim.x, ++it) {
+    float* Vs = Vb + (it & 1) * APPLY_ROWS * LV;
+    if (t + (int)gridDim.x < ntiles) fetch(t + gridDim.x, Vb + ((it + 1) & 1) * APPLY_ROWS * LV);
+    asm volatile("cp.async.commit_group;\ncp.async.wait_group 1;" ::: "memory");
+    __syncthreads();
+    float acc[2][8];
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+#pragma unroll
+      for (int c = 0; c < 8; ++c) acc[i][c] = 0.f;
+    const float* v0p = Vs + lr * LV;
+    const float* v1p = Vs + (lr + 16) * LV;
+#pragma unroll 1
+    for (int u4 = 0; u4 < ua / 4; ++u4) {
+      const float4 v0 = *reinterpret_cast<const float4*>(v0p + 4 * u4);
+      const float4 v1 = *reinterpret_cast<const float4*>(v1p + 4 * u4);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float4 la = *reinterpret_cast<const float4*>(Lt + (4 * u4 + j) * NB + c1);
+        const float4 lb = *reinterpret_cast<const float4*>(Lt + (4 * u4 + j) * NB + c2);
+        const float x0 = j == 0 ? v0.x : j == 1 ? v0.y : j == 2 ? v0.z : v0.w;
+        const float x1 = j == 0 ? v1.x : j == 1 ? v1.y : j == 2 ? v1.z : v1.w;
+        acc[0][0] = fmaf(x0, la.x, acc[0][0]); acc[0][1] = fmaf(x0, la.y, acc[0][1]);
+        acc[0][2] = fmaf(x0, la.z, acc[0][2]); acc[0][3] = fmaf(x0, la.w, acc[0][3]);
+        acc[0][4] = fmaf(x0, lb.x, acc[0][4]); acc[0][5] = fmaf(x0, lb.y, acc[0][5]);
+        acc[0][6] = fmaf(x0, lb.z, acc[0][6]); acc[0][7] = fmaf(x0, lb.w, acc[0][7]);
+        acc[1][0] = fmaf(x1, la.x, acc[1][0]); acc[1][1] = fmaf(x1, la.y, acc[1][1]);
+        acc[1][2] = fmaf(x1, la.z, acc[1][2]); acc[1][3] = fmaf(x1, la.w, acc[1][3]);
+        acc[1][4] = fmaf(x1, lb.x, acc[1][4]); acc[1][5] = fmaf(x1, lb.y, acc[1][5]);
+        acc[1][6] = fmaf(x1, lb.z, acc[1][6]); acc[1][7] = fmaf(x1, lb.w, acc[1][7]);
+      }
+    }
+#pragma unroll 1
+    for (int u4 = ua / 4; u4 < ub / 4; ++u4) {
+      const float4 v0 = *reinterpret_cast<const float4*>(v0p + 4 * u4);
+      const float4 v1 = *reinterpret_cast<const float4*>(v1p + 4 * u4);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float4 lb = *reinterpret_cast<const float4*>(Lt + (4 * u4 + j) * NB + c2);
+        const float x0 = j == 0 ? v0.x : j == 1 ? v0.y : j == 2 ? v0.z : v0.w;
+        const float x1 = j == 0 ? v1.x : j == 1 ? v1.y : j == 2 ? v1.z : v1.w;
+        acc[0][4] = fmaf(x0, lb.x, acc[0][4]); acc[0][5] = fmaf(x0, lb.y, acc[0][5]);
+        acc[0][6] = fmaf(x0, lb.z, acc[0][6]); acc[0][7] = fmaf(x0, lb.w, acc[0][7]);
+        acc[1][4] = fmaf(x1, lb.x, acc[1][4]); acc[1][5] = fmaf(x1, lb.y, acc[1][5]);
+        acc[1][6] = fmaf(x1, lb.z, acc[1][6]); acc[1][7] = fmaf(x1, lb.w, acc[1][7]);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      float* z = Zs + (lr + 16 * i) * LV;
+      *reinterpret_cast<float4*>(z + c1) = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+      *reinterpret_cast<float4*>(z + c2) = make_float4(acc[i][4], acc[i][5], acc[i][6], acc[i][7]);
+    }
+    __syncthreads();
+    // Panel / inverse-row stores: one row of 32 float4 per warp instruction.
+    const int r0 = t * APPLY_ROWS;
+#pragma unroll
+    for (int i = 0; i < APPLY_ROWS * NB / 4 / APPLY_THREADS; ++i) {
+      const int e = tid + i * APPLY_THREADS, rr = e / (NB / 4), c4 = e % (NB / 4);
+      const int r = r0 + rr;
+      const float4 z = *reinterpret_cast<const float4*>(Zs + rr * LV + 4 * c4);
+      const bool panel = r >= s0;
+      const long long off = (long long)r * PW + col0 + 4 * c4;
+      float4 hv, lv;
+      split_tf32(z.x, hv.x, lv.x);
+      split_tf32(z.y, hv.y, lv.y);
+      split_tf32(z.z, hv.z, lv.z);
+      split_tf32(z.w, hv.w, lv.w);
+      *reinterpret_cast<float4*>((panel ? P_hi : Y_hi) + off) = hv;
+      *reinterpret_cast<float4*>((panel ? P_lo : Y_lo) + off) = lv;
+      if (panel && r < zero_end) {
+        // Rows of the next block: their part of Yp in this half is X[block k][r] = 0.
+        *reinterpret_cast<float4*>(Y_hi + off) = make_float4(0.f, 0.f, 0.f, 0.f);
+        *reinterpret_cast<float4*>(Y_lo + off) = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+    // Entries of U: for a fixed output column c, consecutive rows r are
+    // consecutive (descending) columns of U's row n-1-(k+c).
+    if (r0 < s0 && r0 < n) {
+      const int rr = tid % APPLY_ROWS;
+      const int r = r0 + rr;
+      if (r < s0 && r < n) {
+        const int m = n - 1 - r;
+        const float dm = dabs[m];
+#pragma unroll 4
+        for (int c = tid / APPLY_ROWS; c < NB; c += APPLY_THREADS / APPLY_ROWS) {
+          const int i = k + c;
+          if (i < n) U[(long long)(n - 1 - i) * n + m] = __fdiv_rn(Zs[rr * LV + c], dm);
         }
       }
-      v[i] = x;
-    }
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int e = tid + i * APPLY_ROWS * 4, rr = e / (NB / 4), c4 = e % (NB / 4);
-      *reinterpret_cast<float4*>(Vs + rr * LV + 4 * c4) = v[i];
     }
   }
-  __syncthreads();
-  const int rr = tid % APPLY_ROWS, q = tid / APPLY_ROWS;  // q: which 32 outputs
-  const int r = r0 + rr;
-  if (r >= N) return;
-  float acc[32];
-#pragma unroll
-  for (int t = 0; t < 32; ++t) acc[t] = 0.f;
-  const float* vrow = Vs + rr * LV;
-  const float* lrow = Ls + (q * 32) * NB;
-#pragma unroll 2
-  for (int u4 = 0; u4 < NB / 4; ++u4) {
-    const float4 v = *reinterpret_cast<const float4*>(vrow + 4 * u4);
-#pragma unroll
-    for (int t = 0; t < 32; ++t) {
-      const float4 l = *reinterpret_cast<const float4*>(lrow + t * NB + 4 * u4);
-      acc[t] = fmaf(l.x, v.x, fmaf(l.y, v.y, fmaf(l.z, v.z, fmaf(l.w, v.w, acc[t]))));
-    }
-  }
-  const bool panel = r >= s0;
-  const long long off = (long long)r * PW + col0 + q * 32;
-  float4* dh = reinterpret_cast<float4*>((panel ? P_hi : Y_hi) + off);
-  float4* dl = reinterpret_cast<float4*>((panel ? P_lo : Y_lo) + off);
-  if (panel && r < zero_end) {
-    // Rows of the next block: their part of Yp in this half is X[block k][r] = 0.
-    float4* zh = reinterpret_cast<float4*>(Y_hi + off);
-    float4* zl = reinterpret_cast<float4*>(Y_lo + off);
-#pragma unroll
-    for (int t = 0; t < 8; ++t) {
-      zh[t] = make_float4(0.f, 0.f, 0.f, 0.f);
-      zl[t] = make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-  }
-#pragma unroll
-  for (int t = 0; t < 8; ++t) {
-    float4 h, l;
-    split_tf32(acc[4 * t], h.x, l.x);
-    split_tf32(acc[4 * t + 1], h.y, l.y);
-    split_tf32(acc[4 * t + 2], h.z, l.z);
-    split_tf32(acc[4 * t + 3], h.w, l.w);
-    dh[t] = h;
-    dl[t] = l;
-  }
-  if (!panel && r < n) {
-    const int m = n - 1 - r;
-    const float dm = dabs[m];
-#pragma unroll
-    for (int t = 0; t < 32; ++t) {
-      const int i = k + q * 32 + t;
-      if (i < n) U[(long long)(n - 1 - i) * n + m] = __fdiv_rn(acc[t], dm);
-    }
-  }
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
 }
 
 // Act-order channel order ([host page] act_order_perm): descending H_ii in
@@ -311,7 +358,7 @@ struct FoldWs {
   float* P_lo;
   float* Yp_hi;   // N x PW   (Y panels of the current pair of steps, TF32 hi/lo)
   float* Yp_lo;
-  float* Lkk;     // NB x NB: inverse of the current diagonal block of L
+  float* Lkk;     // NB x NB: inverse of the current diagonal block of L, transposed
   float* hdiag;   // n
   float* dabs;    // n
   double* base;   // 1
@@ -343,7 +390,7 @@ size_t fold_ws_bytes(int n) {
 }
 
 constexpr int POTRF_SMEM = POTRF_SMEM_BYTES;
-constexpr int APPLY_SMEM = (NB * NB + APPLY_ROWS * (NB + 4)) * 4;
+constexpr int APPLY_SMEM = (NB * NB + 3 * APPLY_ROWS * LV) * 4;
 
 static gptq_status init_attrs() {
   static bool done = false;
@@ -381,7 +428,9 @@ static gptq_status fold_attempt(const float* hp, const FoldWs& w, const OperandM
   // its block (tile 0 of that GEMM is exactly that block).
   auto apply = [&](int k, int col0, int zero_end) -> gptq_status {
     GQ_PROF(K_TRSM, s);
-    k_apply<<<N / APPLY_ROWS, APPLY_ROWS * 4, APPLY_SMEM, s>>>(w.A, ld, k, k + NB, N, col0, zero_end,
+    const int tiles = N / APPLY_ROWS;
+    const int sms = num_sms();
+    k_apply<<<tiles < sms ? tiles : sms, APPLY_THREADS, APPLY_SMEM, s>>>(w.A, ld, k, k + NB, N, col0, zero_end,
                                                                w.Lkk, w.P_hi, w.P_lo, w.Yp_hi,
                                                                w.Yp_lo, w.flag, U, w.dabs, n);
     GQ_LAUNCHED();

@@ -209,7 +209,10 @@ __global__ void __launch_bounds__(THREADS, 1)
               const __grid_constant__ CUtensorMap cmap, TcJob j0, TcJob j1, int K, int kseg,
               const unsigned* flag, unsigned* status, FusedPotrf fp) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // 1024-byte alignment by an offset on the shared array itself (not an
+  // integer round trip), so that accesses through `smem` stay shared-memory
+  // instructions, here and in the diagonal-block step that reuses it.
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   __shared__ __align__(8) uint64_t full[STAGES], empty[STAGES], tfull[2], tempty[2], drain;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
@@ -444,7 +447,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     // load has landed and every MMA has retired).
     if (threadIdx.x == 64) asm volatile("fence.proxy.async.global;" ::: "memory");
     __syncthreads();
-    potrf_inverse_block(fp.A + (long long)fp.k * fp.lda + fp.k, fp.lda, fp.Linv, status,
+    potrf_inverse_block(fp.A + (long long)fp.k * fp.lda + fp.k, fp.lda, fp.LinvT, status,
                         reinterpret_cast<float*>(smem));
   }
 }
@@ -462,6 +465,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
+}  // namespace
+
 int num_sms() {
   static int sms = 0;
   if (sms == 0) {
@@ -473,7 +478,6 @@ int num_sms() {
   return sms;
 }
 
-}  // namespace
 
 gptq_status make_operand_map(CUtensorMap* m, const float* base, long long rows, int K) {
   auto fn = encode_fn();

@@ -19,32 +19,35 @@ constexpr int POTRF_SMEM_BYTES = 3 * NB * LDS * 4;
 // chol_diag: !(piv > 0) (NaN included) -> flag, piv := 1.
 // Inverse ([fold page] inv_diag, blocked): the four 32 x 32 diagonal blocks
 // are inverted by four warps (lane = column), then the off-diagonal blocks
-// by block diagonals: X_ij = -X_ii sum_{j <= m < i} L_im X_mj.
-// Output: Linv (NB x NB, zeros above the diagonal).
+// by block diagonals: X_ij = -X_ii sum_{j <= m < i} L_im X_mj, as register-
+// tiled block products.
+// Output: LinvT = Linv transposed (NB x NB, LinvT[c][r] = Linv[r][c], zeros
+// below its diagonal).
 // Runs on the whole CTA (any multiple of 32 threads >= 128); S is at least
 // POTRF_SMEM_BYTES of shared memory.  The block starts at Ablk (leading
 // dimension lda); it is read with L1-bypassing loads.
 static __device__ __noinline__ void potrf_inverse_block(const float* __restrict__ Ablk, long long lda,
-                                                 float* __restrict__ Linv, unsigned* flag, float* S) {
+                                                 float* __restrict__ LinvT, unsigned* flag, float* S) {
   float* Li = S + NB * LDS;
   float* T = Li + NB * LDS;
   __shared__ float rinv[NB];
+  __shared__ __align__(16) float colbuf[2][32];
   __shared__ int bad;
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   const int NT = blockDim.x;
   if (tid == 0) bad = 0;
-  // 16 float4 loads per thread, all in flight before the first store.
+  // Up to 24 float4 loads per thread, all in flight before the first store.
   {
 #pragma unroll 1
-    for (int b0 = 0; b0 < NB * NB / 4; b0 += 8 * NT) {
-      float4 v[8];
+    for (int b0 = 0; b0 < NB * NB / 4; b0 += 24 * NT) {
+      float4 v[24];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
+      for (int i = 0; i < 24; ++i) {
         const int e = b0 + tid + NT * i, r = e / (NB / 4), c4 = e % (NB / 4);
         if (e < NB * NB / 4) v[i] = __ldcg(reinterpret_cast<const float4*>(Ablk + (long long)r * lda + 4 * c4));
       }
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
+      for (int i = 0; i < 24; ++i) {
         const int e = b0 + tid + NT * i, r = e / (NB / 4), c = 4 * (e % (NB / 4));
         if (e >= NB * NB / 4) continue;
         float* dst = S + r * LDS + c;
@@ -61,9 +64,30 @@ static __device__ __noinline__ void potrf_inverse_block(const float* __restrict_
       float a[32];
 #pragma unroll
       for (int j = 0; j < 32; ++j) a[j] = S[(p + lane) * LDS + p + j];
+      // Column c needs only column c-1's update of itself before its pivot
+      // (one shuffle); column c-1's updates of columns c+1.. are issued after
+      // that pivot's exchange, in the latency of its reciprocal square root,
+      // reading column c-1 from a shared buffer (float4 broadcasts).  Every
+      // entry still receives its updates in column order.
+      // The next pivot (lane c+1's own entry minus its own square) does not
+      // wait for the exchange that the other lanes need.
+      float lprev = 0.f, pn = a[0];
 #pragma unroll
       for (int c = 0; c < 32; ++c) {
-        float piv = __shfl_sync(0xffffffffu, a[c], c);
+        float piv = __shfl_sync(0xffffffffu, pn, c);
+        if (c > 0) {
+          const float* cb = colbuf[(c - 1) & 1];
+#pragma unroll
+          for (int j4 = (c + 1) / 4; j4 < 8; ++j4) {
+            const float4 l4 = *reinterpret_cast<const float4*>(cb + 4 * j4);
+            const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+              const int j = 4 * j4 + jj;
+              if (j >= c + 1 && lane >= j) a[j] = fmaf(-lprev, lv[jj], a[j]);
+            }
+          }
+        }
         if (!(piv > 0.f)) {
           piv = 1.f;
           if (lane == 0) bad = 1;
@@ -72,12 +96,14 @@ static __device__ __noinline__ void potrf_inverse_block(const float* __restrict_
         const float lic = (lane == c) ? piv * rs : a[c] * rs;
         if (lane >= c) a[c] = lic;
         if (lane == c) rinv[p + c] = rs;
-#pragma unroll
-        for (int j = 1; j < 32; ++j) {
-          if (j <= c) continue;
-          const float ljc = __shfl_sync(0xffffffffu, lic, j);
-          if (lane >= j) a[j] = fmaf(-lic, ljc, a[j]);
+        colbuf[c & 1][lane] = lic;
+        if (c + 1 < 32) {
+          pn = fmaf(-lic, lic, a[c + 1]);
+          const float lnc = __shfl_sync(0xffffffffu, lic, c + 1);
+          if (lane >= c + 1) a[c + 1] = (lane == c + 1) ? pn : fmaf(-lic, lnc, a[c + 1]);
         }
+        __syncwarp();
+        lprev = lic;
       }
 #pragma unroll
       for (int j = 0; j < 32; ++j)
@@ -161,33 +187,84 @@ static __device__ __noinline__ void potrf_inverse_block(const float* __restrict_
       if (t >= lane) Li[(b + t) * LDS + b + lane] = x[t];
   }
   __syncthreads();
-  // Off-diagonal blocks, one block diagonal d at a time.  Each of the
-  // (4 - d) blocks has 32 x 32 outputs; thread (blk, 4 outputs).
+  // Off-diagonal blocks, one block diagonal d at a time: for block (i, j),
+  // i = j + d, the products L_im X_mj (m = j .. i-1, each 32 x 32 x 32) go
+  // to partials P in T, then X_ij = -X_ii (P_j + P_j+1 + ...), partials
+  // summed in m order.  Every product is cut into 64 register tiles of
+  // 4 x 4; the zero upper halves of X_jj and X_ii are simply multiplied.
+  constexpr int PS = 33;  // partial row stride
+#pragma unroll
   for (int d = 1; d < 4; ++d) {
     const int nblk = 4 - d;
-    // T_ij = sum_{m = j}^{i-1} L_im X_mj  (block rows i = j + d)
-    for (int o = tid; o < nblk * 1024; o += NT) {
-      const int blk = o / 1024, rr = (o % 1024) / 32, cc = o % 32;
-      const int j = blk, i = blk + d;
-      float acc = 0.f;
-      for (int mm = j * 32; mm < i * 32; ++mm) acc = fmaf(S[(i * 32 + rr) * LDS + mm], Li[mm * LDS + j * 32 + cc], acc);
-      T[(i * 32 + rr) * LDS + j * 32 + cc] = acc;
+    for (int tix = tid; tix < nblk * d * 64; tix += NT) {
+      const int pr = tix / 64, tt = tix % 64;
+      const int j = pr / d, i = j + d, m = j + pr % d;
+      const int r0 = (tt / 8) * 4, c0 = (tt % 8) * 4;
+      const float* Lb = S + (32 * i + r0) * LDS + 32 * m;
+      const float* Xb = Li + (32 * m) * LDS + 32 * j + c0;
+      float acc[4][4];
+#pragma unroll
+      for (int ii = 0; ii < 4; ++ii)
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) acc[ii][jj] = 0.f;
+#pragma unroll 8
+      for (int k = 0; k < 32; ++k) {
+        float av[4], bv[4];
+#pragma unroll
+        for (int ii = 0; ii < 4; ++ii) av[ii] = Lb[ii * LDS + k];
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) bv[jj] = Xb[k * LDS + jj];
+#pragma unroll
+        for (int ii = 0; ii < 4; ++ii)
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) acc[ii][jj] = fmaf(av[ii], bv[jj], acc[ii][jj]);
+      }
+      float* P = T + pr * 32 * PS;
+#pragma unroll
+      for (int ii = 0; ii < 4; ++ii)
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) P[(r0 + ii) * PS + c0 + jj] = acc[ii][jj];
     }
     __syncthreads();
-    // X_ij = -X_ii T_ij
-    for (int o = tid; o < nblk * 1024; o += NT) {
-      const int blk = o / 1024, rr = (o % 1024) / 32, cc = o % 32;
-      const int j = blk, i = blk + d;
-      float acc = 0.f;
-#pragma unroll 8
-      for (int u = 0; u <= rr; ++u) acc = fmaf(Li[(i * 32 + rr) * LDS + i * 32 + u], T[(i * 32 + u) * LDS + j * 32 + cc], acc);
-      Li[(i * 32 + rr) * LDS + j * 32 + cc] = -acc;
+    for (int tix = tid; tix < nblk * 64; tix += NT) {
+      const int j = tix / 64, tt = tix % 64, i = j + d;
+      const int r0 = (tt / 8) * 4, c0 = (tt % 8) * 4;
+      const float* Xa = Li + (32 * i + r0) * LDS + 32 * i;
+      const float* P = T + j * d * 32 * PS + c0;
+      float acc[4][4];
+#pragma unroll
+      for (int ii = 0; ii < 4; ++ii)
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) acc[ii][jj] = 0.f;
+#pragma unroll 4
+      for (int k = 0; k < 32; ++k) {
+        float av[4], bv[4];
+#pragma unroll
+        for (int ii = 0; ii < 4; ++ii) av[ii] = Xa[ii * LDS + k];
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+          float t = P[k * PS + jj];
+#pragma unroll
+          for (int q = 1; q < d; ++q) t += P[q * 32 * PS + k * PS + jj];
+          bv[jj] = t;
+        }
+#pragma unroll
+        for (int ii = 0; ii < 4; ++ii)
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) acc[ii][jj] = fmaf(av[ii], bv[jj], acc[ii][jj]);
+      }
+#pragma unroll
+      for (int ii = 0; ii < 4; ++ii)
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) Li[(32 * i + r0 + ii) * LDS + 32 * j + c0 + jj] = -acc[ii][jj];
     }
     __syncthreads();
   }
+  // Column-major (the transpose, row-contiguous for its consumer); Li's
+  // odd stride keeps the column reads free of bank conflicts.
   for (int e = tid; e < NB * NB; e += NT) {
-    const int r = e / NB, c = e % NB;
-    Linv[e] = (c <= r) ? Li[r * LDS + c] : 0.f;
+    const int c = e / NB, r = e % NB;
+    LinvT[e] = (c <= r) ? Li[r * LDS + c] : 0.f;
   }
 }
 

@@ -38,18 +38,34 @@ namespace {
 // One rounding per operation (no contraction), so the f32 results are the
 // pages' bit for bit.  The up to four candidate rungs are evaluated side by
 // side (independent sums), which changes no result.
+// Nominal rung clamp(round_half_away((l2 - lo) / st), 0, 31) of x = amax/7
+// (amax > 0, st > 0), l2 = log2(x) taken in f64 and rounded to f32.  The
+// f32 log2f (CUDA documents at most 1 ulp of error) decides the integer
+// unless its quotient lands within a margin of a rounding boundary k + 1/2
+// (0 <= k <= 30); only then is the f64 value computed, so the result is the
+// f64 reading's exactly.  The margin covers 8 ulps of l2 (log2f's error plus
+// l2's own rounding, with room), one ulp for the subtraction and two for the
+// division, each scaled to the quotient.
+__device__ __forceinline__ int nominal_rung(float x, float lo, float st) {
+  const float l2a = log2f(x);
+  const float tta = __fdiv_rn(__fsub_rn(l2a, lo), st);
+  const float bnd = fminf(fmaxf(floorf(tta) + 0.5f, 0.5f), 30.5f);
+  const float margin =
+      (fabsf(l2a) * 9.6e-7f + (fabsf(l2a) + fabsf(lo)) * 1.2e-7f) / st + fabsf(tta) * 2.4e-7f + 1e-6f;
+  float tt = tta;
+  if (!(fabsf(tta - bnd) > margin)) {  // near a boundary, or NaN
+    const float l2 = (float)log2((double)x);
+    tt = __fdiv_rn(__fsub_rn(l2, lo), st);
+  }
+  return (int)fminf(fmaxf(roundf(tt), 0.f), 31.f);
+}
+
 __device__ __forceinline__ int q4tp_pick(const float (&w)[GROUP], const float* hw,
                                          const float* tabrow, float lo, float st) {
   float amax = 0.f;
 #pragma unroll
   for (int t = 0; t < GROUP; ++t) amax = fmaxf(amax, fabsf(w[t]));
-  int nominal = 0;
-  if (amax > 0.f && st > 0.f) {
-    const float x = __fdiv_rn(amax, 7.0f);
-    const float l2 = (float)log2((double)x);
-    const float tt = __fdiv_rn(__fsub_rn(l2, lo), st);
-    nominal = (int)fminf(fmaxf(roundf(tt), 0.f), 31.f);
-  }
+  const int nominal = (amax > 0.f && st > 0.f) ? nominal_rung(__fdiv_rn(amax, 7.0f), lo, st) : 0;
   int best_c = nominal;
   if (amax > 0.f) {
     const int lo_c = nominal >= 2 ? nominal - 2 : 0;
@@ -99,29 +115,6 @@ __device__ __forceinline__ void q4tp_round(float (&w)[GROUP], float s, const flo
     const float dj = U[j * ldu + j];
     float ej = 0.f;
     if (dj > 0.f) ej = __fdiv_rn(__fsub_rn(w[j], __fmul_rn(q, s)), dj);
-    e[j] = ej;
-    if (ej != 0.f) {
-#pragma unroll
-      for (int t = j + 1; t < GROUP; ++t) w[t] = __fsub_rn(w[t], __fmul_rn(ej, U[j * ldu + t]));
-    }
-  }
-}
-
-// Act-order rounding of 32 consecutive (permuted) columns with per-column
-// scales ([host page] gptq_quantize_q4tp_act_order): q_j = clamp(rne(w_j /
-// s_j), -8, 7) (0 if s_j <= 0), e_j = (w_j - q_j s_j) / U_jj (0 if
-// U_jj <= 0), w_t -= e_j U_jt for t > j; one rounding per operation.
-__device__ __forceinline__ void q4tp_round_cols(float (&w)[GROUP], const float (&s)[GROUP],
-                                                const float* U, int ldu, int (&q8)[GROUP],
-                                                float (&e)[GROUP]) {
-#pragma unroll
-  for (int j = 0; j < GROUP; ++j) {
-    float q = 0.f;
-    if (s[j] > 0.f) q = fminf(fmaxf(rintf(__fdiv_rn(w[j], s[j])), -8.f), 7.f);
-    q8[j] = (int)q;
-    const float dj = U[j * ldu + j];
-    float ej = 0.f;
-    if (dj > 0.f) ej = __fdiv_rn(__fsub_rn(w[j], __fmul_rn(q, s[j])), dj);
     e[j] = ej;
     if (ej != 0.f) {
 #pragma unroll
@@ -228,18 +221,31 @@ __global__ void __launch_bounds__(128) k_group(const float* __restrict__ tile, i
   for (int t = 0; t < GROUP; ++t) E[(long long)r * GROUP + t] = e[t];
 }
 
-constexpr int SWEEP_ROWS = 32;
-constexpr int SWEEP_THREADS = 128;
-constexpr int LW = SB + 1;
-constexpr int EW = 2 * SB;  // residual / U-stripe buffers hold a pair of blocks
+constexpr int SWEEP_ROWS = 40;                 // 5 warps: 5120 rows fill 128 CTAs, one wave
+constexpr int SWEEP_THREADS = 4 * SWEEP_ROWS;  // a quad of lanes per row
+constexpr int LW = SB + 16;  // W block row stride: float4 rows, two rows per phase conflict-free
+constexpr int ESR = GROUP + 4;  // row stride of the group residuals in shared memory
+constexpr int EW = 2 * SB;   // residual / U-stripe buffers hold a pair of blocks
+constexpr int SWEEP_SMEM = (SB * SB + SB + SWEEP_ROWS * LW + SWEEP_ROWS * ESR) * 4;
 
-// One lazy block [b0, b0+B) (B <= SB) for 32 rows per CTA: the block's U
-// (B x B), rung weights and the rows' block of W sit in shared memory.  Group
-// by group, warp 0 runs the rung / rounding rule (one thread per row) and
-// writes nibbles, rung, scale and the residuals E (TF32 hi/lo, the trailing
-// GEMM's operand); then all four warps push the group's residuals into the
-// rest of the block (w_c -= sum_j e_j U_jc), each warp a quarter of the
-// columns.
+// One lazy block [b0, b0+B) (B <= SB, a multiple of 32) for 40 rows per CTA.
+// The block's U (B x B), the rung weights and the rows' block of W sit in
+// shared memory.  Each row belongs to a quad of four lanes of one warp (8
+// rows per warp), and a warp carries its rows through the whole block
+// without waiting on the other warps:
+//  * rung choice: lane k of the quad evaluates candidate nominal-2+k over
+//    the group's 32 columns (its own sum, in column order), the quad swaps
+//    the four sums and every lane takes the same pick;
+//  * rounding: every lane of the quad runs the row's 32 columns in full
+//    (no exchange on the sequential path).  Per column the critical path is
+//    the code, the residual and the next column's update; the updates of
+//    the later columns by the previous residual are issued after the
+//    column's first division, in its latency.  Each column still receives
+//    e_0, e_1, ... in order with one rounding per operation, so codes and
+//    residuals are the one-thread rule's bit for bit;
+//  * the group's residuals go to E (TF32 hi/lo, the trailing GEMM's
+//    operand) and into the block's later columns (w_c -= sum_j e_j U_jc),
+//    lane k taking the 4-column chunks 4k, 4k+16, ... .
 // ACT (act order): W and U are in permuted channel order, the rungs are
 // given (static, per original group) and each column takes the scale of its
 // original group; codes go to `codes` (int8, permuted order) instead of the
@@ -252,119 +258,192 @@ __global__ void __launch_bounds__(SWEEP_THREADS) k_sweep_block(
     float* __restrict__ E_hi, float* __restrict__ E_lo, int ecol0, const int* __restrict__ perm,
     int8_t* __restrict__ codes) {
   extern __shared__ __align__(16) float sm[];
-  float* Us = sm;                 // [SB][SB]
-  float* hws = Us + SB * SB;      // [SB]
-  float* Ws = hws + SB;           // [SWEEP_ROWS][LW]
-  float* Es = Ws + SWEEP_ROWS * LW;  // [SWEEP_ROWS][GROUP + 1]
+  float* Us = sm;             // [SB][SB]
+  float* hws = Us + SB * SB;  // [SB]
+  float* Ws = hws + SB;       // [SWEEP_ROWS][LW]
+  float* Es = Ws + SWEEP_ROWS * LW;  // [SWEEP_ROWS][ESR]
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   const int r0 = blockIdx.x * SWEEP_ROWS;
   {
-    // U block rows as float4 (B is a multiple of 32), 16 loads in flight per
-    // thread per batch.
+    // The block's U and the rows' block of W by asynchronous 16-byte copies
+    // (all in flight at once); rows past the end are zeros.
     const int q4 = B / 4;
-    const int tot = B * q4;
-#pragma unroll 1
-    for (int b = 0; b < tot; b += 16 * SWEEP_THREADS) {
-      float4 v[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const int e = b + tid + i * SWEEP_THREADS;
-        if (e < tot)
-          v[i] = *reinterpret_cast<const float4*>(U + (long long)(b0 + e / q4) * n + b0 + 4 * (e % q4));
-      }
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const int e = b + tid + i * SWEEP_THREADS;
-        if (e < tot) *reinterpret_cast<float4*>(Us + (e / q4) * SB + 4 * (e % q4)) = v[i];
-      }
+#pragma unroll 4
+    for (int e = tid; e < B * q4; e += SWEEP_THREADS)
+      cp_async16(Us + (e / q4) * SB + 4 * (e % q4), U + (long long)(b0 + e / q4) * n + b0 + 4 * (e % q4));
+#pragma unroll 4
+    for (int e = tid; e < SWEEP_ROWS * q4; e += SWEEP_THREADS) {
+      const int rr = e / q4, c4 = e % q4;
+      float* dst = Ws + rr * LW + 4 * c4;
+      if (r0 + rr < rows)
+        cp_async16(dst, W + (long long)(r0 + rr) * n + b0 + 4 * c4);
+      else
+        *reinterpret_cast<float4*>(dst) = make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    // The rows' block of W, coalesced along each row (warp w: rows w, w+4, ...).
-    float v[SWEEP_ROWS / 4][SB / 32];
-#pragma unroll
-    for (int i = 0; i < SWEEP_ROWS / 4; ++i)
-#pragma unroll
-      for (int kq = 0; kq < SB / 32; ++kq) {
-        const int rr = r0 + warp + 4 * i, c = kq * 32 + lane;
-        v[i][kq] = (rr < rows && c < B) ? W[(long long)rr * n + b0 + c] : 0.f;
-      }
-#pragma unroll
-    for (int i = 0; i < SWEEP_ROWS / 4; ++i)
-#pragma unroll
-      for (int kq = 0; kq < SB / 32; ++kq) Ws[(warp + 4 * i) * LW + kq * 32 + lane] = v[i][kq];
+    cp_async_wait_all();
   }
   for (int e = tid; e < B; e += SWEEP_THREADS) hws[e] = ACT ? 0.f : hw[b0 + e];
   __syncthreads();
-  const int r = r0 + lane;
+  const int sub = lane & 3, qbase = lane & ~3;
+  const int rl = warp * 8 + (lane >> 2);
+  const int r = r0 + rl;
   const bool live = r < rows;
+  const int rs = live ? r : rows - 1;  // rows past the end compute on a real row, store nothing
   const int gpr = n / GROUP;
-  float* wrow = Ws + lane * LW;
+  const float* tabrow = tab + (long long)rs * 32;
+  float* wrow = Ws + rl * LW;
+  float* es = Es + rl * ESR;
+  float lo = 0.f, st = 0.f;
+  if (!ACT) {
+    lo = lost[2 * rs];
+    st = lost[2 * rs + 1];
+  }
   for (int g = 0; g < B / GROUP; ++g) {
-    if (warp == 0 && live) {
-      const float* tabrow = tab + (long long)r * 32;
-      float w[GROUP], e[GROUP];
+    const int gc = g * GROUP;
+    float w[GROUP];
 #pragma unroll
-      for (int t = 0; t < GROUP; ++t) w[t] = wrow[g * GROUP + t];
+    for (int q = 0; q < GROUP / 4; ++q) {
+      const float4 v = *reinterpret_cast<const float4*>(wrow + gc + 4 * q);
+      w[4 * q] = v.x;
+      w[4 * q + 1] = v.y;
+      w[4 * q + 2] = v.z;
+      w[4 * q + 3] = v.w;
+    }
+    float s = 0.f;
+    int best_c = 0;
+    float sc[ACT ? GROUP : 1];
+    if (ACT) {
+#pragma unroll
+      for (int t = 0; t < GROUP; ++t) sc[t] = tabrow[rungs[(long long)rs * gpr + perm[b0 + gc + t] / GROUP]];
+    } else {
+      // Rung rule, one candidate per lane.
+      float amax = 0.f;
+#pragma unroll
+      for (int t = 0; t < GROUP; ++t) amax = fmaxf(amax, fabsf(w[t]));
+      const int nominal = (amax > 0.f && st > 0.f) ? nominal_rung(__fdiv_rn(amax, 7.0f), lo, st) : 0;
+      // Every lane of the warp reaches the exchange below (rows differ in
+      // amax, the four lanes of a quad do not); a row with amax == 0 has no
+      // valid candidate and keeps the nominal rung.
+      best_c = nominal;
+      const bool any = amax > 0.f;
+      const int lo_c = nominal >= 2 ? nominal - 2 : 0;
+      const int hi_c = nominal + 1 < 31 ? nominal + 1 : 31;
+      const int cand = lo_c + sub;
+      const float sck = (any && cand <= hi_c) ? tabrow[cand] : 0.f;
+      const bool valid = any && cand <= hi_c && sck > 0.f;
+      float err = 0.f;
+      if (any) {
+        const float iv = __fdiv_rn(1.0f, valid ? sck : 1.f);
+        const float* hg = hws + gc;
+#pragma unroll
+        for (int t = 0; t < GROUP; ++t) {
+          const float q = fminf(fmaxf(rintf(__fmul_rn(w[t], iv)), -8.f), 7.f);
+          const float d = __fsub_rn(w[t], __fmul_rn(q, sck));
+          err = __fadd_rn(err, __fmul_rn(__fmul_rn(hg[t], d), d));
+        }
+      }
+      float best_e = INFINITY;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float ek = __shfl_sync(0xffffffffu, err, qbase | k);
+        const int vk = __shfl_sync(0xffffffffu, (int)valid, qbase | k);
+        if (vk && ek < best_e) {
+          best_e = ek;
+          best_c = lo_c + k;
+        }
+      }
+      s = tabrow[best_c];
+    }
+    // Rounding with in-group feedback (software-pipelined, see above).
+    const float* Ug = Us + gc * SB + gc;
+    uint32_t words[ACT ? GROUP / 4 : GROUP / 8];
+#pragma unroll
+    for (int i = 0; i < (ACT ? GROUP / 4 : GROUP / 8); ++i) words[i] = 0u;
+    float eprev = 0.f;
+#pragma unroll
+    for (int j = 0; j < GROUP; ++j) {
+      const float x = w[j];  // current: e_{j-1} reached it at the end of the last step
+      const float sj = ACT ? sc[j] : s;
+      const float t1 = sj > 0.f ? __fdiv_rn(x, sj) : 0.f;
+      if (j > 0) {
+#pragma unroll
+        for (int t = j + 1; t < GROUP; ++t) w[t] = __fsub_rn(w[t], __fmul_rn(eprev, Ug[(j - 1) * SB + t]));
+      }
+      const float q = sj > 0.f ? fminf(fmaxf(rintf(t1), -8.f), 7.f) : 0.f;
+      const float dj = Ug[j * SB + j];
+      float ej = 0.f;
+      if (dj > 0.f) ej = __fdiv_rn(__fsub_rn(x, __fmul_rn(q, sj)), dj);
+      es[j] = ej;  // the same value from the four lanes
+      if (ACT)
+        words[j / 4] |= ((uint32_t)(int)q & 255u) << (8 * (j % 4));
+      else
+        words[j / 8] |= ((uint32_t)((int)q + 8) & 15u) << (4 * (j % 8));
+      if (j + 1 < GROUP) w[j + 1] = __fsub_rn(w[j + 1], __fmul_rn(ej, Ug[j * SB + j + 1]));
+      eprev = ej;
+    }
+    __syncwarp();
+    float e[GROUP];
+#pragma unroll
+    for (int q = 0; q < GROUP / 4; ++q) {
+      const float4 v = *reinterpret_cast<const float4*>(es + 4 * q);
+      e[4 * q] = v.x;
+      e[4 * q + 1] = v.y;
+      e[4 * q + 2] = v.z;
+      e[4 * q + 3] = v.w;
+    }
+    if (live) {
       if (ACT) {
-        float sc[GROUP];
-        int q8[GROUP];
+        // Lane k stores the int8 codes of columns 8k .. 8k+7.
 #pragma unroll
-        for (int t = 0; t < GROUP; ++t)
-          sc[t] = tabrow[rungs[(long long)r * gpr + perm[b0 + g * GROUP + t] / GROUP]];
-        q4tp_round_cols(w, sc, Us + g * GROUP * SB + g * GROUP, SB, q8, e);
-        uint32_t pk[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-          pk[i] = (uint32_t)(q8[4 * i] & 255) | ((uint32_t)(q8[4 * i + 1] & 255) << 8) |
-                  ((uint32_t)(q8[4 * i + 2] & 255) << 16) | ((uint32_t)(q8[4 * i + 3] & 255) << 24);
-        uint4* dst = reinterpret_cast<uint4*>(codes + (long long)r * n + b0 + g * GROUP);
-        dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-        dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-      } else {
-        const float lo = lost[2 * r], st = lost[2 * r + 1];
-        const int c = q4tp_pick(w, hws + g * GROUP, tabrow, lo, st);
-        const float s = tabrow[c];
-        uint32_t words[4];
-        q4tp_round(w, s, Us + g * GROUP * SB + g * GROUP, SB, words, e);
+        for (int c = 0; c < 4; ++c)
+          if (sub == c)
+            *reinterpret_cast<uint2*>(codes + (long long)r * n + b0 + gc + 8 * c) =
+                make_uint2(words[2 * c], words[2 * c + 1]);
+      } else if (sub == 0) {
         const long long tix = (long long)r * gpr + b0 / GROUP + g;
         reinterpret_cast<uint4*>(nib)[tix] = make_uint4(words[0], words[1], words[2], words[3]);
-        rungs[tix] = (uint8_t)c;
+        rungs[tix] = (uint8_t)best_c;
         scales[tix] = s;
       }
-      float4* eh = reinterpret_cast<float4*>(E_hi + (long long)r * EW + ecol0 + g * GROUP);
-      float4* el = reinterpret_cast<float4*>(E_lo + (long long)r * EW + ecol0 + g * GROUP);
+      float* eh = E_hi + (long long)r * EW + ecol0 + gc;
+      float* el = E_lo + (long long)r * EW + ecol0 + gc;
 #pragma unroll
-      for (int t = 0; t < GROUP / 4; ++t) {
-        float4 h, l;
-        split_tf32(e[4 * t], h.x, l.x);
-        split_tf32(e[4 * t + 1], h.y, l.y);
-        split_tf32(e[4 * t + 2], h.z, l.z);
-        split_tf32(e[4 * t + 3], h.w, l.w);
-        eh[t] = h;
-        el[t] = l;
-      }
+      for (int c = 0; c < 4; ++c) {
+        if (sub != c) continue;
 #pragma unroll
-      for (int t = 0; t < GROUP; ++t) Es[lane * (GROUP + 1) + t] = e[t];
-    }
-    __syncthreads();
-    const int rest = B - (g + 1) * GROUP;  // later columns of the block
-    if (rest > 0 && live) {
-      float e[GROUP];
-#pragma unroll
-      for (int t = 0; t < GROUP; ++t) e[t] = Es[lane * (GROUP + 1) + t];
-      const int per = rest / 4;  // multiple of 8
-      const int c0 = (g + 1) * GROUP + warp * per;
-#pragma unroll 2
-      for (int col = c0; col < c0 + per; ++col) {
-        float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-        for (int j = 0; j < GROUP; j += 2) {
-          a0 = fmaf(e[j], Us[(g * GROUP + j) * SB + col], a0);
-          a1 = fmaf(e[j + 1], Us[(g * GROUP + j + 1) * SB + col], a1);
+        for (int t = 0; t < 2; ++t) {
+          float4 h, l;
+          split_tf32(e[8 * c + 4 * t], h.x, l.x);
+          split_tf32(e[8 * c + 4 * t + 1], h.y, l.y);
+          split_tf32(e[8 * c + 4 * t + 2], h.z, l.z);
+          split_tf32(e[8 * c + 4 * t + 3], h.w, l.w);
+          reinterpret_cast<float4*>(eh + 8 * c)[t] = h;
+          reinterpret_cast<float4*>(el + 8 * c)[t] = l;
         }
-        wrow[col] -= a0 + a1;
       }
     }
-    __syncthreads();
+    // The group's residuals into the rest of the block.
+    const int rest = B - gc - GROUP;
+#pragma unroll 1
+    for (int m = 0; m < rest / 16; ++m) {
+      const int c = gc + GROUP + 16 * m + 4 * sub;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int j = 0; j < GROUP; ++j) {
+        const float4 u = *reinterpret_cast<const float4*>(Us + (gc + j) * SB + c);
+        acc.x = fmaf(e[j], u.x, acc.x);
+        acc.y = fmaf(e[j], u.y, acc.y);
+        acc.z = fmaf(e[j], u.z, acc.z);
+        acc.w = fmaf(e[j], u.w, acc.w);
+      }
+      float4 v = *reinterpret_cast<float4*>(wrow + c);
+      v.x -= acc.x;
+      v.y -= acc.y;
+      v.z -= acc.z;
+      v.w -= acc.w;
+      *reinterpret_cast<float4*>(wrow + c) = v;
+    }
+    __syncwarp();
   }
 }
 
@@ -415,9 +494,9 @@ static gptq_status sweep_attrs() {
   static bool done = false;
   if (done) return GPTQ_OK;
   GQ_CUDA(cudaFuncSetAttribute(k_sweep_block<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (SB * SB + SB + SWEEP_ROWS * LW + SWEEP_ROWS * (GROUP + 1)) * 4));
+                               SWEEP_SMEM));
   GQ_CUDA(cudaFuncSetAttribute(k_sweep_block<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (SB * SB + SB + SWEEP_ROWS * LW + SWEEP_ROWS * (GROUP + 1)) * 4));
+                               SWEEP_SMEM));
   done = true;
   return GPTQ_OK;
 }
@@ -492,7 +571,7 @@ static gptq_status sweep_core(float* W, int rows, int n, const float* U, const f
   GQ_TRY(make_operand_map(&maps.m[2], E_hi, rows, EW));
   GQ_TRY(make_operand_map(&maps.m[3], E_lo, rows, EW));
   GQ_TRY(make_c_map(&maps.c, W, rows, n, n));
-  const int smem = (SB * SB + SB + SWEEP_ROWS * LW + SWEEP_ROWS * (GROUP + 1)) * 4;
+  const int smem = SWEEP_SMEM;
   const TcJob none{};
   const int grid_rows = (rows + SWEEP_ROWS - 1) / SWEEP_ROWS;
   auto block = [&](int b0, int B, int ecol0) -> gptq_status {
