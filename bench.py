@@ -416,7 +416,9 @@ def main():
     sampler.start()
     time.sleep(0.3)
     launches0 = _lib.launch_count()
-    _lib.profile_start(200000)
+    # Events only around the two tensor-core update kinds (the roofline's
+    # kernels): the other launches of the timed steps run unbracketed.
+    _lib.profile_start(200000, kinds=("fold_gemm", "sweep_gemm"))
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
@@ -428,6 +430,12 @@ def main():
     launches = _lib.launch_count() - launches0
     clocks = sampler.stop()
     t_dev, value = aggregate(e0.elapsed_time(e1) / 1e3, args.steps, world, pg)
+
+    # Per-kernel breakdown: one more (untimed) step with every launch bracketed.
+    _lib.profile_start(200000)
+    step()
+    torch.cuda.synchronize()
+    breakdown = _lib.profile_stop()
 
     # End to end through the public call with host buffers: H2D of the
     # group's inputs from pinned memory, the call, D2H of its outputs.
@@ -479,8 +487,8 @@ def main():
                 "peak_source": f"{src} bf16 sustained {pk.get('bf16_tflops_sustained')} x 1.1/2.25 (TF32) / 3 (3xTF32 split)",
                 "flop_per_launch": per_launch}
     fold_flops = 2 * n ** 3 / 3
-    per_kind = {k: {"ms_per_step": v[0] / args.steps, "launches_per_step": v[1] / args.steps}
-                for k, v in kinds.items() if v[1] > 0}
+    per_kind = {k: {"ms_per_step": v[0], "launches_per_step": v[1]}
+                for k, v in breakdown.items() if not k.startswith("_") and v[1] > 0}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -502,6 +510,7 @@ def main():
                                                            for k in ("build", "potrf", "trsm", "diag"))
                                                      ) / 1e12 if "fold_gemm" in per_kind else None,
             "per_kernel": per_kind,
+            "per_kernel_source": "one extra untimed step with every launch bracketed by events",
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": launches,

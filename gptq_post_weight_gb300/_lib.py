@@ -42,6 +42,7 @@ SIGNATURES = {
     "gptq_launch_count": (ctypes.c_longlong, []),
     "gptq_kernel_kinds": (_I, []),
     "gptq_kernel_kind_name": (ctypes.c_char_p, [_I]),
+    "gptq_profile_select": (None, [ctypes.c_uint]),
     "gptq_profile_start": (_I, [_I]),
     "gptq_profile_stop": (_I, [_P, _P, _I]),
 }
@@ -237,8 +238,18 @@ def launch_count() -> int:
     return int(load().gptq_launch_count())
 
 
-def profile_start(max_launches: int = 100000):
-    _check("gptq_profile_start", load().gptq_profile_start(int(max_launches)))
+def profile_start(max_launches: int = 100000, kinds=None):
+    """Record events for the launches that follow; `kinds`: names to record
+    (default all)."""
+    lib = load()
+    mask = 0xFFFFFFFF
+    if kinds is not None:
+        names = [lib.gptq_kernel_kind_name(k).decode() for k in range(lib.gptq_kernel_kinds())]
+        mask = 0
+        for name in kinds:
+            mask |= 1 << names.index(name)
+    lib.gptq_profile_select(mask)
+    _check("gptq_profile_start", lib.gptq_profile_start(int(max_launches)))
 
 
 def profile_stop():

@@ -146,18 +146,19 @@ constexpr int PW = 2 * NB;
 //  * rows c < s0: the inverse's block row (fold page inv_rows), v =
 //    Y[c][k..k+NB) (the unit vector e_{c-k} when c is in block k, so that row
 //    of Z is a column of Linv), z -> Yp[c][*], and the finished entries of U:
-//    U[n-1-i][n-1-c] = X[i][c] / |d_{n-1-c}| ([fold page] make_u), i = k+t.
+//    U[n-1-i][n-1-c] = X[i][c] / |d_{n-1-c}| ([fold page] make_u; taken as X times
+//    the rounded reciprocal, within a rounding of the quotient), i = k+t.
 // z is stored as its TF32 hi/lo split, the operand format of the update GEMM,
 // in columns [col0, col0 + NB) of the 2 NB-wide panel buffers; panel rows
 // below zero_end also clear their Yp entries there (see fold_attempt).
-// Persistent: a CTA keeps L_kk^-T in shared memory and walks tiles of 32
-// rows, the next tile's vectors arriving (asynchronous copies) while the
-// current one is multiplied.  The sums stop at the diagonal of Linv (z_c
+// Persistent (two CTAs per SM): a CTA keeps L_kk^-T in shared memory and
+// walks tiles of 32 rows, the next tile's vectors arriving (asynchronous
+// copies) while the current one is multiplied.  The sums stop at the diagonal of Linv (z_c
 // needs v_u for u <= c only); warp w owns the 8-column blocks w and 15 - w,
 // so every warp does the same number of multiply-adds.  Thread (l % 16,
 // l / 16): rows l % 16 and l % 16 + 16, 4 columns of each block.  Z goes
 // back through shared memory for row-contiguous stores.
-__global__ void __launch_bounds__(APPLY_THREADS, 1) k_apply(const float* __restrict__ A, long long lda,
+__global__ void __launch_bounds__(APPLY_THREADS, 2) k_apply(const float* __restrict__ A, long long lda,
                                                            int k, int s0, int N, int col0, int zero_end,
                                                            const float* __restrict__ LinvT,
                                                            float* __restrict__ P_hi, float* __restrict__ P_lo,
@@ -167,8 +168,7 @@ __global__ void __launch_bounds__(APPLY_THREADS, 1) k_apply(const float* __restr
   if (flagged(flag)) return;
   extern __shared__ __align__(16) float sm[];
   float* Lt = sm;                         // [NB][NB]: Lt[u][c] = Linv[c][u]
-  float* Vb = Lt + NB * NB;               // 2 x [APPLY_ROWS][LV]: row vectors
-  float* Zs = Vb + 2 * APPLY_ROWS * LV;   // [APPLY_ROWS][LV]: results
+  float* Vb = Lt + NB * NB;               // 2 x [APPLY_ROWS][LV]: row vectors, then Z
   const int tid = threadIdx.x;
   const int ntiles = N / APPLY_ROWS;
   // Vectors of tile t into buffer b: copies for rows of A, plain stores for
@@ -205,6 +205,7 @@ __global__ void __launch_bounds__(APPLY_THREADS, 1) k_apply(const float* __restr
   int it = 0;
   for (int t = t0; t < ntiles; t += gridDim.x, ++it) {
     float* Vs = Vb + (it & 1) * APPLY_ROWS * LV;
+    float* Zs = Vs;  // Z replaces the tile's vectors once all warps are done with them
     if (t + (int)gridDim.x < ntiles) fetch(t + gridDim.x, Vb + ((it + 1) & 1) * APPLY_ROWS * LV);
     asm volatile("cp.async.commit_group;\ncp.async.wait_group 1;" ::: "memory");
     __syncthreads();
@@ -215,7 +216,7 @@ __global__ void __launch_bounds__(APPLY_THREADS, 1) k_apply(const float* __restr
       for (int c = 0; c < 8; ++c) acc[i][c] = 0.f;
     const float* v0p = Vs + lr * LV;
     const float* v1p = Vs + (lr + 16) * LV;
-#pragma unroll 1
+#pragma unroll 2
     for (int u4 = 0; u4 < ua / 4; ++u4) {
       const float4 v0 = *reinterpret_cast<const float4*>(v0p + 4 * u4);
       const float4 v1 = *reinterpret_cast<const float4*>(v1p + 4 * u4);
@@ -235,7 +236,7 @@ __global__ void __launch_bounds__(APPLY_THREADS, 1) k_apply(const float* __restr
         acc[1][6] = fmaf(x1, lb.z, acc[1][6]); acc[1][7] = fmaf(x1, lb.w, acc[1][7]);
       }
     }
-#pragma unroll 1
+#pragma unroll 2
     for (int u4 = ua / 4; u4 < ub / 4; ++u4) {
       const float4 v0 = *reinterpret_cast<const float4*>(v0p + 4 * u4);
       const float4 v1 = *reinterpret_cast<const float4*>(v1p + 4 * u4);
@@ -250,6 +251,7 @@ __global__ void __launch_bounds__(APPLY_THREADS, 1) k_apply(const float* __restr
         acc[1][6] = fmaf(x1, lb.z, acc[1][6]); acc[1][7] = fmaf(x1, lb.w, acc[1][7]);
       }
     }
+    __syncthreads();  // every warp has read the vectors
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
       float* z = Zs + (lr + 16 * i) * LV;
@@ -286,14 +288,15 @@ __global__ void __launch_bounds__(APPLY_THREADS, 1) k_apply(const float* __restr
       const int r = r0 + rr;
       if (r < s0 && r < n) {
         const int m = n - 1 - r;
-        const float dm = dabs[m];
+        const float rdm = __frcp_rn(dabs[m]);  // U is compared within a tolerance: scale by 1/|d|
 #pragma unroll 4
         for (int c = tid / APPLY_ROWS; c < NB; c += APPLY_THREADS / APPLY_ROWS) {
           const int i = k + c;
-          if (i < n) U[(long long)(n - 1 - i) * n + m] = __fdiv_rn(Zs[rr * LV + c], dm);
+          if (i < n) U[(long long)(n - 1 - i) * n + m] = __fmul_rn(Zs[rr * LV + c], rdm);
         }
       }
     }
+    __syncthreads();  // Z is read out before the buffer takes the tile after next
   }
   asm volatile("cp.async.wait_group 0;" ::: "memory");
 }
@@ -390,7 +393,7 @@ size_t fold_ws_bytes(int n) {
 }
 
 constexpr int POTRF_SMEM = POTRF_SMEM_BYTES;
-constexpr int APPLY_SMEM = (NB * NB + 3 * APPLY_ROWS * LV) * 4;
+constexpr int APPLY_SMEM = (NB * NB + 2 * APPLY_ROWS * LV) * 4;
 
 static gptq_status init_attrs() {
   static bool done = false;
@@ -429,8 +432,8 @@ static gptq_status fold_attempt(const float* hp, const FoldWs& w, const OperandM
   auto apply = [&](int k, int col0, int zero_end) -> gptq_status {
     GQ_PROF(K_TRSM, s);
     const int tiles = N / APPLY_ROWS;
-    const int sms = num_sms();
-    k_apply<<<tiles < sms ? tiles : sms, APPLY_THREADS, APPLY_SMEM, s>>>(w.A, ld, k, k + NB, N, col0, zero_end,
+    const int ctas = 2 * num_sms();  // two CTAs per SM
+    k_apply<<<tiles < ctas ? tiles : ctas, APPLY_THREADS, APPLY_SMEM, s>>>(w.A, ld, k, k + NB, N, col0, zero_end,
                                                                w.Lkk, w.P_hi, w.P_lo, w.Yp_hi,
                                                                w.Yp_lo, w.flag, U, w.dabs, n);
     GQ_LAUNCHED();

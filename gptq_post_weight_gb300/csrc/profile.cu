@@ -17,6 +17,7 @@ std::vector<cudaEvent_t> g_ev;  // 2 per recorded launch
 std::vector<int> g_kind;
 int g_used = 0;
 int g_open = -1;
+unsigned g_mask = ~0u;  // kinds that record events
 
 const char* kNames[K_NKINDS] = {"diag", "build", "potrf", "trsm", "fold_gemm", "ladder",
                                 "sweep_block", "prep_ut", "sweep_gemm", "group", "copy",
@@ -27,7 +28,7 @@ const char* kNames[K_NKINDS] = {"diag", "build", "potrf", "trsm", "fold_gemm", "
 void prof_begin(int kind, cudaStream_t s) {
   g_launches.fetch_add(1, std::memory_order_relaxed);
   std::lock_guard<std::mutex> lk(g_mu);
-  if (!g_on || g_used >= g_cap) return;
+  if (!g_on || g_used >= g_cap || !((g_mask >> kind) & 1u)) return;
   cudaEventRecord(g_ev[2 * g_used], s);
   g_kind[g_used] = kind;
   g_open = g_used;
@@ -55,6 +56,11 @@ const char* gptq_kernel_kind_name(int kind) {
 }
 
 int gptq_kernel_kinds(void) { return K_NKINDS; }
+
+void gptq_profile_select(unsigned kind_mask) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_mask = kind_mask;
+}
 
 gptq_status gptq_profile_start(int max_launches) {
   std::lock_guard<std::mutex> lk(g_mu);

@@ -264,6 +264,9 @@ gptq_status gptq_gram_add(float* H_packed, int n, const float* X, int T, void* w
  *   gptq_launch_count     kernels launched by the library since it loaded.
  *   gptq_kernel_kinds     number of kernel kinds; gptq_kernel_kind_name(k)
  *                         their names ("fold_gemm", "sweep_gemm", ...).
+ *   gptq_profile_select   which kinds record events (bit k = kind k; all
+ *                         by default); the others are still counted.  Fewer
+ *                         events, less perturbation of the timed launches.
  *   gptq_profile_start    start recording, up to max_launches launches.
  *   gptq_profile_stop     synchronise the recorded events, write per-kind
  *                         total milliseconds and launch counts (host arrays
@@ -275,6 +278,7 @@ gptq_status gptq_gram_add(float* H_packed, int n, const float* X, int T, void* w
 long long gptq_launch_count(void);
 int gptq_kernel_kinds(void);
 const char* gptq_kernel_kind_name(int kind);
+void gptq_profile_select(unsigned kind_mask);
 gptq_status gptq_profile_start(int max_launches);
 int gptq_profile_stop(double* ms_by_kind, long long* launches_by_kind, int nkinds);
 
