@@ -90,7 +90,8 @@ def sweep_gemm_flops(rows, n, SB=128):
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    """nvidia-smi clocks, power and throttle reasons sampled every 20 ms;
+    only the samples inside [t0, t1] (host clock) count."""
 
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -105,7 +106,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "20"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (OSError, ValueError):
             self.proc = None
             return
@@ -114,9 +115,9 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.perf_counter(), line.strip()))
 
-    def stop(self):
+    def stop(self, t0=None, t1=None):
         if self.proc is None:
             return None
         self.proc.terminate()
@@ -124,9 +125,11 @@ class ClockSampler:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-        sm, mx, reasons = [], None, set()
+        sm, pw, mx, reasons = [], [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        for ts, ln in self.lines:
+            if (t0 is not None and ts < t0) or (t1 is not None and ts > t1):
+                continue
             f = [x.strip() for x in ln.split(",")]
             if len(f) < 9:
                 continue
@@ -135,12 +138,17 @@ class ClockSampler:
                 mx = float(f[2])
             except ValueError:
                 continue
+            try:
+                pw.append(float(f[3]))
+            except ValueError:
+                pass
             for nm, v in zip(names, f[5:9]):
                 if v.lower().startswith("active"):
                     reasons.add(nm)
         if not sm:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "sm_min_mhz": min(sm),
+                "power_w": statistics.median(pw) if pw else None, "reasons": sorted(reasons),
                 "samples": len(sm)}
 
 
@@ -421,14 +429,16 @@ def main():
     _lib.profile_start(200000, kinds=("fold_gemm", "sweep_gemm"))
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+    t_host0 = time.perf_counter()
     e0.record(stream)
     for _ in range(args.steps):
         step()
     e1.record(stream)
     torch.cuda.synchronize()
+    t_host1 = time.perf_counter()
     prof = _lib.profile_stop()
     launches = _lib.launch_count() - launches0
-    clocks = sampler.stop()
+    clocks = sampler.stop(t_host0, t_host1)
     t_dev, value = aggregate(e0.elapsed_time(e1) / 1e3, args.steps, world, pg)
 
     # Per-kernel breakdown: one more (untimed) step with every launch bracketed.
@@ -437,33 +447,51 @@ def main():
     torch.cuda.synchronize()
     breakdown = _lib.profile_stop()
 
-    # End to end through the public call with host buffers: H2D of the
-    # group's inputs from pinned memory, the call, D2H of its outputs.
+    # End to end through the public call with host buffers: every step
+    # copies its group's inputs from pinned host memory, runs the call and
+    # reads its outputs back.  Two device buffer sets and a copy stream let
+    # the next group's upload run under the current group's compute (the
+    # call returns once its stream is idle, so a set is free again by then).
     e2e = None
     if not args.no_e2e:
         hp_h = hp.cpu().pin_memory()
         w_h = w.cpu().pin_memory()
-        outs_h = tuple(torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs)
-        hp_d = torch.empty_like(hp)
-        w_d = torch.empty_like(w)
+        outs_h = [tuple(torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs) for _ in range(2)]
+        sets = [(torch.empty_like(hp), torch.empty_like(w), outs),
+                (torch.empty_like(hp), torch.empty_like(w), tuple(torch.empty_like(o) for o in outs))]
+        copy = torch.cuda.Stream(dev)
+        ready = [torch.cuda.Event(), torch.cuda.Event()]
 
-        def e2e_step():
-            hp_d.copy_(hp_h, non_blocking=True)
-            w_d.copy_(w_h, non_blocking=True)
-            _lib.quantize_group(hp_d, n, w_d, cfg.lam, ws=ws, want_u=False, stream=stream, out=outs)
-            for o_h, o in zip(outs_h, outs):
-                o_h.copy_(o, non_blocking=True)
+        def upload(j):
+            hp_d, w_d, _ = sets[j % 2]
+            with torch.cuda.stream(copy):
+                hp_d.copy_(hp_h, non_blocking=True)
+                w_d.copy_(w_h, non_blocking=True)
+                ready[j % 2].record(copy)
 
-        e2e_step()
+        def e2e_run(k):
+            upload(0)
+            for j in range(k):
+                if j + 1 < k:
+                    upload(j + 1)
+                hp_d, w_d, o_d = sets[j % 2]
+                stream.wait_event(ready[j % 2])
+                _lib.quantize_group(hp_d, n, w_d, cfg.lam, ws=ws, want_u=False, stream=stream, out=o_d)
+                copy.wait_stream(stream)
+                with torch.cuda.stream(copy):
+                    for o_h, o in zip(outs_h[j % 2], o_d):
+                        o_h.copy_(o, non_blocking=True)
+            torch.cuda.synchronize()
+
+        e2e_run(2)
         barrier()
         t0 = time.perf_counter()
-        for _ in range(args.steps):
-            e2e_step()
-        torch.cuda.synchronize()
+        e2e_run(args.steps)
         t_e2e, v_e2e = aggregate(time.perf_counter() - t0, args.steps, world, pg)
         e2e = {"value": v_e2e, "unit": UNIT,
                "h2d_bytes_per_step": hp.numel() * 4 + w.numel() * 4,
-               "d2h_bytes_per_step": sum(o.numel() * o.element_size() for o in outs)}
+               "d2h_bytes_per_step": sum(o.numel() * o.element_size() for o in outs),
+               "overlap": "next group's upload on a copy stream under the current group's compute"}
 
     # Roofline of the dominant kernel kind, from the live event timings.
     pk, src = peaks()

@@ -17,10 +17,12 @@ constexpr int POTRF_SMEM_BYTES = 3 * NB * LDS * 4;
 // are solved against it (one thread per row), then a rank-32 update of the
 // rest of the block (4 x 4 register tiles).  Pivot test of the fold page's
 // chol_diag: !(piv > 0) (NaN included) -> flag, piv := 1.
-// Inverse ([fold page] inv_diag, blocked): the four 32 x 32 diagonal blocks
-// are inverted by four warps (lane = column), then the off-diagonal blocks
-// by block diagonals: X_ij = -X_ii sum_{j <= m < i} L_im X_mj, as register-
-// tiled block products.
+// Inverse ([fold page] inv_diag, blocked): each 32 x 32 diagonal block comes
+// out of its panel's triangular solve (identity rows solved beside the rows
+// below), then the off-diagonal blocks by block diagonals: X_ij = -X_ii
+// sum_{j <= m < i} L_im X_mj, as register-tiled block products.  Loops stay
+// rolled where unrolling buys little: the step runs once per block column on
+// whichever SM its CTA lands on, mostly from a cold instruction cache.
 // Output: LinvT = Linv transposed (NB x NB, LinvT[c][r] = Linv[r][c], zeros
 // below its diagonal).
 // Runs on the whole CTA (any multiple of 32 threads >= 128); S is at least
@@ -110,10 +112,17 @@ static __device__ __noinline__ void potrf_inverse_block(const float* __restrict_
         if (j <= lane) S[(p + lane) * LDS + p + j] = a[j];
     }
     __syncthreads();
-    for (int r = p + 32 + tid; r < NB; r += NT) {
+    // Rows below the panel, L_rp = A_rp L_pp^-T, and after them 32 identity
+    // rows e_t0, whose solutions are the rows of L_pp^-T, i.e. the columns of
+    // X_pp = L_pp^-1 (the inverse's diagonal block, zeros above its diagonal):
+    // one code path for both.
+    const int nbelow = NB - p - 32;
+    for (int v = tid; v < nbelow + 32; v += NT) {
+      const bool unit = v >= nbelow;
+      const int r = p + 32 + v, t0 = v - nbelow;
       float x[32];
 #pragma unroll
-      for (int t = 0; t < 32; ++t) x[t] = S[r * LDS + p + t];
+      for (int t = 0; t < 32; ++t) x[t] = unit ? (t == t0 ? 1.f : 0.f) : S[r * LDS + p + t];
 #pragma unroll
       for (int t = 0; t < 32; ++t) {
         float a0 = 0.f, a1 = 0.f;
@@ -125,8 +134,13 @@ static __device__ __noinline__ void potrf_inverse_block(const float* __restrict_
         if (t & 1) a0 = fmaf(x[t - 1], S[(p + t) * LDS + p + t - 1], a0);
         x[t] = (x[t] - (a0 + a1)) * rinv[p + t];
       }
+      if (unit) {
 #pragma unroll
-      for (int t = 0; t < 32; ++t) S[r * LDS + p + t] = x[t];
+        for (int t = 0; t < 32; ++t) Li[(p + t) * LDS + p + t0] = x[t];
+      } else {
+#pragma unroll
+        for (int t = 0; t < 32; ++t) S[r * LDS + p + t] = x[t];
+      }
     }
     __syncthreads();
     const int m = NB - p - 32;  // rows/cols of the remaining block
@@ -165,35 +179,13 @@ static __device__ __noinline__ void potrf_inverse_block(const float* __restrict_
     __syncthreads();
   }
   if (bad && tid == 0) atomicOr(flag, 1u);
-  // Inverse.  Diagonal blocks: warp b, lane j = column j of inv(L_bb).
-  for (int e = tid; e < NB * LDS; e += NT) Li[e] = 0.f;
-  __syncthreads();
-  if (warp < 4) {
-    const int b = warp * 32;
-    float x[32];
-#pragma unroll
-    for (int t = 0; t < 32; ++t) {
-      float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-      for (int u = 0; u + 1 < t; u += 2) {
-        a0 = fmaf(S[(b + t) * LDS + b + u], x[u], a0);
-        a1 = fmaf(S[(b + t) * LDS + b + u + 1], x[u + 1], a1);
-      }
-      if (t & 1) a0 = fmaf(S[(b + t) * LDS + b + t - 1], x[t - 1], a0);
-      x[t] = (((t == lane) ? 1.f : 0.f) - (a0 + a1)) * rinv[b + t];
-    }
-#pragma unroll
-    for (int t = 0; t < 32; ++t)
-      if (t >= lane) Li[(b + t) * LDS + b + lane] = x[t];
-  }
-  __syncthreads();
   // Off-diagonal blocks, one block diagonal d at a time: for block (i, j),
   // i = j + d, the products L_im X_mj (m = j .. i-1, each 32 x 32 x 32) go
   // to partials P in T, then X_ij = -X_ii (P_j + P_j+1 + ...), partials
   // summed in m order.  Every product is cut into 64 register tiles of
   // 4 x 4; the zero upper halves of X_jj and X_ii are simply multiplied.
   constexpr int PS = 33;  // partial row stride
-#pragma unroll
+#pragma unroll 1
   for (int d = 1; d < 4; ++d) {
     const int nblk = 4 - d;
     for (int tix = tid; tix < nblk * d * 64; tix += NT) {
@@ -245,7 +237,8 @@ static __device__ __noinline__ void potrf_inverse_block(const float* __restrict_
         for (int jj = 0; jj < 4; ++jj) {
           float t = P[k * PS + jj];
 #pragma unroll
-          for (int q = 1; q < d; ++q) t += P[q * 32 * PS + k * PS + jj];
+          for (int q = 1; q < 3; ++q)
+            if (q < d) t += P[q * 32 * PS + k * PS + jj];
           bv[jj] = t;
         }
 #pragma unroll
