@@ -152,6 +152,14 @@ struct FusedPotrf {
   int on;
 };
 
+// The same on pairs of SMs (gemm_pair.cu): tiles of 256 x 256, each shared by
+// the two CTAs of a cluster; for large updates.  Tile 0 of a fused job is
+// the 256 x 256 block at the job's origin (its first 128 rows and columns
+// hold the diagonal block).
+gptq_status gemm_pair_sub(const OperandMaps& maps, const TcJob& j0, const TcJob& j1, int K,
+                          const unsigned* flag, unsigned* status, int kind, cudaStream_t s,
+                          const FusedPotrf& fp = FusedPotrf{}, int kseg = 0);
+
 // Enqueue C -= A B^T for up to two jobs in one persistent launch.
 // `flag`: skip everything when non-zero (may be null).  `status`: bit 1 is
 // set if a device-side wait timed out.

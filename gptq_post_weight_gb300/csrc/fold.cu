@@ -460,7 +460,7 @@ static gptq_status fold_attempt(const float* hp, const FoldWs& w, const OperandM
       if (s1 < N) {
         const TcJob syrk = tc_lower(s1, s1, 0, s1, N - s1);
         const TcJob inv = tc_rect(s1, 0, 2, 0, 0, s1, s1, N - s1);
-        GQ_TRY(gemm_tc_sub(maps, syrk, inv, 2 * NB, w.flag, w.flag, K_FOLD_GEMM, s, fused(s1)));
+        GQ_TRY(gemm_pair_sub(maps, syrk, inv, 2 * NB, w.flag, w.flag, K_FOLD_GEMM, s, fused(s1)));
       }
       k = s1;
     } else {

@@ -98,7 +98,7 @@ gptq_status gram_run(float* Hp, int n, const float* X, int T, void* ws, size_t w
     }
     TcJob j = tc_lower(0, 0, 0, 0, N);
     j.add = 1;  // C += A A^T
-    GQ_TRY(gemm_tc_sub(maps, j, none, K, status, status, K_GRAM_GEMM, s, FusedPotrf{}, KSEG));
+    GQ_TRY(gemm_pair_sub(maps, j, none, K, status, status, K_GRAM_GEMM, s, FusedPotrf{}, KSEG));
   }
   {
     GQ_PROF(K_GRAM_PREP, s);

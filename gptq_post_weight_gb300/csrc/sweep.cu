@@ -605,8 +605,8 @@ static gptq_status sweep_core(float* W, int rows, int n, const float* U, const f
                          K_SWEEP_GEMM, s));
       GQ_TRY(block(b1, SB, SB));
       if (b2 < n)
-        GQ_TRY(gemm_tc_sub(maps, tc_rect(b2, 0, 2, 0, 0, SB, rows, n - b2), none, 2 * SB, status,
-                           status, K_SWEEP_GEMM, s));
+        GQ_TRY(gemm_pair_sub(maps, tc_rect(b2, 0, 2, 0, 0, SB, rows, n - b2), none, 2 * SB, status,
+                             status, K_SWEEP_GEMM, s));
       b0 = b2;
     } else {
       const int B = (n - b0) < SB ? (n - b0) : SB;
