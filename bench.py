@@ -34,10 +34,11 @@ UNIT = "s/group"
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # Nominal dense tensor ratios (TF32 : BF16 = 1.1 : 2.25 PFLOP/s).
 TF32_PER_BF16 = 1.1 / 2.25
-# DRAM bytes per launch of the dominant kernels at the bench workload, from
-# the committed ncu summaries under profiles/ (None until measured for the
-# current kernel version).
-TRAFFIC = {}
+# DRAM bytes (read + write) per launch of the update kinds at the bench
+# workload, from the launch list summarised in profiles/launches_n17408.md
+# (one-pass ncu capture of the current kernels); drop an entry whenever its
+# kernels change.
+TRAFFIC = {"fold_gemm": 412.4e6, "sweep_gemm": 170.6e6}
 
 
 def peaks():
