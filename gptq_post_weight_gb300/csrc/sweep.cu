@@ -266,7 +266,7 @@ __global__ void __launch_bounds__(SWEEP_THREADS) k_sweep_block(
   const int r0 = blockIdx.x * SWEEP_ROWS;
   {
     // The block's U and the rows' block of W by asynchronous 16-byte copies
-    // (all in flight at once); rows past the end are zeros.
+    // (all in flight at once); rows past the end are filled with ones.
     const int q4 = B / 4;
 #pragma unroll 4
     for (int e = tid; e < B * q4; e += SWEEP_THREADS)
@@ -277,8 +277,8 @@ __global__ void __launch_bounds__(SWEEP_THREADS) k_sweep_block(
       float* dst = Ws + rr * LW + 4 * c4;
       if (r0 + rr < rows)
         cp_async16(dst, W + (long long)(r0 + rr) * n + b0 + 4 * c4);
-      else
-        *reinterpret_cast<float4*>(dst) = make_float4(0.f, 0.f, 0.f, 0.f);
+      else  // rows past the end round ones (a zero dividend sends a division down its slow path)
+        *reinterpret_cast<float4*>(dst) = make_float4(1.f, 1.f, 1.f, 1.f);
     }
     cp_async_wait_all();
   }
