@@ -23,10 +23,14 @@ item):
   Hessian accumulator H += X^T X over a window of tokens, packed upper.
 * ``cortiq-cli src/gptq.rs``, ``act_order_perm`` / ``permute_sym`` /
   ``gptq_quantize_q4tp_act_order``: act-order with static groups.
+* ``cortiq-engine src/gpu_wgpu/gptq_dev.rs``, WGSL ``q2_level`` /
+  ``q2tp_group``, and ``cortiq-cli src/gptq.rs``, ``gptq_quantize_q2tp`` with
+  ``Q2tpRule::Placed``: the 2-bit "placed" rule (ladder placement, full rung
+  search, the lazy-block host sweep).
 
 Readings of points the pages leave open are stated where they are used
 (``ladder`` for the missing converter ladder, ``nominal_rung`` for the f32
-log2).
+log2, the ``q2tp`` module docstring for the placed ladder).
 
 Every function is pinned by ``tests/test_oracle_*.py`` (closed forms,
 hand-computed cases, invariants, brute force); none is "parity unpinned".
@@ -55,4 +59,14 @@ from .actorder import (  # noqa: F401,E402
     permute_packed,
     sweep_q4tp_act_order,
     total_cmp_key,
+)
+from .q2tp import (  # noqa: F401,E402
+    q2_level,
+    place_scale,
+    ladder_q2tp,
+    group_q2tp,
+    sweep_q2tp,
+    sweep_q2tp_f64,
+    dequant_q2tp,
+    plane_to_codes,
 )
