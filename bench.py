@@ -1,12 +1,15 @@
 """Benchmark: seconds per GPTQ group (fold + q4tp sweep) at n = 17408.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--codec q4tp|q2tp]
 
 One step = one full pass of the hot path on one synthetic Hessian group
 already resident in HBM: fold (builder, Cholesky, inverse, U), dead-column
 zeroing, ladder, q4tp sweep, through the C ABI (gptq_quantize_group).  With
 N > 1 (torchrun) every rank folds and quantizes its own group (independent
-problems, no collective on the data path): weak scaling.
+problems, no collective on the data path): weak scaling.  ``--codec q2tp``
+times the same step with the q2tp "placed" rule instead (placed ladder,
+31-rung search, 2-bit codes: gptq_quantize_group_q2tp), under its own metric.
 
 ``--impl reference`` times the CPU oracle (the plain f64/f32 restatement of
 the pages) on the host cores, on a bounded sample of the same workload
@@ -28,6 +31,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "s per GPTQ group (fold+q4tp) at n=17408"
+METRIC_Q2 = "s per GPTQ group (fold+q2tp placed) at n=17408"
 UNIT = "s/group"
 
 # Peaks for the roofline denominators when the driver's measured file is absent.
@@ -50,11 +54,11 @@ def peaks():
     return dict(FALLBACK), "fallback"
 
 
-def workload_desc(cfg):
+def workload_desc(cfg, codec="q4tp"):
     return (f"{cfg.name}: one Hessian group, n={cfg.n} channels, W [{cfg.rows}, {cfg.n}] f32 "
             f"N(0, {cfg.w_std}^2); H = X X^T / T, X [{cfg.n}, {cfg.T}] N(0,1) with lognormal(0, {cfg.sigma}) "
             f"channel scales, {cfg.n_outlier} outlier channels x100, {cfg.n_dead} dead; "
-            f"lambda={cfg.lam}, group 32, q4tp")
+            f"lambda={cfg.lam}, group 32, " + ("q4tp" if codec == "q4tp" else "q2tp placed rule"))
 
 
 def fold_gemm_flops(n, NB=128):
@@ -153,12 +157,12 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def cpu_baseline_sample(cfg, n_fold=None, rows_sweep=8):
+def cpu_baseline_sample(cfg, n_fold=None, rows_sweep=8, codec="q4tp"):
     """Oracle on a bounded sample, scaled to seconds per full group:
     the fold on the leading n_fold x n_fold block of the group's H (cost
-    scaled by (n / n_fold)^3) and the q4tp sweep of `rows_sweep` rows at full
-    n against that block's operator padded with the identity (cost scaled by
-    rows / rows_sweep)."""
+    scaled by (n / n_fold)^3) and the sweep (ladder included) of `rows_sweep`
+    rows at full n against that block's operator padded with the identity
+    (cost scaled by rows / rows_sweep)."""
     import numpy as np
     import torch
 
@@ -180,13 +184,17 @@ def cpu_baseline_sample(cfg, n_fold=None, rows_sweep=8):
     big = np.eye(cfg.n, dtype=np.float32)
     big[:n_fold, :n_fold] = u.astype(np.float32)
     hw = np.ones(cfg.n, dtype=np.float32)
-    tab, lost = oracle.ladder(w)
     t0 = time.perf_counter()
-    oracle.sweep_q4tp(w, big, hw, tab, lost)
+    if codec == "q4tp":
+        tab, lost = oracle.ladder(w)
+        oracle.sweep_q4tp(w, big, hw, tab, lost)
+    else:
+        tab, lost, _ = oracle.ladder_q2tp(w, hw)
+        oracle.sweep_q2tp(w, big, hw, tab)
     t_sweep = time.perf_counter() - t0
     est = t_fold * (cfg.n / n_fold) ** 3 + t_sweep * (cfg.rows / rows_sweep)
-    sample = (f"oracle fold at n={n_fold} ({t_fold:.2f} s, x(n/{n_fold})^3) + oracle q4tp sweep of "
-              f"{rows_sweep} rows at n={cfg.n} ({t_sweep:.2f} s, x{cfg.rows}/{rows_sweep})")
+    sample = (f"oracle fold at n={n_fold} ({t_fold:.2f} s, x(n/{n_fold})^3) + oracle {codec} ladder and "
+              f"sweep of {rows_sweep} rows at n={cfg.n} ({t_sweep:.2f} s, x{cfg.rows}/{rows_sweep})")
     return est, sample, t_fold + t_sweep
 
 
@@ -197,14 +205,16 @@ def run_reference(args, cfg, rank):
     vals = []
     sample = ""
     for i in range(args.warmup + args.steps):
-        est, sample, spent = cpu_baseline_sample(cfg, n_fold=args.ref_n, rows_sweep=args.ref_rows)
+        est, sample, spent = cpu_baseline_sample(cfg, n_fold=args.ref_n, rows_sweep=args.ref_rows,
+                                                 codec=args.codec)
         if i >= args.warmup:
             vals.append(est)
     v = statistics.median(vals)
-    line = {"metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
+    line = {"metric": METRIC if args.codec == "q4tp" else METRIC_Q2, "value": v, "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": v * 1e3, "higher_is_better": False, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
-            "config": {"workload": workload_desc(cfg)},
+            "config": {"workload": workload_desc(cfg, args.codec)},
             "cpu_baseline": {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
             "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -358,6 +368,7 @@ def main():
     ap.add_argument("--n", type=int, default=None, help="override n (T = 2n) for small profiling cases")
     ap.add_argument("--rows", type=int, default=None)
     ap.add_argument("--streams", type=int, default=2, help="host threads / streams for --config batch")
+    ap.add_argument("--codec", choices=["q4tp", "q2tp"], default="q4tp")
     args = ap.parse_args()
 
     import synth
@@ -401,13 +412,15 @@ def main():
     n, rows = cfg.n, cfg.rows
     gpr = n // 32
     ws = _lib.workspace(lib.gptq_group_workspace_bytes(rows, n), dev)
-    outs = (torch.empty(rows * n // 2, dtype=torch.uint8, device=dev),
+    q2 = args.codec == "q2tp"
+    quantize = _lib.quantize_group_q2tp if q2 else _lib.quantize_group
+    outs = (torch.empty(rows * n // (4 if q2 else 2), dtype=torch.uint8, device=dev),
             torch.empty(rows * gpr, dtype=torch.uint8, device=dev),
             torch.empty(rows * gpr, dtype=torch.float32, device=dev))
     stream = torch.cuda.current_stream(dev)
 
     def step():
-        return _lib.quantize_group(hp, n, w, cfg.lam, ws=ws, want_u=False, stream=stream, out=outs)
+        return quantize(hp, n, w, cfg.lam, ws=ws, want_u=False, stream=stream, out=outs)
 
     res = None
     for _ in range(max(args.warmup, 0)):
@@ -486,7 +499,7 @@ def main():
                     upload(j + 1)
                 hp_d, w_d, o_d = sets[j % 2]
                 stream.wait_event(ready[j % 2])
-                _lib.quantize_group(hp_d, n, w_d, cfg.lam, ws=ws, want_u=False, stream=stream, out=o_d)
+                quantize(hp_d, n, w_d, cfg.lam, ws=ws, want_u=False, stream=stream, out=o_d)
                 copy.wait_stream(stream)
                 with torch.cuda.stream(copy):
                     for o_h, o in zip(outs_h[j % 2], o_d):
@@ -532,15 +545,17 @@ def main():
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        est, sample, spent = cpu_baseline_sample(cfg, n_fold=args.ref_n, rows_sweep=args.ref_rows)
+        est, sample, spent = cpu_baseline_sample(cfg, n_fold=args.ref_n, rows_sweep=args.ref_rows,
+                                                 codec=args.codec)
         cpu = {"value": est, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle", "sample": sample}
 
     if rank == 0:
         line = {
-            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "metric": METRIC_Q2 if q2 else METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": t_dev / args.steps * 1e3, "higher_is_better": False,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": workload_desc(cfg), "n": n, "rows": rows, "lambda_used": lam_used,
+            "config": {"workload": workload_desc(cfg, args.codec), "n": n, "rows": rows, "lambda_used": lam_used,
                        "l2": "inputs larger than L2 (H_packed %.0f MB, W %.0f MB, U %.0f MB); no flush"
                              % (hp.numel() * 4 / 1e6, w.numel() * 4 / 1e6, n * n * 4 / 1e6),
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},

@@ -37,6 +37,10 @@ SIGNATURES = {
     "gptq_q4tp_sweep_act_order": (_I, [_P, _I, _I, _P, _P, _P, _P, _P, _P, _S, _P]),
     "gptq_group_act_order_workspace_bytes": (_S, [_I, _I]),
     "gptq_quantize_group_act_order": (_I, [_P, _I, _D, _P, _I, _P, _P, _P, _P, _P, _P, _P, _S, _P]),
+    "gptq_q2tp_place": (_I, [_P, _I, _I, _P, _P, _P, _P, _P]),
+    "gptq_q2tp_group": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "gptq_q2tp_sweep": (_I, [_P, _I, _I, _P, _P, _P, _P, _P, _P, _P, _S, _P]),
+    "gptq_quantize_group_q2tp": (_I, [_P, _I, _D, _P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _S, _P]),
     "gptq_gram_workspace_bytes": (_S, [_I]),
     "gptq_gram_add": (_I, [_P, _I, _P, _I, _P, _S, _P]),
     "gptq_launch_count": (ctypes.c_longlong, []),
@@ -356,3 +360,93 @@ def quantize_group_act_order(h_packed, n, w, lam=0.01, ws=None, want_u=True, str
                                              _stream(torch, stream))
     _check("gptq_quantize_group_act_order", code)
     return dict(nibbles=nib, rungs=rungs, scales=scales, perm=perm, u=u, lam=lam_used.value)
+
+
+# ------------------------------------------------------------------ q2tp
+
+
+def q2tp_place(w, hw, want_gscale=False):
+    """Placed q2tp ladder of the (dead-zeroed) W: (tab [rows, 32], lost
+    [rows, 2], gscale [rows, n/32] or None)."""
+    import torch
+
+    lib = load()
+    _cuda_f32(w, "w")
+    _cuda_f32(hw, "hw")
+    rows, n = w.shape
+    tab = torch.empty(rows, 32, dtype=torch.float32, device=w.device)
+    lost = torch.empty(rows, 2, dtype=torch.float32, device=w.device)
+    gs = torch.empty(rows, n // 32, dtype=torch.float32, device=w.device) if want_gscale else None
+    _check("gptq_q2tp_place", lib.gptq_q2tp_place(_ptr(w), rows, n, _ptr(hw), _ptr(tab), _ptr(lost),
+                                                  _ptr(gs), _stream(torch)))
+    return tab, lost, gs
+
+
+def q2tp_group(tile, ublk, hw, tab):
+    """The q2tp group rule on given tiles: (codes [rows, 8] u8, rungs, scales, E)."""
+    import torch
+
+    lib = load()
+    rows = tile.shape[0]
+    dev = tile.device
+    codes = torch.empty(rows, 8, dtype=torch.uint8, device=dev)
+    rungs = torch.empty(rows, dtype=torch.uint8, device=dev)
+    scales = torch.empty(rows, dtype=torch.float32, device=dev)
+    e = torch.empty(rows, 32, dtype=torch.float32, device=dev)
+    code = lib.gptq_q2tp_group(_ptr(tile), rows, _ptr(ublk), _ptr(hw), _ptr(tab), _ptr(codes),
+                               _ptr(rungs), _ptr(scales), _ptr(e), _stream(torch))
+    _check("gptq_q2tp_group", code)
+    return codes, rungs, scales, e
+
+
+def _outs_q2(torch, rows, n, dev):
+    gpr = n // 32
+    codes = torch.empty(rows * n // 4, dtype=torch.uint8, device=dev)
+    rungs = torch.empty(rows * gpr, dtype=torch.uint8, device=dev)
+    scales = torch.empty(rows * gpr, dtype=torch.float32, device=dev)
+    return codes, rungs, scales
+
+
+def q2tp_sweep(w, u, hw, tab, ws=None, out=None, stream=None):
+    """q2tp sweep of W (consumed in place).  Returns (codes, rungs, scales)."""
+    import torch
+
+    lib = load()
+    for t, nm in ((w, "w"), (u, "u"), (hw, "hw"), (tab, "tab")):
+        _cuda_f32(t, nm)
+    rows, n = w.shape
+    codes, rungs, scales = out if out is not None else _outs_q2(torch, rows, n, w.device)
+    if ws is None:
+        ws = workspace(lib.gptq_sweep_workspace_bytes(rows, n), w.device)
+    code = lib.gptq_q2tp_sweep(_ptr(w), rows, n, _ptr(u), _ptr(hw), _ptr(tab), _ptr(codes),
+                               _ptr(rungs), _ptr(scales), _ptr(ws), ws.numel(), _stream(torch, stream))
+    _check("gptq_q2tp_sweep", code)
+    return codes, rungs, scales
+
+
+def quantize_group_q2tp(h_packed, n, w, lam=0.01, ws=None, want_u=True, stream=None, out=None):
+    """Fold + placed ladder + q2tp sweep.  Returns dict(codes, rungs, scales,
+    tab, lost, u, d, hdiag, lam)."""
+    import torch
+
+    lib = load()
+    _cuda_f32(h_packed, "h_packed")
+    _cuda_f32(w, "w")
+    rows = w.shape[0]
+    dev = w.device
+    codes, rungs, scales = out if out is not None else _outs_q2(torch, rows, n, dev)
+    tab = torch.empty(rows, 32, dtype=torch.float32, device=dev)
+    lost = torch.empty(rows, 2, dtype=torch.float32, device=dev)
+    u = torch.empty(n, n, dtype=torch.float32, device=dev) if want_u else None
+    d = torch.empty(n, dtype=torch.float32, device=dev)
+    hd = torch.empty(n, dtype=torch.float32, device=dev)
+    if ws is None:
+        ws = workspace(lib.gptq_group_workspace_bytes(rows, n), dev)
+    lam_used = ctypes.c_double(0.0)
+    code = lib.gptq_quantize_group_q2tp(_ptr(h_packed), n, float(lam), _ptr(w), rows, _ptr(codes),
+                                        _ptr(rungs), _ptr(scales), _ptr(tab), _ptr(lost), _ptr(u),
+                                        _ptr(d), _ptr(hd), ctypes.byref(lam_used), _ptr(ws),
+                                        ws.numel(), _stream(torch, stream))
+    _check("gptq_quantize_group_q2tp", code)
+    return dict(codes=codes, rungs=rungs, scales=scales, tab=tab, lost=lost, u=u, d=d, hdiag=hd,
+                lam=lam_used.value)

@@ -31,6 +31,14 @@ gptq_status sweep_run(float* W, int rows, int n, const float* U, const float* hw
                       const float* lost, uint8_t* nib, uint8_t* rungs, float* scales, void* ws,
                       size_t ws_bytes, cudaStream_t s);
 gptq_status noalloc_scratch(void** out);
+gptq_status place_q2_run(const float* W, int rows, int n, const float* hw, float* tab, float* lost,
+                         float* gscale, cudaStream_t s);
+gptq_status group_q2_run(const float* tile, int rows, const float* ublk, const float* hw,
+                         const float* tab, uint8_t* codes, uint8_t* rungs, float* scales, float* E,
+                         cudaStream_t s);
+gptq_status sweep_q2_run(float* W, int rows, int n, const float* U, const float* hw,
+                         const float* tab, uint8_t* codes, uint8_t* rungs, float* scales, void* ws,
+                         size_t ws_bytes, cudaStream_t s);
 size_t gram_ws_bytes(int n);
 gptq_status gram_run(float* Hp, int n, const float* X, int T, void* ws, size_t ws_bytes,
                      cudaStream_t s);
@@ -168,6 +176,65 @@ gptq_status gptq_quantize_group(const float* H_packed, int n, double lambda, con
   GQ_TRY(copy_dead_zeroed(W, rows, n, hd, wz, s));
   GQ_TRY(ladder_run(wz, rows, n, tb, ls, s));
   return sweep_run(wz, rows, n, u, hd, tb, ls, nibbles, rungs, scales, rest, rest_bytes, s);
+}
+
+gptq_status gptq_q2tp_place(const float* W, int rows, int n, const float* hw, float* tab,
+                            float* lost, float* gscale, void* stream) {
+  if (bad_n(n) || bad_rows(rows) || n % GPTQ_GROUP != 0) return GPTQ_ERR_SHAPE;
+  if (!ptr_ok(W) || !ptr_ok(hw) || !ptr_ok(tab) || !ptr_ok(lost) || !opt_ok(gscale))
+    return GPTQ_ERR_ARG;
+  return place_q2_run(W, rows, n, hw, tab, lost, gscale, as_stream(stream));
+}
+
+gptq_status gptq_q2tp_group(const float* tile, int rows, const float* ublk, const float* hw,
+                            const float* tab, uint8_t* codes, uint8_t* rungs, float* scales,
+                            float* E, void* stream) {
+  if (bad_rows(rows)) return GPTQ_ERR_SHAPE;
+  if (!ptr_ok(tile) || !ptr_ok(ublk) || !ptr_ok(hw) || !ptr_ok(tab) || !ptr_ok(codes) ||
+      rungs == nullptr || !ptr_ok(scales) || !ptr_ok(E))
+    return GPTQ_ERR_ARG;
+  return group_q2_run(tile, rows, ublk, hw, tab, codes, rungs, scales, E, as_stream(stream));
+}
+
+gptq_status gptq_q2tp_sweep(float* W, int rows, int n, const float* U, const float* hw,
+                            const float* tab, uint8_t* codes, uint8_t* rungs, float* scales,
+                            void* ws, size_t ws_bytes, void* stream) {
+  if (bad_n(n) || bad_rows(rows) || n % GPTQ_GROUP != 0) return GPTQ_ERR_SHAPE;
+  if (!ptr_ok(W) || !ptr_ok(U) || !ptr_ok(hw) || !ptr_ok(tab) || !ptr_ok(codes) ||
+      rungs == nullptr || !ptr_ok(scales) || ws == nullptr)
+    return GPTQ_ERR_ARG;
+  if (ws_bytes < sweep_ws_bytes(rows, n)) return GPTQ_ERR_NOMEM;
+  return sweep_q2_run(W, rows, n, U, hw, tab, codes, rungs, scales, ws, ws_bytes,
+                      as_stream(stream));
+}
+
+gptq_status gptq_quantize_group_q2tp(const float* H_packed, int n, double lambda, const float* W,
+                                     int rows, uint8_t* codes, uint8_t* rungs, float* scales,
+                                     float* tab, float* lost, float* U, float* D, float* hdiag,
+                                     double* lambda_used, void* ws, size_t ws_bytes, void* stream) {
+  if (bad_n(n) || bad_rows(rows) || n % GPTQ_GROUP != 0) return GPTQ_ERR_SHAPE;
+  if (!ptr_ok(H_packed) || !ptr_ok(W) || !ptr_ok(codes) || rungs == nullptr || !ptr_ok(scales) ||
+      !opt_ok(tab) || !opt_ok(lost) || !opt_ok(U) || !opt_ok(D) || !opt_ok(hdiag) || ws == nullptr)
+    return GPTQ_ERR_ARG;
+  if (!isfinite(lambda)) return GPTQ_ERR_ARG;
+  if (ws_bytes < gptq_group_workspace_bytes(rows, n)) return GPTQ_ERR_NOMEM;
+  cudaStream_t s = as_stream(stream);
+  Carve c(ws, ws_bytes);
+  float* u = U ? U : c.take<float>((size_t)n * n);
+  float* d = D ? D : c.take<float>((size_t)n);
+  float* hd = hdiag ? hdiag : c.take<float>((size_t)n);
+  float* wz = c.take<float>((size_t)rows * n);
+  float* tb = tab ? tab : c.take<float>((size_t)rows * 32);
+  float* ls = lost ? lost : c.take<float>((size_t)rows * 2);
+  c.take<float>((size_t)n);
+  if (!c.ok) return GPTQ_ERR_NOMEM;
+  const size_t off = round_up(c.off, 256);
+  void* rest = static_cast<char*>(ws) + off;
+  const size_t rest_bytes = ws_bytes - off;
+  GQ_TRY(fold_run(H_packed, n, lambda, u, d, hd, lambda_used, rest, rest_bytes, s));
+  GQ_TRY(copy_dead_zeroed(W, rows, n, hd, wz, s));
+  GQ_TRY(place_q2_run(wz, rows, n, hd, tb, ls, nullptr, s));
+  return sweep_q2_run(wz, rows, n, u, hd, tb, codes, rungs, scales, rest, rest_bytes, s);
 }
 
 size_t gptq_gram_workspace_bytes(int n) { return bad_n(n) ? 0 : gram_ws_bytes(n); }

@@ -38,7 +38,7 @@ constexpr int GROUP = 32;
 // Kernel kinds for launch accounting / per-kind timing (gptq_profile_*).
 enum Kind : int {
   K_DIAG = 0, K_BUILD, K_POTRF, K_TRSM, K_FOLD_GEMM, K_LADDER, K_SWEEP_BLOCK, K_PREP_UT,
-  K_SWEEP_GEMM, K_GROUP, K_COPY, K_GRAM_PREP, K_GRAM_GEMM, K_NKINDS
+  K_SWEEP_GEMM, K_GROUP, K_COPY, K_GRAM_PREP, K_GRAM_GEMM, K_PLACE, K_NKINDS
 };
 
 // Every launch site calls prof_begin/prof_end around its <<<>>>: they count
@@ -185,6 +185,12 @@ __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
 __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
 }
+
+// q2tp level code clamp(round_half_even(clamp(x, -1, 4)), 0, 3) ([fold page]
+// WGSL q2_level).  The inner clamp changes no result (rint of anything below
+// -1 is <= -1, of anything above 4 is >= 4, and CUDA's fmaxf maps a NaN to 0
+// either way), so it is left out.
+__device__ __forceinline__ float q2_code(float x) { return fminf(fmaxf(rintf(x), 0.f), 3.f); }
 
 __device__ __forceinline__ void split_tf32(float x, float& hi, float& lo) {
   hi = tf32_rna(x);

@@ -13,6 +13,10 @@
 // this is the fold page's per-group q4tp_trail; the wider blocks are the
 // same mathematics with the residual sums taken in a different order.
 //
+// The same pipeline runs the q2tp "placed" rule ([fold page] WGSL q2_level /
+// q2tp_group; [host page] gptq_quantize_q2tp_dev): a full rung search and
+// 2-bit codes in the block kernel, everything else unchanged.
+//
 // The per-group rule uses one rounding per operation (no contraction) so it
 // reproduces the pages' f32 arithmetic bit for bit.
 #include "common.cuh"
@@ -246,17 +250,29 @@ constexpr int SWEEP_SMEM = (SB * SB + SB + SWEEP_ROWS * LW + SWEEP_ROWS * ESR) *
 //  * the group's residuals go to E (TF32 hi/lo, the trailing GEMM's
 //    operand) and into the block's later columns (w_c -= sum_j e_j U_jc),
 //    lane k taking the 4-column chunks 4k, 4k+16, ... .
-// ACT (act order): W and U are in permuted channel order, the rungs are
-// given (static, per original group) and each column takes the scale of its
-// original group; codes go to `codes` (int8, permuted order) instead of the
-// nibble plane.
-template <bool ACT>
+// MODE_Q4_ACT (act order): W and U are in permuted channel order, the rungs
+// are given (static, per original group) and each column takes the scale of
+// its original group; codes go to `codes` (int8, permuted order) instead of
+// the nibble plane.
+// MODE_Q2 (the q2tp "placed" rule, [fold page] WGSL q2_level / q2tp_group):
+// rungs 1..31 searched in full (lane k of the quad takes rungs 1+k, 5+k, ...;
+// each lane keeps its lowest best rung, the quad then takes the lowest rung
+// of the smallest error, which is the one-thread ascending strict-'<' scan
+// from (3.4e38, rung 1)); an all-zero tile takes rung 0; codes
+// q2_level(w/s + 1.5) into the 2-bit plane (8 bytes a tile); residual
+// (w - (q - 1.5) s) / U_jj; rung weights H_ii clipped at 0.
+enum SweepMode : int { MODE_Q4 = 0, MODE_Q4_ACT = 1, MODE_Q2 = 2 };
+
+template <int MODE>
 __global__ void __launch_bounds__(SWEEP_THREADS) k_sweep_block(
     const float* __restrict__ W, int rows, int n, int b0, int B, const float* __restrict__ U,
     const float* __restrict__ hw, const float* __restrict__ tab, const float* __restrict__ lost,
     uint8_t* __restrict__ nib, uint8_t* __restrict__ rungs, float* __restrict__ scales,
     float* __restrict__ E_hi, float* __restrict__ E_lo, int ecol0, const int* __restrict__ perm,
     int8_t* __restrict__ codes) {
+  constexpr bool ACT = MODE == MODE_Q4_ACT;
+  constexpr bool Q2 = MODE == MODE_Q2;
+  constexpr int NWORDS = ACT ? GROUP / 4 : (Q2 ? GROUP / 16 : GROUP / 8);
   extern __shared__ __align__(16) float sm[];
   float* Us = sm;             // [SB][SB]
   float* hws = Us + SB * SB;  // [SB]
@@ -282,7 +298,10 @@ __global__ void __launch_bounds__(SWEEP_THREADS) k_sweep_block(
     }
     cp_async_wait_all();
   }
-  for (int e = tid; e < B; e += SWEEP_THREADS) hws[e] = ACT ? 0.f : hw[b0 + e];
+  for (int e = tid; e < B; e += SWEEP_THREADS) {
+    const float h = ACT ? 0.f : hw[b0 + e];
+    hws[e] = Q2 ? (h > 0.f ? h : 0.f) : h;
+  }
   __syncthreads();
   const int sub = lane & 3, qbase = lane & ~3;
   const int rl = warp * 8 + (lane >> 2);
@@ -294,7 +313,7 @@ __global__ void __launch_bounds__(SWEEP_THREADS) k_sweep_block(
   float* wrow = Ws + rl * LW;
   float* es = Es + rl * ESR;
   float lo = 0.f, st = 0.f;
-  if (!ACT) {
+  if (MODE == MODE_Q4) {
     lo = lost[2 * rs];
     st = lost[2 * rs + 1];
   }
@@ -315,6 +334,47 @@ __global__ void __launch_bounds__(SWEEP_THREADS) k_sweep_block(
     if (ACT) {
 #pragma unroll
       for (int t = 0; t < GROUP; ++t) sc[t] = tabrow[rungs[(long long)rs * gpr + perm[b0 + gc + t] / GROUP]];
+    } else if (Q2) {
+      float amax = 0.f;
+#pragma unroll
+      for (int t = 0; t < GROUP; ++t) amax = fmaxf(amax, fabsf(w[t]));
+      const bool any = amax > 0.f;
+      float be = 3.4e38f;
+      int bc = 64;  // none below 3.4e38 yet
+      if (any) {
+        const float* hg = hws + gc;
+#pragma unroll 1
+        for (int k = 0; k < 8; ++k) {
+          const int cand = 1 + sub + 4 * k;
+          if (cand > 31) break;
+          const float sck = tabrow[cand];
+          if (!(sck > 0.f)) continue;
+          const float iv = __fdiv_rn(1.0f, sck);
+          float err = 0.f;
+#pragma unroll
+          for (int t = 0; t < GROUP; ++t) {
+            const float q = q2_code(__fadd_rn(__fmul_rn(w[t], iv), 1.5f));
+            const float d = __fsub_rn(w[t], __fmul_rn(__fsub_rn(q, 1.5f), sck));
+            err = __fadd_rn(err, __fmul_rn(__fmul_rn(hg[t], d), d));
+          }
+          if (err < be) {
+            be = err;
+            bc = cand;
+          }
+        }
+      }
+      // Every lane reaches the exchange (rows differ in amax).
+#pragma unroll
+      for (int o = 1; o < 4; o <<= 1) {
+        const float oe = __shfl_xor_sync(0xffffffffu, be, o);
+        const int oc = __shfl_xor_sync(0xffffffffu, bc, o);
+        if (oe < be || (oe == be && oc < bc)) {
+          be = oe;
+          bc = oc;
+        }
+      }
+      best_c = any ? (bc < 32 ? bc : 1) : 0;
+      s = tabrow[best_c];
     } else {
       // Rung rule, one candidate per lane.
       float amax = 0.f;
@@ -356,9 +416,9 @@ __global__ void __launch_bounds__(SWEEP_THREADS) k_sweep_block(
     }
     // Rounding with in-group feedback (software-pipelined, see above).
     const float* Ug = Us + gc * SB + gc;
-    uint32_t words[ACT ? GROUP / 4 : GROUP / 8];
+    uint32_t words[NWORDS];
 #pragma unroll
-    for (int i = 0; i < (ACT ? GROUP / 4 : GROUP / 8); ++i) words[i] = 0u;
+    for (int i = 0; i < NWORDS; ++i) words[i] = 0u;
     float eprev = 0.f;
 #pragma unroll
     for (int j = 0; j < GROUP; ++j) {
@@ -369,13 +429,22 @@ __global__ void __launch_bounds__(SWEEP_THREADS) k_sweep_block(
 #pragma unroll
         for (int t = j + 1; t < GROUP; ++t) w[t] = __fsub_rn(w[t], __fmul_rn(eprev, Ug[(j - 1) * SB + t]));
       }
-      const float q = sj > 0.f ? fminf(fmaxf(rintf(t1), -8.f), 7.f) : 0.f;
+      float q, lev;
+      if (Q2) {
+        q = sj > 0.f ? q2_code(__fadd_rn(t1, 1.5f)) : 0.f;
+        lev = __fsub_rn(q, 1.5f);
+      } else {
+        q = sj > 0.f ? fminf(fmaxf(rintf(t1), -8.f), 7.f) : 0.f;
+        lev = q;
+      }
       const float dj = Ug[j * SB + j];
       float ej = 0.f;
-      if (dj > 0.f) ej = __fdiv_rn(__fsub_rn(x, __fmul_rn(q, sj)), dj);
+      if (dj > 0.f) ej = __fdiv_rn(__fsub_rn(x, __fmul_rn(lev, sj)), dj);
       es[j] = ej;  // the same value from the four lanes
       if (ACT)
         words[j / 4] |= ((uint32_t)(int)q & 255u) << (8 * (j % 4));
+      else if (Q2)
+        words[j / 16] |= (uint32_t)q << (2 * (j % 16));
       else
         words[j / 8] |= ((uint32_t)((int)q + 8) & 15u) << (4 * (j % 8));
       if (j + 1 < GROUP) w[j + 1] = __fsub_rn(w[j + 1], __fmul_rn(ej, Ug[j * SB + j + 1]));
@@ -401,7 +470,10 @@ __global__ void __launch_bounds__(SWEEP_THREADS) k_sweep_block(
                 make_uint2(words[2 * c], words[2 * c + 1]);
       } else if (sub == 0) {
         const long long tix = (long long)r * gpr + b0 / GROUP + g;
-        reinterpret_cast<uint4*>(nib)[tix] = make_uint4(words[0], words[1], words[2], words[3]);
+        if constexpr (Q2)
+          reinterpret_cast<uint2*>(nib)[tix] = make_uint2(words[0], words[1]);
+        else
+          reinterpret_cast<uint4*>(nib)[tix] = make_uint4(words[0], words[1], words[2], words[3]);
         rungs[tix] = (uint8_t)best_c;
         scales[tix] = s;
       }
@@ -493,9 +565,11 @@ size_t sweep_ws_bytes(int rows, int n) {
 static gptq_status sweep_attrs() {
   static bool done = false;
   if (done) return GPTQ_OK;
-  GQ_CUDA(cudaFuncSetAttribute(k_sweep_block<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  GQ_CUDA(cudaFuncSetAttribute(k_sweep_block<MODE_Q4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                SWEEP_SMEM));
-  GQ_CUDA(cudaFuncSetAttribute(k_sweep_block<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  GQ_CUDA(cudaFuncSetAttribute(k_sweep_block<MODE_Q4_ACT>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, SWEEP_SMEM));
+  GQ_CUDA(cudaFuncSetAttribute(k_sweep_block<MODE_Q2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                SWEEP_SMEM));
   done = true;
   return GPTQ_OK;
@@ -552,7 +626,7 @@ gptq_status noalloc_scratch(void** out) {
   return GPTQ_OK;
 }
 
-static gptq_status sweep_core(float* W, int rows, int n, const float* U, const float* hw,
+static gptq_status sweep_core(int mode, float* W, int rows, int n, const float* U, const float* hw,
                               const float* tab, const float* lost, uint8_t* nib, uint8_t* rungs,
                               float* scales, void* ws, size_t ws_bytes, cudaStream_t s,
                               const int* perm, int8_t* codes) {
@@ -576,14 +650,17 @@ static gptq_status sweep_core(float* W, int rows, int n, const float* U, const f
   const int grid_rows = (rows + SWEEP_ROWS - 1) / SWEEP_ROWS;
   auto block = [&](int b0, int B, int ecol0) -> gptq_status {
     GQ_PROF(K_SWEEP_BLOCK, s);
-    if (perm)
-      k_sweep_block<true><<<grid_rows, SWEEP_THREADS, smem, s>>>(W, rows, n, b0, B, U, hw, tab, lost,
-                                                                 nib, rungs, scales, E_hi, E_lo, ecol0,
-                                                                 perm, codes);
+    if (mode == MODE_Q4_ACT)
+      k_sweep_block<MODE_Q4_ACT><<<grid_rows, SWEEP_THREADS, smem, s>>>(
+          W, rows, n, b0, B, U, hw, tab, lost, nib, rungs, scales, E_hi, E_lo, ecol0, perm, codes);
+    else if (mode == MODE_Q2)
+      k_sweep_block<MODE_Q2><<<grid_rows, SWEEP_THREADS, smem, s>>>(
+          W, rows, n, b0, B, U, hw, tab, lost, nib, rungs, scales, E_hi, E_lo, ecol0, nullptr,
+          nullptr);
     else
-      k_sweep_block<false><<<grid_rows, SWEEP_THREADS, smem, s>>>(W, rows, n, b0, B, U, hw, tab, lost,
-                                                                  nib, rungs, scales, E_hi, E_lo,
-                                                                  ecol0, nullptr, nullptr);
+      k_sweep_block<MODE_Q4><<<grid_rows, SWEEP_THREADS, smem, s>>>(
+          W, rows, n, b0, B, U, hw, tab, lost, nib, rungs, scales, E_hi, E_lo, ecol0, nullptr,
+          nullptr);
     GQ_LAUNCHED();
     return GPTQ_OK;
   };
@@ -629,8 +706,17 @@ static gptq_status sweep_core(float* W, int rows, int n, const float* U, const f
 gptq_status sweep_run(float* W, int rows, int n, const float* U, const float* hw, const float* tab,
                       const float* lost, uint8_t* nib, uint8_t* rungs, float* scales, void* ws,
                       size_t ws_bytes, cudaStream_t s) {
-  return sweep_core(W, rows, n, U, hw, tab, lost, nib, rungs, scales, ws, ws_bytes, s, nullptr,
-                    nullptr);
+  return sweep_core(MODE_Q4, W, rows, n, U, hw, tab, lost, nib, rungs, scales, ws, ws_bytes, s,
+                    nullptr, nullptr);
+}
+
+// The q2tp "placed" sweep: the same blocks and updates with the q2tp rule in
+// the block kernel; `codes` is the 2-bit plane (8 bytes a tile).
+gptq_status sweep_q2_run(float* W, int rows, int n, const float* U, const float* hw,
+                         const float* tab, uint8_t* codes, uint8_t* rungs, float* scales, void* ws,
+                         size_t ws_bytes, cudaStream_t s) {
+  return sweep_core(MODE_Q2, W, rows, n, U, hw, tab, nullptr, codes, rungs, scales, ws, ws_bytes, s,
+                    nullptr, nullptr);
 }
 
 namespace {
@@ -732,7 +818,8 @@ gptq_status sweep_act_run(const float* W, int rows, int n, const float* Up, cons
     k_invperm<<<(n + 255) / 256, 256, 0, s>>>(perm, n, inv);
     GQ_LAUNCHED();
   }
-  GQ_TRY(sweep_core(Wp, rows, n, Up, nullptr, tab, nullptr, nullptr, const_cast<uint8_t*>(srungs),
+  GQ_TRY(sweep_core(MODE_Q4_ACT, Wp, rows, n, Up, nullptr, tab, nullptr, nullptr,
+                    const_cast<uint8_t*>(srungs),
                     nullptr, static_cast<char*>(ws) + off, ws_bytes - off, s, perm, codes));
   const long long tot = (long long)rows * (n / GROUP);
   GQ_PROF(K_COPY, s);

@@ -1,5 +1,5 @@
 /*
- * gptq_fold.h -- C ABI of the GB300 GPTQ fold + q4tp sweep library
+ * gptq_fold.h -- C ABI of the GB300 GPTQ fold + q4tp / q2tp sweep library
  * (libgptqfold.so).
  *
  * What it computes is defined by two pages of the cortiq project:
@@ -173,7 +173,79 @@ gptq_status gptq_q4tp_sweep_noalloc(float* W, int rows, int n, const float* U, c
                                     const float* tab, const float* lost, uint8_t* nibbles,
                                     uint8_t* rungs, float* scales, void* stream);
 
-/* Workspace bytes gptq_quantize_group needs. */
+/*
+ * The q2tp "placed" rule: 2-bit codes on the levels (q - 1.5) * s, q in 0..3,
+ * with the per-(row, group) scale s from a per-row ladder of 31 rungs.
+ * [fold page] WGSL q2_level, q2tp_group, host fn sweep_q2tp; [host page]
+ * Q2tpRule::Placed, gptq_quantize_q2tp, gptq_quantize_q2tp_dev.
+ *
+ * gptq_q2tp_place -- the ladder ([host page] gptq_quantize_q2tp_dev: placed
+ * from the dead-zeroed weights; the placement function is not on the pages).
+ * Reading implemented: each group's scale s*_g is the exact minimiser over
+ * s > 0 of sum_t h_t (w_t - (q2_level(w_t/s + 1.5) - 1.5) s)^2 with h = hw
+ * clipped at 0 (found among the 33 stationary points of its quadratic
+ * pieces, winner recomputed in f64); groups with no channel where h > 0 and
+ * w != 0 are left out.  lo = f16(log2 min s*), step = f16(max(0, (log2 max
+ * s* - lo)/30)) (0 if min == max), tab[0] = 0, tab[c] = f32(2^(lo + (c-1)
+ * step)) for c = 1..31; a row with no group left gets zeros.
+ *
+ *   W      in  f32 rows*n (dead columns zeroed), n % 32 == 0.
+ *   hw     in  f32 n: H_ii (values that are not > 0 count as 0).
+ *   tab    out f32 rows*32;  lost out f32 rows*2 = (lo, step).
+ *   gscale out f32 rows*n/32 (may be NULL): s*_g, 0 for groups left out.
+ */
+gptq_status gptq_q2tp_place(const float* W, int rows, int n, const float* hw, float* tab,
+                            float* lost, float* gscale, void* stream);
+
+/*
+ * gptq_q2tp_group -- the q2tp rung + rounding + in-group feedback rule alone
+ * on one 32-column tile of every row ([fold page] WGSL q2tp_group):
+ * rung 0 for an all-zero tile, else the lowest of rungs 1..31 with the
+ * smallest hw-weighted error of q2_level(w (1/s) + 1.5) (rungs with s <= 0
+ * skipped; rung 1 if none scores below 3.4e38); per column q =
+ * q2_level(w_j / s + 1.5) (0 if s <= 0), e_j = (w_j - (q - 1.5) s)/U_jj (0 if
+ * U_jj <= 0), w_t -= e_j U_jt for t > j.  f32, one rounding per operation.
+ *
+ *   tile in f32 rows*32; ublk in f32 32*32; hw in f32 32 (clipped at 0);
+ *   tab in f32 rows*32.  codes out u8 rows*8 (the tile's 2-bit bytes, see
+ *   gptq_q2tp_sweep); rungs out u8 rows; scales out f32 rows; E out f32 rows*32.
+ */
+gptq_status gptq_q2tp_group(const float* tile, int rows, const float* ublk, const float* hw,
+                            const float* tab, uint8_t* codes, uint8_t* rungs, float* scales,
+                            float* E, void* stream);
+
+/*
+ * gptq_q2tp_sweep -- the column-sequential q2tp GPTQ sweep of W against U
+ * ([fold page] sweep_q2tp; [host page] gptq_quantize_q2tp, placed rule,
+ * natural column order), with the residuals applied per block of 128
+ * columns as in gptq_q4tp_sweep.
+ *
+ *   W     in/out f32 rows*n (dead columns zeroed); consumed.
+ *   U     in  f32 n*n from gptq_fold.  hw in f32 n: H_ii (clipped at 0).
+ *   tab   in  f32 rows*32 from gptq_q2tp_place.
+ *   codes out u8 rows*n/4: tile (row, group) = 8 bytes at (row*n/32 +
+ *         group)*8; column j -> byte j/4, bits 2*(j%4) (the same bytes as
+ *         two little-endian u32 words with bits 2*(j%16)).
+ *   rungs out u8 rows*n/32; scales out f32 rows*n/32 = tab[row][rung].
+ *   ws    >= gptq_sweep_workspace_bytes(rows, n).
+ */
+gptq_status gptq_q2tp_sweep(float* W, int rows, int n, const float* U, const float* hw,
+                            const float* tab, uint8_t* codes, uint8_t* rungs, float* scales,
+                            void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * gptq_quantize_group_q2tp -- fold + dead-column zeroing + placed ladder +
+ * q2tp sweep for one Hessian group ([host page] gptq_fold_dev then
+ * gptq_quantize_q2tp_dev).  Arguments as gptq_quantize_group, with the
+ * 2-bit plane `codes` (rows*n/4 bytes) in place of the nibbles;
+ * ws >= gptq_group_workspace_bytes(rows, n).
+ */
+gptq_status gptq_quantize_group_q2tp(const float* H_packed, int n, double lambda, const float* W,
+                                     int rows, uint8_t* codes, uint8_t* rungs, float* scales,
+                                     float* tab, float* lost, float* U, float* D, float* hdiag,
+                                     double* lambda_used, void* ws, size_t ws_bytes, void* stream);
+
+/* Workspace bytes gptq_quantize_group (and gptq_quantize_group_q2tp) needs. */
 size_t gptq_group_workspace_bytes(int rows, int n);
 
 /*

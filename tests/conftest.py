@@ -23,3 +23,20 @@ def lib():
     from gptq_post_weight_gb300 import _lib
 
     return _lib.load()
+
+
+@pytest.fixture(scope="session")
+def oracle_folds():
+    """oracle.fold(hp, n, lam), computed once per `key` for the whole session
+    (the f64 fold of a full-size group takes minutes on the host)."""
+    import oracle
+
+    cache = {}
+
+    def get(hp, n, lam, key):
+        k = (key, n, float(lam))
+        if k not in cache:
+            cache[k] = oracle.fold(hp, n, lam)
+        return cache[k]
+
+    return get

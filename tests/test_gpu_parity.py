@@ -254,7 +254,7 @@ def test_gptq_beats_rtn_on_device(lib):
 
 @pytest.mark.slow
 @pytest.mark.parametrize("name", ["n4096", "n17408"])
-def test_full_size_group(lib, name):
+def test_full_size_group(lib, name, oracle_folds):
     """The bench's workload: GPU inputs, full fold compared with the f64
     oracle, the sweep on sampled rows (rows are independent given U)."""
     from gptq_post_weight_gb300 import _lib
@@ -265,7 +265,7 @@ def test_full_size_group(lib, name):
     hp = np_(hpd)
     w = np_(wd)
     del hpd, wd
-    uo, do, dead, lamo = oracle.fold(hp, cfg.n, cfg.lam)
+    uo, do, dead, lamo = oracle_folds(hp, cfg.n, cfg.lam, key=(cfg.name, cfg.seed))
     assert out["lam"] == lamo
     assert rel_fro(np_(out["u"]), uo) <= 1e-4
     rng = np.random.default_rng(0)
