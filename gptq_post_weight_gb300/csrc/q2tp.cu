@@ -12,9 +12,10 @@
 // each kink concave, so the minimum is the stationary point of one piece,
 //   s_O = (0.5 sum_t h|w| + sum_O h|w|) / (0.25 sum_t h + 2 sum_O h),
 // for an outer set O = the k largest |w| (k = 0..32).  The kernel scores the
-// pieces in f32 and recomputes the winner's scale in f64; when the two best
-// f32 scores are within the f32 error of each other, both are scored again
-// in f64 (ties: the smaller scale).  A group takes part only if some
+// pieces in f32 with compensated sums; when a group's two best f32 scores
+// are within their f32 error of each other both are scored again in f64
+// (ties: the smaller scale), and the scales that set the row's ladder (its
+// extremes) are recomputed in f64.  A group takes part only if some
 // channel has h > 0 and w != 0.  The row's ladder: lo = f16(log2 min s*),
 // step = f16(max(0, (log2 max s* - lo) / 30)) (0 if min == max), rung 0 = 0,
 // rung c >= 1 = f32(2^(lo + (c-1) step)); no group taking part: all zero.
@@ -53,141 +54,249 @@ __device__ __forceinline__ void sort_desc(float (&a)[GROUP], float (&h)[GROUP]) 
   }
 }
 
-// f64 stationary scale of the outer set = the first k of the sorted group.
-__device__ double top_scale_f64(const float (&a)[GROUP], const float (&h)[GROUP], int k) {
-  double ta = 0.0, th = 0.0, oa = 0.0, oh = 0.0;
+// s + e == a + b exactly (Knuth's two-sum; no contraction, no reordering).
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+  s = __fadd_rn(a, b);
+  const float bp = __fsub_rn(s, a);
+  e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bp)), __fsub_rn(b, bp));
+}
+
+// (hi, lo) += x * y, the product's own rounding error kept (fmaf).
+__device__ __forceinline__ void acc_prod(float& hi, float& lo, float x, float y) {
+  const float p = __fmul_rn(x, y);
+  const float pe = fmaf(x, y, -p);
+  float e;
+  two_sum(hi, p, hi, e);
+  lo = __fadd_rn(lo, __fadd_rn(e, pe));
+}
+__device__ __forceinline__ void acc(float& hi, float& lo, float x) {
+  float e;
+  two_sum(hi, x, hi, e);
+  lo = __fadd_rn(lo, e);
+}
+
+// The f32 search of one group (a sorted descending, h with it): the piece
+// whose k largest weights sit on the outer levels has B_k = sum h|w| l =
+// 0.5 sum h|w| + sum_top-k h|w| and C_k = sum h l^2 = 0.25 sum h +
+// 2 sum_top-k h; its stationary point is s_k = B_k / C_k, where E = sum h w^2
+// - B_k s_k; it counts when it lies in its piece, a_(k+1) <= s_k <= a_(k).
+// The sums are compensated (two-sum, exact products), so B_k and C_k carry
+// about one rounding each and the f32 E of two pieces differ from their
+// exact difference by less than 1e-6 sum h w^2; the runner-up within 2e-6
+// of the best is a tie, left to f64.  thr1 / thr2 = the smallest outer
+// weight of the best / runner-up piece (+inf for no outer weight).
+struct PlaceSearch {
+  float s, thr1, thr2;
+  bool tie;
+};
+
+__device__ __forceinline__ PlaceSearch place_search(const float (&a)[GROUP], const float (&h)[GROUP]) {
+  float tah = 0.f, tal = 0.f, thh = 0.f, thl = 0.f, aa = 0.f;
 #pragma unroll
   for (int t = 0; t < GROUP; ++t) {
-    const double ht = h[t], ha = ht * (double)a[t];
-    ta += ha;
-    th += ht;
-    if (t < k) {
-      oa += ha;
-      oh += ht;
+    acc_prod(tah, tal, h[t], a[t]);
+    acc(thh, thl, h[t]);
+    aa += h[t] * a[t] * a[t];
+  }
+  float e1 = INFINITY, e2 = INFINITY, s1 = 0.f, thr1 = INFINITY, thr2 = INFINITY;
+  float pah = 0.f, pal = 0.f, phh = 0.f, phl = 0.f;
+#pragma unroll
+  for (int k = 0; k <= GROUP; ++k) {
+    float bs, be, cs, ce;
+    two_sum(0.5f * tah, pah, bs, be);
+    two_sum(0.25f * thh, 2.f * phh, cs, ce);
+    const float B = bs + (be + (0.5f * tal + pal));
+    const float C = cs + (ce + (0.25f * thl + 2.f * phl));
+    const float sc = B / C;
+    const float up = k == 0 ? INFINITY : a[k - 1];
+    const float dn = k == GROUP ? 0.f : a[k];
+    if (sc <= up && sc >= dn) {
+      const float e = aa - B * sc;
+      if (e < e1) {
+        if (sc != s1) {
+          e2 = e1;
+          thr2 = thr1;
+        }
+        e1 = e;
+        s1 = sc;
+        thr1 = up;
+      } else if (e < e2 && sc != s1) {
+        e2 = e;
+        thr2 = up;
+      }
+    }
+    if (k < GROUP) {
+      acc_prod(pah, pal, h[k], a[k]);
+      acc(phh, phl, h[k]);
     }
   }
+  PlaceSearch r;
+  r.s = s1;
+  r.thr1 = thr1;
+  r.thr2 = thr2;
+  r.tie = e2 - e1 <= 2e-6f * aa;
+  return r;
+}
+
+// Load group g (|w|, clipped h); false if it does not take part.
+__device__ __forceinline__ bool place_load(const float* wr, const float* hw, int g, float (&a)[GROUP],
+                                           float (&h)[GROUP]) {
+  bool part = false;
+#pragma unroll
+  for (int q = 0; q < GROUP / 4; ++q) {
+    const float4 v = reinterpret_cast<const float4*>(wr + g * GROUP)[q];
+    const float4 u = reinterpret_cast<const float4*>(hw + g * GROUP)[q];
+    a[4 * q] = fabsf(v.x); a[4 * q + 1] = fabsf(v.y); a[4 * q + 2] = fabsf(v.z); a[4 * q + 3] = fabsf(v.w);
+    h[4 * q] = hclip(u.x); h[4 * q + 1] = hclip(u.y); h[4 * q + 2] = hclip(u.z); h[4 * q + 3] = hclip(u.w);
+  }
+#pragma unroll
+  for (int t = 0; t < GROUP; ++t) part |= (h[t] > 0.f && a[t] > 0.f);
+  return part;
+}
+
+__device__ __forceinline__ double warp_sum_f64(double x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+
+// f64 scale of group g's piece whose outer weights are {t : |w_t| >= thr},
+// one element per lane (the whole warp calls it for the same group).
+__device__ double warp_scale_f64(float a, float h, float thr) {
+  const double hd = h, ha = hd * (double)a;
+  const bool o = a >= thr;
+  const double ta = warp_sum_f64(ha), th = warp_sum_f64(hd);
+  const double oa = warp_sum_f64(o ? ha : 0.0), oh = warp_sum_f64(o ? hd : 0.0);
   return (0.5 * ta + oa) / (0.25 * th + 2.0 * oh);
 }
 
-// E(s) in f64 (levels by |w| > s).
-__device__ double err_f64(const float (&a)[GROUP], const float (&h)[GROUP], double s) {
-  double e = 0.0;
-#pragma unroll
-  for (int t = 0; t < GROUP; ++t) {
-    const double at = a[t];
-    const double d = at - (at > s ? 1.5 : 0.5) * s;
-    e += (double)h[t] * d * d;
-  }
-  return e;
+__device__ double warp_err_f64(float a, float h, double s) {
+  const double ad = a;
+  const double d = ad - (ad > s ? 1.5 : 0.5) * s;
+  return warp_sum_f64((double)h * d * d);
 }
 
-// One block per row; thread k places groups k, k + 128, ... .  Per group:
-// sort |w| (with h) descending; the piece with the k largest outer has
-// B_k = sum h|w| l = 0.5 sum h|w| + sum_top-k h|w|, C_k = sum h l^2 = 0.25
-// sum h + 2 sum_top-k h, stationary point s_k = B_k / C_k and there
-// E = sum h w^2 - B_k s_k; it counts when s_k lies in its piece,
-// a_(k+1) <= s_k <= a_(k).  The smallest f32 E wins; the winner's scale is
-// recomputed in f64, and if the runner-up is within the f32 error both are
-// scored again in f64.
-__global__ void __launch_bounds__(PLACE_THREADS) k_q2tp_place(const float* __restrict__ W, int n,
+constexpr int PLACE_MAX_GPR = GPTQ_MAX_N / GROUP;
+
+// One block per row.  Phase 1: thread k places groups k, k + 128, ... in
+// f32 (sort, piece search).  Phase 2: the groups whose two best pieces tie
+// in f32 are decided in f64 by a whole warp (one element per lane).  Only
+// the row's extreme scales set the ladder, so phase 3 recomputes in f64 just
+// the groups within 1e-4 (relative) of the f32 minimum or maximum -- far
+// above the f32 scale's error -- and the ladder comes from their f64
+// scales.  gscale gets the f32 scales (0 for groups that do not take part).
+__global__ void __launch_bounds__(PLACE_THREADS, 3) k_q2tp_place(const float* __restrict__ W, int n,
                                                               const float* __restrict__ hw,
                                                               float* __restrict__ tab,
                                                               float* __restrict__ lost,
                                                               float* __restrict__ gscale) {
+  __shared__ float gs[PLACE_MAX_GPR], thr1s[PLACE_MAX_GPR], thr2s[PLACE_MAX_GPR];
+  __shared__ uint8_t ties[PLACE_MAX_GPR];
+  __shared__ float fmn[PLACE_THREADS / 32], fmx[PLACE_THREADS / 32];
   __shared__ double smin[PLACE_THREADS / 32], smax[PLACE_THREADS / 32];
   __shared__ int scnt[PLACE_THREADS / 32];
   __shared__ float slo, sst;
-  __shared__ int sc_all;
   const int r = blockIdx.x, tid = threadIdx.x;
+  const int wid = tid / 32, lane = tid % 32;
+  constexpr int NW = PLACE_THREADS / 32;
   const int gpr = n / GROUP;
   const float* wr = W + (long long)r * n;
-  double dmin = INFINITY, dmax = 0.0;
-  int cnt = 0;
   for (int g = tid; g < gpr; g += PLACE_THREADS) {
     float a[GROUP], h[GROUP];
-    bool part = false;
-#pragma unroll
-    for (int q = 0; q < GROUP / 4; ++q) {
-      const float4 v = reinterpret_cast<const float4*>(wr + g * GROUP)[q];
-      const float4 u = reinterpret_cast<const float4*>(hw + g * GROUP)[q];
-      a[4 * q] = fabsf(v.x); a[4 * q + 1] = fabsf(v.y); a[4 * q + 2] = fabsf(v.z); a[4 * q + 3] = fabsf(v.w);
-      h[4 * q] = hclip(u.x); h[4 * q + 1] = hclip(u.y); h[4 * q + 2] = hclip(u.z); h[4 * q + 3] = hclip(u.w);
-    }
-#pragma unroll
-    for (int t = 0; t < GROUP; ++t) part |= (h[t] > 0.f && a[t] > 0.f);
-    double sd = 0.0;
-    if (part) {
+    float sf = 0.f, t1 = INFINITY, t2 = INFINITY;
+    bool tie = false;
+    if (place_load(wr, hw, g, a, h)) {
       sort_desc(a, h);
-      float ta = 0.f, th = 0.f, aa = 0.f;
-#pragma unroll
-      for (int t = 0; t < GROUP; ++t) {
-        ta += h[t] * a[t];
-        th += h[t];
-        aa += h[t] * a[t] * a[t];
+      const PlaceSearch ps = place_search(a, h);
+      sf = ps.s;
+      t1 = ps.thr1;
+      t2 = ps.thr2;
+      tie = ps.tie;
+    }
+    gs[g] = sf;
+    thr1s[g] = t1;
+    thr2s[g] = t2;
+    ties[g] = tie;
+  }
+  __syncthreads();
+  // Phase 2: f32 ties, one warp per group.
+  for (int g0 = wid * 32; g0 < gpr; g0 += PLACE_THREADS) {
+    unsigned m = __ballot_sync(0xffffffffu, g0 + lane < gpr && ties[g0 + lane]);
+    while (m) {
+      const int g = g0 + __ffs(m) - 1;
+      m &= m - 1;
+      const float a = fabsf(wr[g * GROUP + lane]), h = hclip(hw[g * GROUP + lane]);
+      const double s1 = warp_scale_f64(a, h, thr1s[g]), s2 = warp_scale_f64(a, h, thr2s[g]);
+      const double e1 = warp_err_f64(a, h, s1), e2 = warp_err_f64(a, h, s2);
+      const bool take2 = e2 < e1 || (e2 == e1 && s2 < s1);
+      __syncwarp();
+      if (lane == 0) {
+        gs[g] = (float)(take2 ? s2 : s1);
+        if (take2) thr1s[g] = thr2s[g];
       }
-      float e1 = INFINITY, e2 = INFINITY, s1 = 0.f;
-      int k1 = 0, k2 = 0;
-      float pa = 0.f, ph = 0.f;
-#pragma unroll
-      for (int k = 0; k <= GROUP; ++k) {
-        const float B = 0.5f * ta + pa, C = 0.25f * th + 2.f * ph;
-        const float sc = B / C;
-        const float up = k == 0 ? INFINITY : a[k - 1];
-        const float dn = k == GROUP ? 0.f : a[k];
-        if (sc <= up && sc >= dn) {
-          const float e = aa - B * sc;
-          if (e < e1) {
-            if (sc != s1) {
-              e2 = e1;
-              k2 = k1;
-            }
-            e1 = e;
-            s1 = sc;
-            k1 = k;
-          } else if (e < e2 && sc != s1) {
-            e2 = e;
-            k2 = k;
-          }
-        }
-        if (k < GROUP) {
-          pa += h[k] * a[k];
-          ph += h[k];
-        }
-      }
-      sd = top_scale_f64(a, h, k1);
-      if (e2 - e1 <= 1e-4f * fabsf(e1) + 1e-5f * aa) {
-        const double sd2 = top_scale_f64(a, h, k2);
-        const double ea1 = err_f64(a, h, sd), ea2 = err_f64(a, h, sd2);
-        if (ea2 < ea1 || (ea2 == ea1 && sd2 < sd)) sd = sd2;
-      }
-      dmin = fmin(dmin, sd);
-      dmax = fmax(dmax, sd);
+    }
+  }
+  __syncthreads();
+  float mnf = INFINITY, mxf = 0.f;
+  int cnt = 0;
+  for (int g = tid; g < gpr; g += PLACE_THREADS) {
+    const float sf = gs[g];
+    if (gscale) gscale[(long long)r * gpr + g] = sf;
+    if (sf > 0.f) {
+      mnf = fminf(mnf, sf);
+      mxf = fmaxf(mxf, sf);
       ++cnt;
     }
-    if (gscale) gscale[(long long)r * gpr + g] = (float)sd;
   }
   for (int o = 16; o > 0; o >>= 1) {
-    dmin = fmin(dmin, __shfl_xor_sync(0xffffffffu, dmin, o));
-    dmax = fmax(dmax, __shfl_xor_sync(0xffffffffu, dmax, o));
+    mnf = fminf(mnf, __shfl_xor_sync(0xffffffffu, mnf, o));
+    mxf = fmaxf(mxf, __shfl_xor_sync(0xffffffffu, mxf, o));
     cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
   }
-  const int wid = tid / 32, lane = tid % 32;
+  if (lane == 0) {
+    fmn[wid] = mnf;
+    fmx[wid] = mxf;
+    scnt[wid] = cnt;
+  }
+  __syncthreads();
+  mnf = fmn[0];
+  mxf = fmx[0];
+  cnt = scnt[0];
+  for (int i = 1; i < NW; ++i) {
+    mnf = fminf(mnf, fmn[i]);
+    mxf = fmaxf(mxf, fmx[i]);
+    cnt += scnt[i];
+  }
+  // Phase 3: the candidates for the extremes, in f64, one warp per group.
+  double dmin = INFINITY, dmax = 0.0;
+  if (cnt > 0) {
+    const float lo_cut = mnf * (1.f + 1e-4f), hi_cut = mxf * (1.f - 1e-4f);
+    for (int g0 = wid * 32; g0 < gpr; g0 += PLACE_THREADS) {
+      const float sl = g0 + lane < gpr ? gs[g0 + lane] : 0.f;
+      unsigned m = __ballot_sync(0xffffffffu, sl > 0.f && (sl <= lo_cut || sl >= hi_cut));
+      while (m) {
+        const int g = g0 + __ffs(m) - 1;
+        m &= m - 1;
+        const float a = fabsf(wr[g * GROUP + lane]), h = hclip(hw[g * GROUP + lane]);
+        const double sd = warp_scale_f64(a, h, thr1s[g]);
+        dmin = fmin(dmin, sd);
+        dmax = fmax(dmax, sd);
+      }
+    }
+  }
   if (lane == 0) {
     smin[wid] = dmin;
     smax[wid] = dmax;
-    scnt[wid] = cnt;
   }
   __syncthreads();
   if (tid == 0) {
     double mn = smin[0], mx = smax[0];
-    int c = scnt[0];
-    for (int i = 1; i < PLACE_THREADS / 32; ++i) {
+    for (int i = 1; i < NW; ++i) {
       mn = fmin(mn, smin[i]);
       mx = fmax(mx, smax[i]);
-      c += scnt[i];
     }
     float lo = 0.f, st = 0.f;
-    if (c > 0) {
+    if (cnt > 0) {
       lo = __half2float(__double2half(log2(mn)));
       if (mx > mn) {
         const double sd = (log2(mx) - (double)lo) / 30.0;
@@ -196,14 +305,13 @@ __global__ void __launch_bounds__(PLACE_THREADS) k_q2tp_place(const float* __res
     }
     slo = lo;
     sst = st;
-    sc_all = c;
     lost[2 * r] = lo;
     lost[2 * r + 1] = st;
   }
   __syncthreads();
   if (tid < 32) {
     const int c = tid;
-    tab[r * 32 + c] = (sc_all > 0 && c > 0) ? (float)exp2((double)slo + (double)(c - 1) * (double)sst) : 0.f;
+    tab[r * 32 + c] = (cnt > 0 && c > 0) ? (float)exp2((double)slo + (double)(c - 1) * (double)sst) : 0.f;
   }
 }
 

@@ -342,24 +342,37 @@ __global__ void __launch_bounds__(SWEEP_THREADS) k_sweep_block(
       float be = 3.4e38f;
       int bc = 64;  // none below 3.4e38 yet
       if (any) {
+        // Two candidates side by side in packed f32x2 arithmetic (each lane
+        // of a packed operation rounds like the scalar one; w - p is taken
+        // as w + (-p), the same IEEE result).
         const float* hg = hws + gc;
+        const float2 c15 = make_float2(1.5f, 1.5f), m15 = make_float2(-1.5f, -1.5f);
 #pragma unroll 1
-        for (int k = 0; k < 8; ++k) {
-          const int cand = 1 + sub + 4 * k;
-          if (cand > 31) break;
-          const float sck = tabrow[cand];
-          if (!(sck > 0.f)) continue;
-          const float iv = __fdiv_rn(1.0f, sck);
-          float err = 0.f;
+        for (int k = 0; k < 8; k += 2) {
+          const int ca = 1 + sub + 4 * k, cb = ca + 4;
+          if (ca > 31) break;
+          const float sa = tabrow[ca], sb = cb <= 31 ? tabrow[cb] : 0.f;
+          const bool va = sa > 0.f, vb = sb > 0.f;
+          if (!va && !vb) continue;
+          const float2 iv = make_float2(__fdiv_rn(1.0f, va ? sa : 1.f), __fdiv_rn(1.0f, vb ? sb : 1.f));
+          const float2 ns = make_float2(-sa, -sb);
+          float2 err = make_float2(0.f, 0.f);
 #pragma unroll
           for (int t = 0; t < GROUP; ++t) {
-            const float q = q2_code(__fadd_rn(__fmul_rn(w[t], iv), 1.5f));
-            const float d = __fsub_rn(w[t], __fmul_rn(__fsub_rn(q, 1.5f), sck));
-            err = __fadd_rn(err, __fmul_rn(__fmul_rn(hg[t], d), d));
+            const float2 w2 = make_float2(w[t], w[t]);
+            const float2 x = __fadd2_rn(__fmul2_rn(w2, iv), c15);
+            const float2 lev = __fadd2_rn(make_float2(q2_code(x.x), q2_code(x.y)), m15);
+            const float2 d = __fadd2_rn(w2, __fmul2_rn(lev, ns));
+            const float2 hd = __fmul2_rn(make_float2(hg[t], hg[t]), d);
+            err = __fadd2_rn(err, __fmul2_rn(hd, d));
           }
-          if (err < be) {
-            be = err;
-            bc = cand;
+          if (va && err.x < be) {
+            be = err.x;
+            bc = ca;
+          }
+          if (vb && err.y < be) {
+            be = err.y;
+            bc = cb;
           }
         }
       }
