@@ -27,6 +27,9 @@ item):
   ``q2tp_group``, and ``cortiq-cli src/gptq.rs``, ``gptq_quantize_q2tp`` with
   ``Q2tpRule::Placed``: the 2-bit "placed" rule (ladder placement, full rung
   search, the lazy-block host sweep).
+* ``cortiq-cli src/gptq.rs``, ``q2tp_debias_hessian`` / ``q4tp_debias_hessian``:
+  the output debias (per-row slope (W^ H W^T)_rr / (W H W^T)_rr removed
+  through the row's f16 lo).
 
 Readings of points the pages leave open are stated where they are used
 (``ladder`` for the missing converter ladder, ``nominal_rung`` for the f32
@@ -70,3 +73,4 @@ from .q2tp import (  # noqa: F401,E402
     dequant_q2tp,
     plane_to_codes,
 )
+from . import debias  # noqa: F401,E402
