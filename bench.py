@@ -369,6 +369,8 @@ def main():
     ap.add_argument("--rows", type=int, default=None)
     ap.add_argument("--streams", type=int, default=2, help="host threads / streams for --config batch")
     ap.add_argument("--codec", choices=["q4tp", "q2tp"], default="q4tp")
+    ap.add_argument("--debias", action="store_true",
+                    help="add the output debias (W H on the tensor cores, per-row lo shift) to the step")
     args = ap.parse_args()
 
     import synth
@@ -419,8 +421,14 @@ def main():
             torch.empty(rows * gpr, dtype=torch.float32, device=dev))
     stream = torch.cuda.current_stream(dev)
 
+    ws_db = _lib.workspace(lib.gptq_debias_workspace_bytes(rows, n), dev) if args.debias else None
+
     def step():
-        return quantize(hp, n, w, cfg.lam, ws=ws, want_u=False, stream=stream, out=outs)
+        res = quantize(hp, n, w, cfg.lam, ws=ws, want_u=False, stream=stream, out=outs)
+        if args.debias:
+            _lib.debias(2 if q2 else 4, w, hp, outs[0], outs[1], res["tab"], res["lost"], outs[2],
+                        ws=ws_db, stream=stream)
+        return res
 
     res = None
     for _ in range(max(args.warmup, 0)):
@@ -499,7 +507,10 @@ def main():
                     upload(j + 1)
                 hp_d, w_d, o_d = sets[j % 2]
                 stream.wait_event(ready[j % 2])
-                quantize(hp_d, n, w_d, cfg.lam, ws=ws, want_u=False, stream=stream, out=o_d)
+                res_d = quantize(hp_d, n, w_d, cfg.lam, ws=ws, want_u=False, stream=stream, out=o_d)
+                if args.debias:
+                    _lib.debias(2 if q2 else 4, w_d, hp_d, o_d[0], o_d[1], res_d["tab"], res_d["lost"], o_d[2],
+                                ws=ws_db, stream=stream)
                 copy.wait_stream(stream)
                 with torch.cuda.stream(copy):
                     for o_h, o in zip(outs_h[j % 2], o_d):
@@ -551,7 +562,8 @@ def main():
 
     if rank == 0:
         line = {
-            "metric": METRIC_Q2 if q2 else METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "metric": (METRIC_Q2 if q2 else METRIC).replace(") at", "+debias) at") if args.debias
+                      else (METRIC_Q2 if q2 else METRIC), "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": t_dev / args.steps * 1e3, "higher_is_better": False,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",

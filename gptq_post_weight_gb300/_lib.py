@@ -41,6 +41,8 @@ SIGNATURES = {
     "gptq_q2tp_group": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _P, _P]),
     "gptq_q2tp_sweep": (_I, [_P, _I, _I, _P, _P, _P, _P, _P, _P, _P, _S, _P]),
     "gptq_quantize_group_q2tp": (_I, [_P, _I, _D, _P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _S, _P]),
+    "gptq_debias_workspace_bytes": (_S, [_I, _I]),
+    "gptq_debias": (_I, [_I, _P, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _S, _P]),
     "gptq_gram_workspace_bytes": (_S, [_I]),
     "gptq_gram_add": (_I, [_P, _I, _P, _I, _P, _S, _P]),
     "gptq_launch_count": (ctypes.c_longlong, []),
@@ -450,3 +452,21 @@ def quantize_group_q2tp(h_packed, n, w, lam=0.01, ws=None, want_u=True, stream=N
     _check("gptq_quantize_group_q2tp", code)
     return dict(codes=codes, rungs=rungs, scales=scales, tab=tab, lost=lost, u=u, d=d, hdiag=hd,
                 lam=lam_used.value)
+
+
+def debias(bits, w, h_packed, codes, rungs, tab, lost, scales, ws=None, want_num_den=False, stream=None):
+    """Output debias (in place on tab, lost, scales).  Returns num_den [rows, 2]
+    f64 or None."""
+    import torch
+
+    lib = load()
+    _cuda_f32(w, "w")
+    _cuda_f32(h_packed, "h_packed")
+    rows, n = w.shape
+    nd = torch.empty(rows, 2, dtype=torch.float64, device=w.device) if want_num_den else None
+    if ws is None:
+        ws = workspace(lib.gptq_debias_workspace_bytes(rows, n), w.device)
+    code = lib.gptq_debias(int(bits), _ptr(w), rows, n, _ptr(h_packed), _ptr(codes), _ptr(rungs), _ptr(tab),
+                           _ptr(lost), _ptr(scales), _ptr(nd), _ptr(ws), ws.numel(), _stream(torch, stream))
+    _check("gptq_debias", code)
+    return nd

@@ -36,6 +36,10 @@ gptq_status place_q2_run(const float* W, int rows, int n, const float* hw, float
 gptq_status group_q2_run(const float* tile, int rows, const float* ublk, const float* hw,
                          const float* tab, uint8_t* codes, uint8_t* rungs, float* scales, float* E,
                          cudaStream_t s);
+size_t debias_ws_bytes(int rows, int n);
+gptq_status debias_run(int bits, const float* W, int rows, int n, const float* Hp,
+                       const uint8_t* codes, const uint8_t* rungs, float* tab, float* lost,
+                       float* scales, double* num_den, void* ws, size_t ws_bytes, cudaStream_t s);
 gptq_status sweep_q2_run(float* W, int rows, int n, const float* U, const float* hw,
                          const float* tab, uint8_t* codes, uint8_t* rungs, float* scales, void* ws,
                          size_t ws_bytes, cudaStream_t s);
@@ -235,6 +239,24 @@ gptq_status gptq_quantize_group_q2tp(const float* H_packed, int n, double lambda
   GQ_TRY(copy_dead_zeroed(W, rows, n, hd, wz, s));
   GQ_TRY(place_q2_run(wz, rows, n, hd, tb, ls, nullptr, s));
   return sweep_q2_run(wz, rows, n, u, hd, tb, codes, rungs, scales, rest, rest_bytes, s);
+}
+
+size_t gptq_debias_workspace_bytes(int rows, int n) {
+  if (bad_n(n) || bad_rows(rows)) return 0;
+  return debias_ws_bytes(rows, n);
+}
+
+gptq_status gptq_debias(int bits, const float* W, int rows, int n, const float* H_packed,
+                        const uint8_t* codes, const uint8_t* rungs, float* tab, float* lost,
+                        float* scales, double* num_den, void* ws, size_t ws_bytes, void* stream) {
+  if (bad_n(n) || bad_rows(rows) || n % GPTQ_GROUP != 0) return GPTQ_ERR_SHAPE;
+  if (bits != 2 && bits != 4) return GPTQ_ERR_ARG;
+  if (!ptr_ok(W) || !ptr_ok(H_packed) || !ptr_ok(codes) || rungs == nullptr || !ptr_ok(tab) ||
+      !ptr_ok(lost) || !ptr_ok(scales) || !opt_ok(num_den) || ws == nullptr)
+    return GPTQ_ERR_ARG;
+  if (ws_bytes < debias_ws_bytes(rows, n)) return GPTQ_ERR_NOMEM;
+  return debias_run(bits, W, rows, n, H_packed, codes, rungs, tab, lost, scales, num_den, ws,
+                    ws_bytes, as_stream(stream));
 }
 
 size_t gptq_gram_workspace_bytes(int n) { return bad_n(n) ? 0 : gram_ws_bytes(n); }

@@ -245,6 +245,36 @@ gptq_status gptq_quantize_group_q2tp(const float* H_packed, int n, double lambda
                                      float* tab, float* lost, float* U, float* D, float* hdiag,
                                      double* lambda_used, void* ws, size_t ws_bytes, void* stream);
 
+/*
+ * gptq_debias -- output debias of a quantized matrix ([host page]
+ * q2tp_debias_hessian / q4tp_debias_hessian, GEMM form q2tp_debias_gemm):
+ * per row the regression slope b = num/den of the quantized outputs on the
+ * original ones, num = (W^ H W^T)_rr, den = (W H W^T)_rr, is removed through
+ * the row's f16 lo; codes, rungs and step stay.  The lo update is not on the
+ * pages; reading implemented: lo' = f16(lo + log2(den/num)) when num > 0
+ * and den > 0 (else lo is kept), the row's rungs rebuilt from (lo', step)
+ * (q2tp: rung 0 = 0, rung c = 2^(lo' + (c-1) step); q4tp: 2^(lo' + c step);
+ * a row with no non-zero rung keeps its zeros) and every scale set to its
+ * rung's new value.  W H on the tensor cores (3xTF32, f32 accumulation
+ * drained every 128 of K), the row dots with compensated f32 sums.
+ *
+ *   bits     2 (q2tp: codes = the 2-bit plane of gptq_q2tp_sweep) or 4
+ *            (q4tp: codes = the nibble plane of gptq_q4tp_sweep).
+ *   W        in  f32 rows*n: the original weights (dead channels have zero
+ *            rows and columns in H, so their weights do not count).
+ *   H_packed in  f32 n(n+1)/2: the raw Hessian, as gptq_fold reads it.
+ *   codes, rungs in: the sweep's outputs.
+ *   tab, lost, scales in/out: the sweep's ladder, (lo, step) and scales;
+ *            rewritten for the rows whose slope is positive.
+ *   num_den  out f64 rows*2 (may be NULL): num, den per row.
+ *   ws       >= gptq_debias_workspace_bytes(rows, n) (dense H as a TF32 pair,
+ *            W as a TF32 pair, W H).  Reads back a 4-byte status at the end.
+ */
+size_t gptq_debias_workspace_bytes(int rows, int n);
+gptq_status gptq_debias(int bits, const float* W, int rows, int n, const float* H_packed,
+                        const uint8_t* codes, const uint8_t* rungs, float* tab, float* lost,
+                        float* scales, double* num_den, void* ws, size_t ws_bytes, void* stream);
+
 /* Workspace bytes gptq_quantize_group (and gptq_quantize_group_q2tp) needs. */
 size_t gptq_group_workspace_bytes(int rows, int n);
 
