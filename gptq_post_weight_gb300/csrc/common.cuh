@@ -99,6 +99,10 @@ struct TcJob {
   int a_map, b_map, a_row0, b_row0;
   int mode, mt, nt, M, N, ntiles;
   int add;  // 0: C -= A B^T; 1: C += A B^T
+  // SM-pair kernel, rectangles: > 0 walks the tiles in bands of this many
+  // tile rows, down each band's columns (tiles running at the same time
+  // then share operand panels in L2: for long K); 0 = row by row.
+  int band;
 };
 
 struct OperandMaps {

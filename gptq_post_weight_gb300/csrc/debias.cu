@@ -201,7 +201,8 @@ gptq_status debias_run(int bits, const float* W, int rows, int n, const float* H
   GQ_TRY(make_operand_map(&maps.m[3], Hl, n, n));
   GQ_TRY(make_c_map(&maps.c, Y, rows, n, n));
   TcJob j = tc_rect(0, 0, 0, 0, 2, 0, rows, n);
-  j.add = 1;  // Y += W H^T (= W H)
+  j.add = 1;   // Y += W H^T (= W H)
+  j.band = 8;  // 76 concurrent tiles ~ 8 x 9.5: about 17 operand panels in flight instead of 70
   GQ_TRY(gemm_pair_sub(maps, j, TcJob{}, n, status, status, K_DEBIAS_GEMM, s, FusedPotrf{}, KSEG));
   {
     GQ_PROF(K_DEBIAS, s);

@@ -56,6 +56,12 @@ __device__ __forceinline__ void ptile_of(const PJob& J, int t, int& ti, int& tj)
     while (i * (i + 1) / 2 > t) --i;
     ti = i;
     tj = t - i * (i + 1) / 2;
+  } else if (J.j.band > 0) {
+    const int per = J.j.band * J.nt;
+    const int g = t / per, r = t - g * per;
+    const int rows = min(J.j.band, J.mt - g * J.j.band);
+    ti = g * J.j.band + r % rows;
+    tj = r / rows;
   } else {
     ti = t / J.nt;
     tj = t % J.nt;
