@@ -61,28 +61,30 @@ def workload_desc(cfg, codec="q4tp"):
             f"lambda={cfg.lam}, group 32, " + ("q4tp" if codec == "q4tp" else "q2tp placed rule"))
 
 
-def fold_gemm_flops(n, NB=128):
+def fold_gemm_flops(n, NB=128, part="all"):
     """Useful flops of the fold's update GEMM launches over one fold, on the
     padded size, following the library's schedule: steps in pairs (a thin
     K = NB strip update of the next block column between them, then one
-    K = 2 NB trailing update), a last unpaired step with K = NB."""
+    K = 2 NB trailing update), a last unpaired step with K = NB.
+    part: "trailing" (the K = 2 NB and unpaired updates, kind fold_gemm),
+    "strip" (the thin K = NB strips, kind fold_strip) or "all"."""
     N = (n + NB - 1) // NB * NB
-    tot = 0
+    strip = trail = 0
     k = 0
     while k < N:
         if k + 2 * NB <= N:
             k1, s1 = k + NB, k + 2 * NB
-            tot += 2 * NB * ((N - k1 - NB) * NB + NB * (NB + 1) // 2)  # SYRK strip
-            tot += 2 * NB * k1 * NB  # inverse strip
+            strip += 2 * NB * ((N - k1 - NB) * NB + NB * (NB + 1) // 2)  # SYRK strip
+            strip += 2 * NB * k1 * NB  # inverse strip
             m = N - s1
-            tot += 2 * (2 * NB) * (m * (m + 1) // 2) + 2 * (2 * NB) * s1 * m
+            trail += 2 * (2 * NB) * (m * (m + 1) // 2) + 2 * (2 * NB) * s1 * m
             k = s1
         else:
             s0 = k + NB
             m = N - s0
-            tot += 2 * NB * (m * (m + 1) // 2) + 2 * NB * s0 * m
+            trail += 2 * NB * (m * (m + 1) // 2) + 2 * NB * s0 * m
             k = s0
-    return tot
+    return {"trailing": trail, "strip": strip, "all": trail + strip}[part]
 
 
 def sweep_gemm_flops(rows, n, SB=128):
@@ -466,7 +468,7 @@ def main():
     # every launch of the two tensor-core update kinds (on the launching
     # stream), for the roofline's achieved rate.
     barrier()
-    _lib.profile_start(200000, kinds=("fold_gemm", "sweep_gemm"))
+    _lib.profile_start(200000, kinds=("fold_gemm", "fold_strip", "sweep_gemm"))
     for _ in range(args.steps):
         step()
     torch.cuda.synchronize()
@@ -529,10 +531,10 @@ def main():
 
     # Roofline of the dominant kernel kind, from the live event timings.
     pk, src = peaks()
-    kinds = {k: v for k, v in prof.items() if not k.startswith("_")}
+    kinds = {k: v for k, v in prof.items() if k in ("fold_gemm", "sweep_gemm")}
     top = max(kinds, key=lambda k: kinds[k][0])
     ms_top, cnt_top = kinds[top]
-    flops = {"fold_gemm": fold_gemm_flops(n) * args.steps,
+    flops = {"fold_gemm": fold_gemm_flops(n, part="trailing") * args.steps,
              "sweep_gemm": sweep_gemm_flops(rows, n) * args.steps}
     roof = None
     if top in flops and cnt_top > 0:
@@ -574,7 +576,7 @@ def main():
             "roofline": roof,
             "fold_tflops_algorithmic": fold_flops / (per_kind.get("fold_gemm", {}).get("ms_per_step", 0) / 1e3
                                                      + sum(per_kind.get(k, {}).get("ms_per_step", 0) / 1e3
-                                                           for k in ("build", "potrf", "trsm", "diag"))
+                                                           for k in ("build", "potrf", "trsm", "diag", "fold_strip"))
                                                      ) / 1e12 if "fold_gemm" in per_kind else None,
             "per_kernel": per_kind,
             "per_kernel_source": "one extra untimed step with every launch bracketed by events",

@@ -38,7 +38,7 @@ constexpr int GROUP = 32;
 // Kernel kinds for launch accounting / per-kind timing (gptq_profile_*).
 enum Kind : int {
   K_DIAG = 0, K_BUILD, K_POTRF, K_TRSM, K_FOLD_GEMM, K_LADDER, K_SWEEP_BLOCK, K_PREP_UT,
-  K_SWEEP_GEMM, K_GROUP, K_COPY, K_GRAM_PREP, K_GRAM_GEMM, K_PLACE, K_DEBIAS, K_DEBIAS_GEMM, K_NKINDS
+  K_SWEEP_GEMM, K_GROUP, K_COPY, K_GRAM_PREP, K_GRAM_GEMM, K_PLACE, K_DEBIAS, K_DEBIAS_GEMM, K_FOLD_STRIP, K_NKINDS
 };
 
 // Every launch site calls prof_begin/prof_end around its <<<>>>: they count

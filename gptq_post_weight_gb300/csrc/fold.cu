@@ -454,7 +454,9 @@ static gptq_status fold_attempt(const float* hp, const FoldWs& w, const OperandM
       {
         const TcJob syrk = tc_strip(k1, k1, 0, k1, 0, k1, N - k1, NB);
         const TcJob inv = tc_rect(k1, 0, 2, 0, 0, k1, k1, NB);
-        GQ_TRY(gemm_tc_sub(maps, syrk, inv, NB, w.flag, w.flag, K_FOLD_GEMM, s, fused(k1)));
+        // Kind fold_strip: a 128-wide update whose time is mostly the fused
+        // diagonal-block step of block k1 (a serial factorisation on one SM).
+        GQ_TRY(gemm_tc_sub(maps, syrk, inv, NB, w.flag, w.flag, K_FOLD_STRIP, s, fused(k1)));
       }
       GQ_TRY(apply(k1, NB, 0));
       if (s1 < N) {

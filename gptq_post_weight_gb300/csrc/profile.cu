@@ -22,7 +22,7 @@ unsigned g_mask = ~0u;  // kinds that record events
 const char* kNames[K_NKINDS] = {"diag", "build", "potrf", "trsm", "fold_gemm", "ladder",
                                 "sweep_block", "prep_ut", "sweep_gemm", "group", "copy",
                                 "gram_prep", "gram_gemm", "place", "debias",
-                                "debias_gemm"};
+                                "debias_gemm", "fold_strip"};
 
 }  // namespace
 
