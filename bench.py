@@ -369,7 +369,7 @@ def main():
     ap.add_argument("--ref-rows", type=int, default=8)
     ap.add_argument("--n", type=int, default=None, help="override n (T = 2n) for small profiling cases")
     ap.add_argument("--rows", type=int, default=None)
-    ap.add_argument("--streams", type=int, default=2, help="host threads / streams for --config batch")
+    ap.add_argument("--streams", type=int, default=4, help="host threads / streams for --config batch")
     ap.add_argument("--codec", choices=["q4tp", "q2tp"], default="q4tp")
     ap.add_argument("--debias", action="store_true",
                     help="add the output debias (W H on the tensor cores, per-row lo shift) to the step")

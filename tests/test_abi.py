@@ -74,3 +74,28 @@ def test_argument_errors_before_launch(clib):
     assert clib.gptq_quantize_group(fake, 64, 0.01, fake, 4, fake, fake, fake, None, None, None, None,
                                     None, None, ws, 16, None) == 3
     assert clib.gptq_status_string(4).startswith(b"not positive definite")
+
+
+def test_q2tp_and_debias_argument_errors(clib):
+    P = ctypes.c_void_p
+    fake = P(1 << 20)
+    mis = P((1 << 20) + 4)
+    ws = P(1 << 21)
+    # shapes: n % 32 != 0, rows = 0
+    assert clib.gptq_q2tp_place(fake, 4, 48, fake, fake, fake, None, None) == 2
+    assert clib.gptq_q2tp_sweep(fake, 4, 40, fake, fake, fake, fake, fake, fake, ws, 1 << 40, None) == 2
+    assert clib.gptq_q2tp_sweep(fake, 0, 64, fake, fake, fake, fake, fake, fake, ws, 1 << 40, None) == 2
+    assert clib.gptq_debias(2, fake, 4, 40, fake, fake, fake, fake, fake, fake, None, ws, 1 << 40, None) == 2
+    # pointers, codec width
+    assert clib.gptq_q2tp_place(fake, 4, 64, mis, fake, fake, None, None) == 1
+    assert clib.gptq_q2tp_place(fake, 4, 64, fake, fake, fake, mis, None) == 1
+    assert clib.gptq_q2tp_group(fake, 8, fake, fake, None, fake, fake, fake, fake, None) == 1
+    assert clib.gptq_debias(3, fake, 4, 64, fake, fake, fake, fake, fake, fake, None, ws, 1 << 40, None) == 1
+    assert clib.gptq_debias(2, fake, 4, 64, fake, fake, fake, fake, fake, fake, mis, ws, 1 << 40, None) == 1
+    # workspace too small
+    assert clib.gptq_q2tp_sweep(fake, 4, 64, fake, fake, fake, fake, fake, fake, ws, 16, None) == 3
+    assert clib.gptq_quantize_group_q2tp(fake, 64, 0.01, fake, 4, fake, fake, fake, None, None, None,
+                                         None, None, None, ws, 16, None) == 3
+    assert clib.gptq_debias(4, fake, 4, 64, fake, fake, fake, fake, fake, fake, None, ws, 16, None) == 3
+    assert clib.gptq_debias_workspace_bytes(5120, 17408) >= 2 * 17408 * 17408 * 4
+    assert clib.gptq_debias_workspace_bytes(0, 64) == 0
