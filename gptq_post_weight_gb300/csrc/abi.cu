@@ -8,6 +8,7 @@
 namespace gq {
 size_t fold_ws_bytes(int n);
 size_t sweep_ws_bytes(int rows, int n);
+size_t sweep_ws_min_bytes(int rows, int n);
 gptq_status fold_run(const float* hp, int n, double lambda, float* U, float* D, float* hdiag,
                      double* lambda_used, void* ws, size_t ws_bytes, cudaStream_t s,
                      const int* perm = nullptr);
@@ -133,7 +134,7 @@ gptq_status gptq_q4tp_sweep(float* W, int rows, int n, const float* U, const flo
   if (!ptr_ok(W) || !ptr_ok(U) || !ptr_ok(hw) || !ptr_ok(tab) || !ptr_ok(lost) ||
       !ptr_ok(nibbles) || rungs == nullptr || !ptr_ok(scales) || ws == nullptr)
     return GPTQ_ERR_ARG;
-  if (ws_bytes < sweep_ws_bytes(rows, n)) return GPTQ_ERR_NOMEM;
+  if (ws_bytes < sweep_ws_min_bytes(rows, n)) return GPTQ_ERR_NOMEM;
   return sweep_run(W, rows, n, U, hw, tab, lost, nibbles, rungs, scales, ws, ws_bytes,
                    as_stream(stream));
 }
@@ -145,7 +146,7 @@ gptq_status gptq_q4tp_sweep_noalloc(float* W, int rows, int n, const float* U, c
   if (!ptr_ok(W) || !ptr_ok(U) || !ptr_ok(hw) || !ptr_ok(tab) || !ptr_ok(lost) ||
       !ptr_ok(nibbles) || rungs == nullptr || !ptr_ok(scales))
     return GPTQ_ERR_ARG;
-  if (sweep_ws_bytes(rows, n) > (size_t)GPTQ_SWEEP_NOALLOC_SCRATCH_BYTES) return GPTQ_ERR_NOMEM;
+  if (sweep_ws_min_bytes(rows, n) > (size_t)GPTQ_SWEEP_NOALLOC_SCRATCH_BYTES) return GPTQ_ERR_NOMEM;
   void* scratch = nullptr;
   GQ_TRY(noalloc_scratch(&scratch));
   return sweep_run(W, rows, n, U, hw, tab, lost, nibbles, rungs, scales, scratch,
@@ -207,7 +208,7 @@ gptq_status gptq_q2tp_sweep(float* W, int rows, int n, const float* U, const flo
   if (!ptr_ok(W) || !ptr_ok(U) || !ptr_ok(hw) || !ptr_ok(tab) || !ptr_ok(codes) ||
       rungs == nullptr || !ptr_ok(scales) || ws == nullptr)
     return GPTQ_ERR_ARG;
-  if (ws_bytes < sweep_ws_bytes(rows, n)) return GPTQ_ERR_NOMEM;
+  if (ws_bytes < sweep_ws_min_bytes(rows, n)) return GPTQ_ERR_NOMEM;
   return sweep_q2_run(W, rows, n, U, hw, tab, codes, rungs, scales, ws, ws_bytes,
                       as_stream(stream));
 }

@@ -229,7 +229,9 @@ constexpr int SWEEP_ROWS = 40;                 // 5 warps: 5120 rows fill 128 CT
 constexpr int SWEEP_THREADS = 4 * SWEEP_ROWS;  // a quad of lanes per row
 constexpr int LW = SB + 16;  // W block row stride: float4 rows, two rows per phase conflict-free
 constexpr int ESR = GROUP + 4;  // row stride of the group residuals in shared memory
-constexpr int EW = 2 * SB;   // residual / U-stripe buffers hold a pair of blocks
+// Blocks whose residuals one trailing update applies (K = GMAX * SB); a
+// workspace too small for that runs groups of GMIN blocks.
+constexpr int GMAX = 4, GMIN = 2;
 constexpr int SWEEP_SMEM = (SB * SB + SB + SWEEP_ROWS * LW + SWEEP_ROWS * ESR) * 4;
 
 // One lazy block [b0, b0+B) (B <= SB, a multiple of 32) for 40 rows per CTA.
@@ -268,8 +270,8 @@ __global__ void __launch_bounds__(SWEEP_THREADS) k_sweep_block(
     const float* __restrict__ W, int rows, int n, int b0, int B, const float* __restrict__ U,
     const float* __restrict__ hw, const float* __restrict__ tab, const float* __restrict__ lost,
     uint8_t* __restrict__ nib, uint8_t* __restrict__ rungs, float* __restrict__ scales,
-    float* __restrict__ E_hi, float* __restrict__ E_lo, int ecol0, const int* __restrict__ perm,
-    int8_t* __restrict__ codes) {
+    float* __restrict__ E_hi, float* __restrict__ E_lo, int ecol0, int ew,
+    const int* __restrict__ perm, int8_t* __restrict__ codes) {
   constexpr bool ACT = MODE == MODE_Q4_ACT;
   constexpr bool Q2 = MODE == MODE_Q2;
   constexpr int NWORDS = ACT ? GROUP / 4 : (Q2 ? GROUP / 16 : GROUP / 8);
@@ -490,8 +492,8 @@ __global__ void __launch_bounds__(SWEEP_THREADS) k_sweep_block(
         rungs[tix] = (uint8_t)best_c;
         scales[tix] = s;
       }
-      float* eh = E_hi + (long long)r * EW + ecol0 + gc;
-      float* el = E_lo + (long long)r * EW + ecol0 + gc;
+      float* eh = E_hi + (long long)r * ew + ecol0 + gc;
+      float* el = E_lo + (long long)r * ew + ecol0 + gc;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         if (sub != c) continue;
@@ -537,7 +539,7 @@ __global__ void __launch_bounds__(SWEEP_THREADS) k_sweep_block(
 // for the GEMM, stored as their TF32 hi/lo split.  Rows b1 + c of U below
 // the diagonal are zero, so the same stripe serves the thin update of the
 // second block (c < SB, first SB of t) and the pair's trailing update.
-__global__ void k_prep_ut(const float* __restrict__ U, int n, int b0, int b1,
+__global__ void k_prep_ut(const float* __restrict__ U, int n, int b0, int b1, int ew,
                           float* __restrict__ Ut_hi, float* __restrict__ Ut_lo) {
   __shared__ float tile[32][33];
   const int c0 = blockIdx.x * 32, t0 = blockIdx.y * 32;
@@ -552,8 +554,8 @@ __global__ void k_prep_ut(const float* __restrict__ U, int n, int b0, int b1,
     if (c < ncol) {
       float h, l;
       split_tf32(tile[threadIdx.x][i], h, l);
-      Ut_hi[(long long)c * EW + t0 + threadIdx.x] = h;
-      Ut_lo[(long long)c * EW + t0 + threadIdx.x] = l;
+      Ut_hi[(long long)c * ew + t0 + threadIdx.x] = h;
+      Ut_lo[(long long)c * ew + t0 + threadIdx.x] = l;
     }
   }
 }
@@ -571,9 +573,12 @@ __global__ void k_copy_dz(const float* __restrict__ W, long long total, int n,
 
 }  // namespace
 
-size_t sweep_ws_bytes(int rows, int n) {
-  return 2 * round_up((size_t)rows * EW * 4, 256) + 2 * round_up((size_t)n * EW * 4, 256) + 1024;
+static size_t sweep_ws_bytes_g(int rows, int n, int g) {
+  const size_t ew = (size_t)g * SB;
+  return 2 * round_up((size_t)rows * ew * 4, 256) + 2 * round_up((size_t)n * ew * 4, 256) + 1024;
 }
+size_t sweep_ws_bytes(int rows, int n) { return sweep_ws_bytes_g(rows, n, GMAX); }
+size_t sweep_ws_min_bytes(int rows, int n) { return sweep_ws_bytes_g(rows, n, GMIN); }
 
 static gptq_status sweep_attrs() {
   static bool done = false;
@@ -644,19 +649,21 @@ static gptq_status sweep_core(int mode, float* W, int rows, int n, const float* 
                               float* scales, void* ws, size_t ws_bytes, cudaStream_t s,
                               const int* perm, int8_t* codes) {
   GQ_TRY(sweep_attrs());
+  const int G = ws_bytes >= sweep_ws_bytes_g(rows, n, GMAX) ? GMAX : GMIN;
+  const int ew = G * SB;
   Carve c(ws, ws_bytes);
-  float* E_hi = c.take<float>((size_t)rows * EW);
-  float* E_lo = c.take<float>((size_t)rows * EW);
-  float* Ut_hi = c.take<float>((size_t)n * EW);
-  float* Ut_lo = c.take<float>((size_t)n * EW);
+  float* E_hi = c.take<float>((size_t)rows * ew);
+  float* E_lo = c.take<float>((size_t)rows * ew);
+  float* Ut_hi = c.take<float>((size_t)n * ew);
+  float* Ut_lo = c.take<float>((size_t)n * ew);
   unsigned* status = c.take<unsigned>(4);
   if (!c.ok) return GPTQ_ERR_NOMEM;
   GQ_CUDA(cudaMemsetAsync(status, 0, sizeof(unsigned), s));
   OperandMaps maps;  // 0/1 = Ut hi/lo, 2/3 = E hi/lo
-  GQ_TRY(make_operand_map(&maps.m[0], Ut_hi, n, EW));
-  GQ_TRY(make_operand_map(&maps.m[1], Ut_lo, n, EW));
-  GQ_TRY(make_operand_map(&maps.m[2], E_hi, rows, EW));
-  GQ_TRY(make_operand_map(&maps.m[3], E_lo, rows, EW));
+  GQ_TRY(make_operand_map(&maps.m[0], Ut_hi, n, ew));
+  GQ_TRY(make_operand_map(&maps.m[1], Ut_lo, n, ew));
+  GQ_TRY(make_operand_map(&maps.m[2], E_hi, rows, ew));
+  GQ_TRY(make_operand_map(&maps.m[3], E_lo, rows, ew));
   GQ_TRY(make_c_map(&maps.c, W, rows, n, n));
   const int smem = SWEEP_SMEM;
   const TcJob none{};
@@ -665,14 +672,14 @@ static gptq_status sweep_core(int mode, float* W, int rows, int n, const float* 
     GQ_PROF(K_SWEEP_BLOCK, s);
     if (mode == MODE_Q4_ACT)
       k_sweep_block<MODE_Q4_ACT><<<grid_rows, SWEEP_THREADS, smem, s>>>(
-          W, rows, n, b0, B, U, hw, tab, lost, nib, rungs, scales, E_hi, E_lo, ecol0, perm, codes);
+          W, rows, n, b0, B, U, hw, tab, lost, nib, rungs, scales, E_hi, E_lo, ecol0, ew, perm, codes);
     else if (mode == MODE_Q2)
       k_sweep_block<MODE_Q2><<<grid_rows, SWEEP_THREADS, smem, s>>>(
-          W, rows, n, b0, B, U, hw, tab, lost, nib, rungs, scales, E_hi, E_lo, ecol0, nullptr,
+          W, rows, n, b0, B, U, hw, tab, lost, nib, rungs, scales, E_hi, E_lo, ecol0, ew, nullptr,
           nullptr);
     else
       k_sweep_block<MODE_Q4><<<grid_rows, SWEEP_THREADS, smem, s>>>(
-          W, rows, n, b0, B, U, hw, tab, lost, nib, rungs, scales, E_hi, E_lo, ecol0, nullptr,
+          W, rows, n, b0, B, U, hw, tab, lost, nib, rungs, scales, E_hi, E_lo, ecol0, ew, nullptr,
           nullptr);
     GQ_LAUNCHED();
     return GPTQ_OK;
@@ -680,35 +687,40 @@ static gptq_status sweep_core(int mode, float* W, int rows, int n, const float* 
   auto prep = [&](int b0, int b1, int kt) -> gptq_status {
     GQ_PROF(K_PREP_UT, s);
     dim3 grid((n - b1 + 31) / 32, kt / 32);
-    k_prep_ut<<<grid, dim3(32, 8), 0, s>>>(U, n, b0, b1, Ut_hi, Ut_lo);
+    k_prep_ut<<<grid, dim3(32, 8), 0, s>>>(U, n, b0, b1, ew, Ut_hi, Ut_lo);
     GQ_LAUNCHED();
     return GPTQ_OK;
   };
-  // maps: 0/1 = Ut hi/lo, 2/3 = E hi/lo (K up to 2 SB).
+  // Groups of up to G blocks from b0: each block in turn, with the residuals
+  // of the group's earlier blocks brought into its columns first (a thin
+  // update, K = i * SB); then one update with K = (blocks) * SB for every
+  // column right of the group.  Ut[c][t] = U[b0 + t][b0 + SB + c] (TF32
+  // split), E[r][t] = the group's residuals, t < K.
+  // maps: 0/1 = Ut hi/lo, 2/3 = E hi/lo.
   int b0 = 0;
   while (b0 < n) {
-    if (b0 + 2 * SB <= n) {
-      const int b1 = b0 + SB, b2 = b0 + 2 * SB;
-      GQ_TRY(block(b0, SB, 0));
-      GQ_TRY(prep(b0, b1, 2 * SB));
-      GQ_TRY(gemm_tc_sub(maps, tc_rect(b1, 0, 2, 0, 0, 0, rows, SB), none, SB, status, status,
-                         K_SWEEP_GEMM, s));
-      GQ_TRY(block(b1, SB, SB));
-      if (b2 < n)
-        GQ_TRY(gemm_pair_sub(maps, tc_rect(b2, 0, 2, 0, 0, SB, rows, n - b2), none, 2 * SB, status,
-                             status, K_SWEEP_GEMM, s));
-      b0 = b2;
-    } else {
-      const int B = (n - b0) < SB ? (n - b0) : SB;
-      const int b1 = b0 + B;
-      GQ_TRY(block(b0, B, 0));
-      if (b1 < n) {
-        GQ_TRY(prep(b0, b1, SB));
-        GQ_TRY(gemm_tc_sub(maps, tc_rect(b1, 0, 2, 0, 0, 0, rows, n - b1), none, SB, status,
-                           status, K_SWEEP_GEMM, s));
+    const int left = (n - b0 + SB - 1) / SB;
+    const int nb = left < G ? left : G;
+    const int b1 = b0 + SB;
+    const int kt = (nb * SB < n - b0) ? nb * SB : n - b0;  // rows of U the group reads
+    int bend = b0;
+    for (int i = 0; i < nb; ++i) {
+      const int bi = b0 + i * SB;
+      const int Bi = (n - bi) < SB ? (n - bi) : SB;
+      GQ_TRY(block(bi, Bi, i * SB));
+      bend = bi + Bi;
+      if (i == 0 && b1 < n) GQ_TRY(prep(b0, b1, kt));
+      if (i + 1 < nb) {
+        const int bn = bi + SB;
+        const int Bn = (n - bn) < SB ? (n - bn) : SB;
+        GQ_TRY(gemm_tc_sub(maps, tc_rect(bn, 0, 2, 0, 0, bn - b1, rows, Bn), none, (i + 1) * SB,
+                           status, status, K_SWEEP_GEMM, s));
       }
-      b0 = b1;
     }
+    if (bend < n)
+      GQ_TRY(gemm_pair_sub(maps, tc_rect(bend, 0, 2, 0, 0, bend - b1, rows, n - bend), none, nb * SB,
+                           status, status, K_SWEEP_GEMM, s));
+    b0 = bend;
   }
   unsigned hs = 0;
   GQ_CUDA(cudaMemcpyAsync(&hs, status, sizeof(unsigned), cudaMemcpyDeviceToHost, s));

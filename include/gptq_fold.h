@@ -97,7 +97,11 @@ gptq_status gptq_fold(const float* H_packed, int n, double lambda, float* U, flo
  */
 gptq_status gptq_ladder(const float* W, int rows, int n, float* tab, float* lost, void* stream);
 
-/* Workspace bytes gptq_q4tp_sweep needs. */
+/* Workspace bytes for gptq_q4tp_sweep / gptq_q2tp_sweep: residuals of four
+ * 128-column blocks go into the later columns in one update (K = 512).  A
+ * workspace of at least half that (rows*2048 + n*2048 bytes, plus slack)
+ * is accepted and runs pairs of blocks (K = 256): the same mathematics, a
+ * different f32 summation order in the updates. */
 size_t gptq_sweep_workspace_bytes(int rows, int n);
 
 /*
@@ -157,9 +161,12 @@ gptq_status gptq_q4tp_group(const float* tile, int rows, const float* ublk, cons
  * ws/ws_bytes.  Scratch lives instead in one file-scope device array of
  * GPTQ_SWEEP_NOALLOC_SCRATCH_BYTES per GPU, which every GPU that loads the
  * library holds until the process exits.  It fits shapes with
- * gptq_sweep_workspace_bytes(rows, n) <= that size (about rows + n <= 24575,
+ * rows*2048 + n*2048 bytes (plus slack) <= that size (about rows + n <= 24575,
  * e.g. 5120 rows x 17408 channels); larger shapes return GPTQ_ERR_NOMEM
- * before any work.  The call allocates nothing.
+ * before any work.  Where the array also holds gptq_sweep_workspace_bytes,
+ * the result is the workspace call's bit for bit; otherwise it runs pairs of
+ * blocks per update (same mathematics, different f32 summation order).  The
+ * call allocates nothing.
  *
  * The first call on a device looks up the array's device address (once per
  * device, with that device current); make that first call before any stream

