@@ -6,12 +6,14 @@
 // groups of a block out of shared memory (rung choice, rounding, in-group
 // feedback, then the group's residuals into the rest of the block), and
 // GEMMs apply the residuals to every later column:
-// W[:, b1:] -= E_blk U[b0:b1, b1:].  Blocks go in pairs: after the first
-// block a thin update (K = 128) brings the second block's columns up to
-// date, and after the second one update with K = 256 (both blocks'
-// residuals) covers everything to the right.  With SB = 32 and no pairing
-// this is the fold page's per-group q4tp_trail; the wider blocks are the
-// same mathematics with the residual sums taken in a different order.
+// W[:, b1:] -= E_blk U[b0:b1, b1:].  Blocks go in groups of four: before
+// each block of a group, a thin update (K = 128, 256, 384) brings its
+// columns up to date with the group's earlier blocks, and after the last
+// one update with K = 512 (all four blocks' residuals) covers everything to
+// the right, so W is read and written once per 512 columns.  With SB = 32
+// and groups of one this is the fold page's per-group q4tp_trail; the wider
+// blocks are the same mathematics with the residual sums taken in a
+// different order.
 //
 // The same pipeline runs the q2tp "placed" rule ([fold page] WGSL q2_level /
 // q2tp_group; [host page] gptq_quantize_q2tp_dev): a full rung search and
