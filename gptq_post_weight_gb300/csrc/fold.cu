@@ -454,9 +454,15 @@ static gptq_status fold_attempt(const float* hp, const FoldWs& w, const OperandM
       {
         const TcJob syrk = tc_strip(k1, k1, 0, k1, 0, k1, N - k1, NB);
         const TcJob inv = tc_rect(k1, 0, 2, 0, 0, k1, k1, NB);
-        // Kind fold_strip: a 128-wide update whose time is mostly the fused
-        // diagonal-block step of block k1 (a serial factorisation on one SM).
-        GQ_TRY(gemm_tc_sub(maps, syrk, inv, NB, w.flag, w.flag, K_FOLD_STRIP, s, fused(k1)));
+        // The 128-wide strip update, then the diagonal-block step of block k1
+        // as its own one-CTA launch (faster here than fused into the strip:
+        // the strip's other tiles are done within microseconds).
+        GQ_TRY(gemm_tc_sub(maps, syrk, inv, NB, w.flag, w.flag, K_FOLD_STRIP, s));
+        {
+          GQ_PROF(K_POTRF, s);
+          k_potrf<<<1, 256, POTRF_SMEM, s>>>(w.A, ld, k1, w.Lkk, w.flag);
+          GQ_LAUNCHED();
+        }
       }
       GQ_TRY(apply(k1, NB, 0));
       if (s1 < N) {
