@@ -427,8 +427,10 @@ static gptq_status fold_attempt(const float* hp, const FoldWs& w, const OperandM
   //   of / below block k + NB.
   // A last unpaired block runs as a single step (K = NB).
   // The diagonal-block step (Cholesky + inverse of block k) of the first
-  // block runs alone; every later one rides in the update GEMM that finishes
-  // its block (tile 0 of that GEMM is exactly that block).
+  // block of a pair rides in the update GEMM that finishes it (tile 0 of
+  // that GEMM is exactly that block); the second block's step runs alone
+  // right after the thin strip (the strip's own tiles are done within
+  // microseconds, so nothing would hide it there), as does the very first.
   auto apply = [&](int k, int col0, int zero_end) -> gptq_status {
     GQ_PROF(K_TRSM, s);
     const int tiles = N / APPLY_ROWS;
