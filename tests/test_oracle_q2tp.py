@@ -9,6 +9,7 @@ GPTQ identities (W0 - Q = E U, ||E||^2 = tr((W0-Q) H_d (W0-Q)^T)), the
 textbook OBS loop, and GPTQ beating round-to-nearest on correlated data.
 """
 import itertools
+import os
 
 import numpy as np
 import pytest
@@ -53,9 +54,12 @@ def prep(w, h, lam=0.01):
 # ---------------------------------------------------------------- level map
 
 def test_q2_level_table():
-    # clamp(round_half_even(clamp(x, -1, 4)), 0, 3), worked by hand.
-    xs = [-7.0, -1.0, -0.5, 0.0, 0.49, 0.5, 0.51, 1.49, 1.5, 2.5, 2.51, 3.49, 3.5, 4.0, 11.0]
-    want = [0, 0, 0, 0, 0, 0, 1, 1, 2, 2, 3, 3, 3, 3, 3]
+    # clamp(round_half_even(clamp(x, -1, 4)), 0, 3), worked by hand
+    # (tests/golden/q2_level.txt, with its citation).
+    path = os.path.join(os.path.dirname(__file__), "golden", "q2_level.txt")
+    rows = [l.split() for l in open(path) if l.strip() and not l.startswith("#")]
+    xs = [float(a) for a, _ in rows]
+    want = [int(b) for _, b in rows]
     got = o2.q2_level(np.array(xs, dtype=F32))
     assert got.tolist() == want
 
