@@ -72,7 +72,9 @@ static __device__ __noinline__ void potrf_inverse_block(const float* __restrict_
       // reading column c-1 from a shared buffer (float4 broadcasts).  Every
       // entry still receives its updates in column order.
       // The next pivot (lane c+1's own entry minus its own square) does not
-      // wait for the exchange that the other lanes need.
+      // wait for the exchange that the other lanes need.  Lanes above a
+      // column's diagonal update their (never stored) upper entries too,
+      // which saves the per-entry lane test.
       float lprev = 0.f, pn = a[0];
 #pragma unroll
       for (int c = 0; c < 32; ++c) {
@@ -86,7 +88,7 @@ static __device__ __noinline__ void potrf_inverse_block(const float* __restrict_
 #pragma unroll
             for (int jj = 0; jj < 4; ++jj) {
               const int j = 4 * j4 + jj;
-              if (j >= c + 1 && lane >= j) a[j] = fmaf(-lprev, lv[jj], a[j]);
+              if (j >= c + 1) a[j] = fmaf(-lprev, lv[jj], a[j]);  // lanes < j: unused upper entries
             }
           }
         }
@@ -102,7 +104,7 @@ static __device__ __noinline__ void potrf_inverse_block(const float* __restrict_
         if (c + 1 < 32) {
           pn = fmaf(-lic, lic, a[c + 1]);
           const float lnc = __shfl_sync(0xffffffffu, lic, c + 1);
-          if (lane >= c + 1) a[c + 1] = (lane == c + 1) ? pn : fmaf(-lic, lnc, a[c + 1]);
+          a[c + 1] = (lane == c + 1) ? pn : fmaf(-lic, lnc, a[c + 1]);
         }
         __syncwarp();
         lprev = lic;
