@@ -80,7 +80,13 @@ def load(path: str = LIB_PATH):
 
 
 def _ptr(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    """Device address of a CUDA tensor (None -> NULL).  Taken when the
+    library call's arguments are built, after every size check."""
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"tensor arguments must be CUDA tensors, got one on {t.device}")
+    return ctypes.c_void_p(t.data_ptr())
 
 
 def _stream(torch, stream=None):
@@ -93,11 +99,52 @@ def _check(fn, code):
         raise GptqError(fn, code)
 
 
-def _cuda_f32(t, name):
+def _need(t, name, dtype=None, numel=None, device=None):
+    """Raise ValueError unless ``t`` is a contiguous tensor of ``dtype``
+    (default float32) with ``numel`` elements on ``device``.  The kernels
+    index every buffer by the sizes the call states, so a buffer of another
+    size is refused here, before anything is launched (that it lives on the
+    GPU is checked by ``_ptr``)."""
     import torch
 
-    if not (t.is_cuda and t.dtype == torch.float32 and t.is_contiguous()):
-        raise ValueError(f"{name} must be a contiguous CUDA float32 tensor")
+    dtype = torch.float32 if dtype is None else dtype
+    if not isinstance(t, torch.Tensor):
+        raise ValueError(f"{name} must be a torch tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if numel is not None and t.numel() != numel:
+        raise ValueError(f"{name} must have {numel} elements, got {t.numel()} (shape {tuple(t.shape)})")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, the call's data on {device}")
+
+
+def _matrix(w, name="w", n=None):
+    """rows, n of a 2-D float32 matrix (n checked when given)."""
+    _need(w, name)
+    if w.dim() != 2:
+        raise ValueError(f"{name} must be 2-D [rows, n], got shape {tuple(w.shape)}")
+    if n is not None and w.shape[1] != n:
+        raise ValueError(f"{name} has {w.shape[1]} columns, n = {n}")
+    return w.shape[0], w.shape[1]
+
+
+def _packed(h_packed, n, device=None):
+    _need(h_packed, "h_packed", numel=n * (n + 1) // 2 if n > 0 else None, device=device)
+
+
+def _ws(ws, device):
+    import torch
+
+    _need(ws, "ws", dtype=torch.uint8, device=device)
+
+
+def _check_outs(out, names, sizes, dtypes, device):
+    if len(out) != len(names):
+        raise ValueError(f"out must hold {len(names)} tensors ({', '.join(names)})")
+    for t, nm, k, dt in zip(out, names, sizes, dtypes):
+        _need(t, nm, dtype=dt, numel=k, device=device)
 
 
 def workspace(nbytes: int, device):
@@ -111,7 +158,7 @@ def fold(h_packed, n: int, lam: float = 0.01, ws=None, stream=None, want_d=True)
     import torch
 
     lib = load()
-    _cuda_f32(h_packed, "h_packed")
+    _packed(h_packed, n)
     dev = h_packed.device
     u = torch.empty(n, n, dtype=torch.float32, device=dev)
     d = torch.empty(n, dtype=torch.float32, device=dev) if want_d else None
@@ -119,6 +166,7 @@ def fold(h_packed, n: int, lam: float = 0.01, ws=None, stream=None, want_d=True)
     need = lib.gptq_fold_workspace_bytes(n)
     if ws is None:
         ws = workspace(need, dev)
+    _ws(ws, dev)
     lam_used = ctypes.c_double(0.0)
     code = lib.gptq_fold(_ptr(h_packed), n, float(lam), _ptr(u), _ptr(d), _ptr(hd),
                          ctypes.byref(lam_used), _ptr(ws), ws.numel(), _stream(torch, stream))
@@ -130,6 +178,7 @@ def build_equilibrated(h_packed, n: int, lam: float = 0.01):
     import torch
 
     lib = load()
+    _packed(h_packed, n)
     dev = h_packed.device
     a = torch.zeros(n, n, dtype=torch.float32, device=dev)
     d = torch.empty(n, dtype=torch.float32, device=dev)
@@ -144,20 +193,35 @@ def ladder(w):
     import torch
 
     lib = load()
-    _cuda_f32(w, "w")
-    rows, n = w.shape
+    rows, n = _matrix(w)
     tab = torch.empty(rows, 32, dtype=torch.float32, device=w.device)
     lost = torch.empty(rows, 2, dtype=torch.float32, device=w.device)
     _check("gptq_ladder", lib.gptq_ladder(_ptr(w), rows, n, _ptr(tab), _ptr(lost), _stream(torch)))
     return tab, lost
 
 
-def _outs(torch, rows, n, dev):
+def _outs(torch, rows, n, dev, out=None):
     gpr = n // 32
+    if out is not None:
+        _check_outs(out, ("nibbles", "rungs", "scales"), (rows * n // 2, rows * gpr, rows * gpr),
+                    (torch.uint8, torch.uint8, torch.float32), dev)
+        return out
     nib = torch.empty(rows * n // 2, dtype=torch.uint8, device=dev)
     rungs = torch.empty(rows * gpr, dtype=torch.uint8, device=dev)
     scales = torch.empty(rows * gpr, dtype=torch.float32, device=dev)
     return nib, rungs, scales
+
+
+def _sweep_inputs(w, u, hw, tab, lost=None):
+    """rows, n after checking W [rows, n], U n*n, hw n, tab rows*32, lost rows*2."""
+    rows, n = _matrix(w)
+    dev = w.device
+    _need(u, "u", numel=n * n, device=dev)
+    _need(hw, "hw", numel=n, device=dev)
+    _need(tab, "tab", numel=rows * 32, device=dev)
+    if lost is not None:
+        _need(lost, "lost", numel=rows * 2, device=dev)
+    return rows, n
 
 
 def q4tp_sweep(w, u, hw, tab, lost, ws=None, out=None, stream=None):
@@ -165,12 +229,11 @@ def q4tp_sweep(w, u, hw, tab, lost, ws=None, out=None, stream=None):
     import torch
 
     lib = load()
-    for t, nm in ((w, "w"), (u, "u"), (hw, "hw"), (tab, "tab"), (lost, "lost")):
-        _cuda_f32(t, nm)
-    rows, n = w.shape
-    nib, rungs, scales = out if out is not None else _outs(torch, rows, n, w.device)
+    rows, n = _sweep_inputs(w, u, hw, tab, lost)
+    nib, rungs, scales = _outs(torch, rows, n, w.device, out)
     if ws is None:
         ws = workspace(lib.gptq_sweep_workspace_bytes(rows, n), w.device)
+    _ws(ws, w.device)
     code = lib.gptq_q4tp_sweep(_ptr(w), rows, n, _ptr(u), _ptr(hw), _ptr(tab), _ptr(lost),
                                _ptr(nib), _ptr(rungs), _ptr(scales), _ptr(ws), ws.numel(),
                                _stream(torch, stream))
@@ -185,14 +248,26 @@ def q4tp_sweep_noalloc(w, u, hw, tab, lost, out=None, stream=None):
     import torch
 
     lib = load()
-    for t, nm in ((w, "w"), (u, "u"), (hw, "hw"), (tab, "tab"), (lost, "lost")):
-        _cuda_f32(t, nm)
-    rows, n = w.shape
-    nib, rungs, scales = out if out is not None else _outs(torch, rows, n, w.device)
+    rows, n = _sweep_inputs(w, u, hw, tab, lost)
+    nib, rungs, scales = _outs(torch, rows, n, w.device, out)
     code = lib.gptq_q4tp_sweep_noalloc(_ptr(w), rows, n, _ptr(u), _ptr(hw), _ptr(tab), _ptr(lost),
                                        _ptr(nib), _ptr(rungs), _ptr(scales), _stream(torch, stream))
     _check("gptq_q4tp_sweep_noalloc", code)
     return nib, rungs, scales
+
+
+def _group_inputs(tile, ublk, hw, tab, lost=None):
+    """rows after checking tile [rows, 32], ublk 32*32, hw 32, tab rows*32, lost rows*2."""
+    rows, c = _matrix(tile, "tile")
+    if c != 32:
+        raise ValueError(f"tile must be [rows, 32], got shape {tuple(tile.shape)}")
+    dev = tile.device
+    _need(ublk, "ublk", numel=32 * 32, device=dev)
+    _need(hw, "hw", numel=32, device=dev)
+    _need(tab, "tab", numel=rows * 32, device=dev)
+    if lost is not None:
+        _need(lost, "lost", numel=rows * 2, device=dev)
+    return rows
 
 
 def q4tp_group(tile, ublk, hw, tab, lost):
@@ -200,7 +275,7 @@ def q4tp_group(tile, ublk, hw, tab, lost):
     import torch
 
     lib = load()
-    rows = tile.shape[0]
+    rows = _group_inputs(tile, ublk, hw, tab, lost)
     dev = tile.device
     nib = torch.empty(rows, 16, dtype=torch.uint8, device=dev)
     rungs = torch.empty(rows, dtype=torch.uint8, device=dev)
@@ -218,11 +293,10 @@ def quantize_group(h_packed, n, w, lam=0.01, ws=None, want_u=True, stream=None, 
     import torch
 
     lib = load()
-    _cuda_f32(h_packed, "h_packed")
-    _cuda_f32(w, "w")
-    rows = w.shape[0]
+    rows, _ = _matrix(w, n=n)
     dev = w.device
-    nib, rungs, scales = out if out is not None else _outs(torch, rows, n, dev)
+    _packed(h_packed, n, dev)
+    nib, rungs, scales = _outs(torch, rows, n, dev, out)
     tab = torch.empty(rows, 32, dtype=torch.float32, device=dev)
     lost = torch.empty(rows, 2, dtype=torch.float32, device=dev)
     u = torch.empty(n, n, dtype=torch.float32, device=dev) if want_u else None
@@ -230,6 +304,7 @@ def quantize_group(h_packed, n, w, lam=0.01, ws=None, want_u=True, stream=None, 
     hd = torch.empty(n, dtype=torch.float32, device=dev)
     if ws is None:
         ws = workspace(lib.gptq_group_workspace_bytes(rows, n), dev)
+    _ws(ws, dev)
     lam_used = ctypes.c_double(0.0)
     code = lib.gptq_quantize_group(_ptr(h_packed), n, float(lam), _ptr(w), rows, _ptr(nib),
                                    _ptr(rungs), _ptr(scales), _ptr(tab), _ptr(lost), _ptr(u),
@@ -278,11 +353,11 @@ def gram_add(h_packed, x, ws=None, stream=None):
     import torch
 
     lib = load()
-    _cuda_f32(h_packed, "h_packed")
-    _cuda_f32(x, "x")
-    t, n = x.shape
+    t, n = _matrix(x, "x")
+    _packed(h_packed, n, x.device)
     if ws is None:
         ws = workspace(lib.gptq_gram_workspace_bytes(n), x.device)
+    _ws(ws, x.device)
     code = lib.gptq_gram_add(_ptr(h_packed), n, _ptr(x), t, _ptr(ws), ws.numel(), _stream(torch, stream))
     _check("gptq_gram_add", code)
     return h_packed
@@ -292,7 +367,7 @@ def act_order_perm(hdiag):
     import torch
 
     lib = load()
-    _cuda_f32(hdiag, "hdiag")
+    _need(hdiag, "hdiag")
     n = hdiag.numel()
     perm = torch.empty(n, dtype=torch.int32, device=hdiag.device)
     _check("gptq_act_order_perm", lib.gptq_act_order_perm(_ptr(hdiag), n, _ptr(perm), _stream(torch)))
@@ -304,7 +379,9 @@ def fold_permuted(h_packed, n, perm, lam=0.01):
     import torch
 
     lib = load()
+    _packed(h_packed, n)
     dev = h_packed.device
+    _need(perm, "perm", dtype=torch.int32, numel=n, device=dev)
     u = torch.empty(n, n, dtype=torch.float32, device=dev)
     d = torch.empty(n, dtype=torch.float32, device=dev)
     hd = torch.empty(n, dtype=torch.float32, device=dev)
@@ -320,7 +397,9 @@ def static_rungs(w, tab, lost):
     import torch
 
     lib = load()
-    rows, n = w.shape
+    rows, n = _matrix(w)
+    _need(tab, "tab", numel=rows * 32, device=w.device)
+    _need(lost, "lost", numel=rows * 2, device=w.device)
     rungs = torch.empty(rows * (n // 32), dtype=torch.uint8, device=w.device)
     scales = torch.empty(rows * (n // 32), dtype=torch.float32, device=w.device)
     code = lib.gptq_static_rungs(_ptr(w), rows, n, _ptr(tab), _ptr(lost), _ptr(rungs), _ptr(scales),
@@ -333,7 +412,12 @@ def q4tp_sweep_act_order(w, u, perm, tab, rungs):
     import torch
 
     lib = load()
-    rows, n = w.shape
+    rows, n = _matrix(w)
+    dev = w.device
+    _need(u, "u", numel=n * n, device=dev)
+    _need(perm, "perm", dtype=torch.int32, numel=n, device=dev)
+    _need(tab, "tab", numel=rows * 32, device=dev)
+    _need(rungs, "rungs", dtype=torch.uint8, numel=rows * (n // 32), device=dev)
     nib = torch.empty(rows * n // 2, dtype=torch.uint8, device=w.device)
     ws = workspace(lib.gptq_sweep_act_order_workspace_bytes(rows, n), w.device)
     code = lib.gptq_q4tp_sweep_act_order(_ptr(w), rows, n, _ptr(u), _ptr(perm), _ptr(tab), _ptr(rungs),
@@ -346,15 +430,15 @@ def quantize_group_act_order(h_packed, n, w, lam=0.01, ws=None, want_u=True, str
     import torch
 
     lib = load()
-    _cuda_f32(h_packed, "h_packed")
-    _cuda_f32(w, "w")
-    rows = w.shape[0]
+    rows, _ = _matrix(w, n=n)
     dev = w.device
+    _packed(h_packed, n, dev)
     nib, rungs, scales = _outs(torch, rows, n, dev)
     perm = torch.empty(n, dtype=torch.int32, device=dev)
     u = torch.empty(n, n, dtype=torch.float32, device=dev) if want_u else None
     if ws is None:
         ws = workspace(lib.gptq_group_act_order_workspace_bytes(rows, n), dev)
+    _ws(ws, dev)
     lam_used = ctypes.c_double(0.0)
     code = lib.gptq_quantize_group_act_order(_ptr(h_packed), n, float(lam), _ptr(w), rows, _ptr(nib),
                                              _ptr(rungs), _ptr(scales), _ptr(perm), _ptr(u),
@@ -373,9 +457,8 @@ def q2tp_place(w, hw, want_gscale=False):
     import torch
 
     lib = load()
-    _cuda_f32(w, "w")
-    _cuda_f32(hw, "hw")
-    rows, n = w.shape
+    rows, n = _matrix(w)
+    _need(hw, "hw", numel=n, device=w.device)
     tab = torch.empty(rows, 32, dtype=torch.float32, device=w.device)
     lost = torch.empty(rows, 2, dtype=torch.float32, device=w.device)
     gs = torch.empty(rows, n // 32, dtype=torch.float32, device=w.device) if want_gscale else None
@@ -389,7 +472,7 @@ def q2tp_group(tile, ublk, hw, tab):
     import torch
 
     lib = load()
-    rows = tile.shape[0]
+    rows = _group_inputs(tile, ublk, hw, tab)
     dev = tile.device
     codes = torch.empty(rows, 8, dtype=torch.uint8, device=dev)
     rungs = torch.empty(rows, dtype=torch.uint8, device=dev)
@@ -401,8 +484,12 @@ def q2tp_group(tile, ublk, hw, tab):
     return codes, rungs, scales, e
 
 
-def _outs_q2(torch, rows, n, dev):
+def _outs_q2(torch, rows, n, dev, out=None):
     gpr = n // 32
+    if out is not None:
+        _check_outs(out, ("codes", "rungs", "scales"), (rows * n // 4, rows * gpr, rows * gpr),
+                    (torch.uint8, torch.uint8, torch.float32), dev)
+        return out
     codes = torch.empty(rows * n // 4, dtype=torch.uint8, device=dev)
     rungs = torch.empty(rows * gpr, dtype=torch.uint8, device=dev)
     scales = torch.empty(rows * gpr, dtype=torch.float32, device=dev)
@@ -414,12 +501,11 @@ def q2tp_sweep(w, u, hw, tab, ws=None, out=None, stream=None):
     import torch
 
     lib = load()
-    for t, nm in ((w, "w"), (u, "u"), (hw, "hw"), (tab, "tab")):
-        _cuda_f32(t, nm)
-    rows, n = w.shape
-    codes, rungs, scales = out if out is not None else _outs_q2(torch, rows, n, w.device)
+    rows, n = _sweep_inputs(w, u, hw, tab)
+    codes, rungs, scales = _outs_q2(torch, rows, n, w.device, out)
     if ws is None:
         ws = workspace(lib.gptq_sweep_workspace_bytes(rows, n), w.device)
+    _ws(ws, w.device)
     code = lib.gptq_q2tp_sweep(_ptr(w), rows, n, _ptr(u), _ptr(hw), _ptr(tab), _ptr(codes),
                                _ptr(rungs), _ptr(scales), _ptr(ws), ws.numel(), _stream(torch, stream))
     _check("gptq_q2tp_sweep", code)
@@ -432,11 +518,10 @@ def quantize_group_q2tp(h_packed, n, w, lam=0.01, ws=None, want_u=True, stream=N
     import torch
 
     lib = load()
-    _cuda_f32(h_packed, "h_packed")
-    _cuda_f32(w, "w")
-    rows = w.shape[0]
+    rows, _ = _matrix(w, n=n)
     dev = w.device
-    codes, rungs, scales = out if out is not None else _outs_q2(torch, rows, n, dev)
+    _packed(h_packed, n, dev)
+    codes, rungs, scales = _outs_q2(torch, rows, n, dev, out)
     tab = torch.empty(rows, 32, dtype=torch.float32, device=dev)
     lost = torch.empty(rows, 2, dtype=torch.float32, device=dev)
     u = torch.empty(n, n, dtype=torch.float32, device=dev) if want_u else None
@@ -444,6 +529,7 @@ def quantize_group_q2tp(h_packed, n, w, lam=0.01, ws=None, want_u=True, stream=N
     hd = torch.empty(n, dtype=torch.float32, device=dev)
     if ws is None:
         ws = workspace(lib.gptq_group_workspace_bytes(rows, n), dev)
+    _ws(ws, dev)
     lam_used = ctypes.c_double(0.0)
     code = lib.gptq_quantize_group_q2tp(_ptr(h_packed), n, float(lam), _ptr(w), rows, _ptr(codes),
                                         _ptr(rungs), _ptr(scales), _ptr(tab), _ptr(lost), _ptr(u),
@@ -460,12 +546,20 @@ def debias(bits, w, h_packed, codes, rungs, tab, lost, scales, ws=None, want_num
     import torch
 
     lib = load()
-    _cuda_f32(w, "w")
-    _cuda_f32(h_packed, "h_packed")
-    rows, n = w.shape
+    rows, n = _matrix(w)
+    dev = w.device
+    _packed(h_packed, n, dev)
+    if int(bits) in (2, 4):
+        gpr = n // 32
+        _need(codes, "codes", dtype=torch.uint8, numel=rows * n * int(bits) // 8, device=dev)
+        _need(rungs, "rungs", dtype=torch.uint8, numel=rows * gpr, device=dev)
+        _need(tab, "tab", numel=rows * 32, device=dev)
+        _need(lost, "lost", numel=rows * 2, device=dev)
+        _need(scales, "scales", numel=rows * gpr, device=dev)
     nd = torch.empty(rows, 2, dtype=torch.float64, device=w.device) if want_num_den else None
     if ws is None:
         ws = workspace(lib.gptq_debias_workspace_bytes(rows, n), w.device)
+    _ws(ws, dev)
     code = lib.gptq_debias(int(bits), _ptr(w), rows, n, _ptr(h_packed), _ptr(codes), _ptr(rungs), _ptr(tab),
                            _ptr(lost), _ptr(scales), _ptr(nd), _ptr(ws), ws.numel(), _stream(torch, stream))
     _check("gptq_debias", code)

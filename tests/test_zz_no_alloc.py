@@ -52,7 +52,7 @@ def test_noalloc_sweep_rejects_oversize(lib):
     rows, n = 4096, 24576
     assert rows * 2048 + n * 2048 > limit
     w = torch.zeros(rows, n, dtype=torch.float32, device="cuda")
-    u = torch.zeros(1, 4, dtype=torch.float32, device="cuda")  # never read: rejected first
+    u = torch.empty(n, n, dtype=torch.float32, device="cuda")  # never read: the library refuses first
     hw = torch.zeros(n, dtype=torch.float32, device="cuda")
     tab = torch.zeros(rows, 32, dtype=torch.float32, device="cuda")
     lost = torch.zeros(rows, 2, dtype=torch.float32, device="cuda")
