@@ -443,8 +443,18 @@ __global__ void __launch_bounds__(SWEEP_THREADS) k_sweep_block(
       const float sj = ACT ? sc[j] : s;
       const float t1 = sj > 0.f ? __fdiv_rn(x, sj) : 0.f;
       if (j > 0) {
+        // w_t -= e_{j-1} U_{j-1,t}, two columns per packed instruction:
+        // w + (-e) U is w - e U bit for bit (one rounding each, as before).
+        const float* ur = Ug + (j - 1) * SB;
+        if ((j + 1) & 1) w[j + 1] = __fsub_rn(w[j + 1], __fmul_rn(eprev, ur[j + 1]));
+        const float2 ne = make_float2(-eprev, -eprev);
 #pragma unroll
-        for (int t = j + 1; t < GROUP; ++t) w[t] = __fsub_rn(w[t], __fmul_rn(eprev, Ug[(j - 1) * SB + t]));
+        for (int t = (j + 2) & ~1; t + 1 < GROUP; t += 2) {
+          const float2 u2 = *reinterpret_cast<const float2*>(ur + t);
+          const float2 w2 = __fadd2_rn(make_float2(w[t], w[t + 1]), __fmul2_rn(ne, u2));
+          w[t] = w2.x;
+          w[t + 1] = w2.y;
+        }
       }
       float q, lev;
       if (Q2) {
