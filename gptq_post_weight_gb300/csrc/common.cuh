@@ -1,4 +1,10 @@
 // Shared definitions for the GB300 GPTQ fold + q4tp sweep kernels.
+//
+// Citations in these sources: [fold page] = cortiq-engine
+// src/gpu_wgpu/gptq_dev.rs (module doc steps 1-5, WGSL kernels, host fns
+// fold / fold_inner / sweep); [host page] = cortiq-cli src/gptq.rs (host
+// fold gptq_fold_operator_par, host sweeps gptq_quantize_q4tp / _q2tp, the
+// debias and calibration functions).
 #pragma once
 
 #include <cuda.h>
