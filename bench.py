@@ -62,8 +62,8 @@ def workload_desc(cfg, codec="q4tp"):
 
 
 def fold_gemm_flops(n, NB=128, part="all"):
-    """Useful flops of the fold's update GEMM launches over one fold, on the
-    padded size, following the library's schedule: steps in pairs (a thin
+    """Algorithmic flops of the fold's update GEMM launches over one fold, on
+    the padded size, following the library's schedule: steps in pairs (a thin
     K = NB strip update of the next block column between them, then one
     K = 2 NB trailing update), a last unpaired step with K = NB.
     part: "trailing" (the K = 2 NB and unpaired updates, kind fold_gemm),
@@ -77,7 +77,11 @@ def fold_gemm_flops(n, NB=128, part="all"):
             strip += 2 * NB * ((N - k1 - NB) * NB + NB * (NB + 1) // 2)  # SYRK strip
             strip += 2 * NB * k1 * NB  # inverse strip
             m = N - s1
-            trail += 2 * (2 * NB) * (m * (m + 1) // 2) + 2 * (2 * NB) * s1 * m
+            # SYRK of the pair, then the inverse rectangle: step k's panel meets
+            # the rows c < k1 only (its rows of block k1 are zero: X is lower
+            # triangular, so the launch multiplies them but they are no work of
+            # the method), step k1's the rows c < s1.
+            trail += 2 * (2 * NB) * (m * (m + 1) // 2) + 2 * NB * (k1 + s1) * m
             k = s1
         else:
             s0 = k + NB

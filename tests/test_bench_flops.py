@@ -1,0 +1,48 @@
+"""The bench's algorithmic flop counts (the roofline's numerator) against an
+independent per-entry count (CPU only).
+
+Blocked right-looking Cholesky: entry (i, j) of the lower triangle receives,
+through update GEMMs, one multiply-add per column of every block before j's
+own block (its own block's columns are the diagonal and panel kernels' work).
+Inverse accumulated alongside: entry (c, i), c < i, receives NB multiply-adds
+from every step k with c < k + NB <= i.  However the schedule groups the steps
+(pairs with a thin strip update between them), the sums must agree exactly.
+The sweep: column t of W receives one multiply-add per row for every column of
+the blocks before t's block.
+"""
+import numpy as np
+import pytest
+
+import bench
+
+
+def per_entry_fold(n, NB=128):
+    N = (n + NB - 1) // NB * NB
+    blk = np.arange(N, dtype=np.int64) // NB
+    chol = int(((N - np.arange(N)) * NB * blk).sum())
+    # sum over c < i of (blk[i] - blk[c]) = i * blk[i] - sum_{c<i} blk[c]
+    before = np.concatenate([[0], np.cumsum(blk)[:-1]])
+    inv = int((NB * (np.arange(N) * blk - before)).sum())
+    return 2 * (chol + inv)
+
+
+@pytest.mark.parametrize("n", [128, 256, 384, 640, 1000, 4096, 17408])
+def test_fold_update_flops_per_entry(n):
+    assert bench.fold_gemm_flops(n, part="all") == per_entry_fold(n)
+    assert bench.fold_gemm_flops(n, part="trailing") + bench.fold_gemm_flops(n, part="strip") == per_entry_fold(n)
+
+
+def test_fold_update_flops_near_textbook():
+    # Cholesky n^3/3 + inverse n^3/3; the update GEMMs carry all but the
+    # O(n^2 NB) diagonal-block and panel work.
+    n = 17408
+    got = bench.fold_gemm_flops(n, part="all")
+    assert 0.99 < got / (2 * n ** 3 / 3) < 1.0
+
+
+@pytest.mark.parametrize("rows,n", [(5, 128), (7, 544), (5120, 17408)])
+def test_sweep_update_flops_per_entry(rows, n):
+    SB = 128
+    t = np.arange(n, dtype=np.int64)
+    want = 2 * rows * int((SB * (t // SB)).sum())
+    assert bench.sweep_gemm_flops(rows, n) == want
