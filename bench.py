@@ -100,6 +100,35 @@ def sweep_gemm_flops(rows, n, SB=128):
     return tot
 
 
+def hbm_report(per_kind, n, rows, codec="q4tp", peak_gbs=None, NB=128, SB=128):
+    """Achieved HBM rate of the sequential, memory-facing kernels: their
+    algorithmic bytes per group over their measured time per group (kinds
+    absent from ``per_kind`` are left out)."""
+    N = (n + NB - 1) // NB * NB
+    gpr = n // 32
+    codes = rows * n // (4 if codec == "q2tp" else 2)
+    tabs = rows * 34 * 4
+    parts = {
+        "build": ("a2 builder: read the packed H, write the N x N working matrix", n * (n + 1) // 2 * 4 + N * N * 4),
+        "trsm": ("a6 U = P X P D^-1 fused into the panel products' store: U's upper triangle written "
+                 "(the kernel itself is bound by its FP32 triangular products)", n * (n + 1) // 2 * 4),
+        "ladder": ("a7 ladder: read W, write tab and lost", rows * n * 4 + tabs),
+        "place": ("q2tp placement: read W, write tab and lost", rows * n * 4 + tabs),
+        "copy": ("dead-column zeroing: read and write W", 2 * rows * n * 4),
+        "sweep_block": ("a8, a9, a11: read W and U's diagonal blocks, write codes, rungs and scales "
+                        "(latency-bound rounding chain)", rows * n * 4 + n * SB * 4 + codes + rows * gpr * 5),
+    }
+    out = {}
+    for kind, (what, nbytes) in parts.items():
+        ms = per_kind.get(kind, {}).get("ms_per_step")
+        if not ms:
+            continue
+        gbs = nbytes / (ms / 1e3) / 1e9
+        out[kind] = {"what": what, "bytes_per_group": nbytes, "ms_per_group": ms, "gbs": gbs,
+                     "frac": gbs / peak_gbs if peak_gbs else None}
+    return out
+
+
 class ClockSampler:
     """nvidia-smi clocks, power and throttle reasons sampled every 20 ms;
     only the samples inside [t0, t1] (host clock) count."""
@@ -584,6 +613,8 @@ def main():
                                                      ) / 1e12 if "fold_gemm" in per_kind else None,
             "per_kernel": per_kind,
             "per_kernel_source": "one extra untimed step with every launch bracketed by events",
+            "hbm": {"unit": "GB/s", "peak": pk.get("hbm_gbs"), "peak_source": src,
+                    "kernels": hbm_report(per_kind, n, rows, args.codec, pk.get("hbm_gbs"))},
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": launches,

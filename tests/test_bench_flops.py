@@ -46,3 +46,21 @@ def test_sweep_update_flops_per_entry(rows, n):
     t = np.arange(n, dtype=np.int64)
     want = 2 * rows * int((SB * (t // SB)).sum())
     assert bench.sweep_gemm_flops(rows, n) == want
+
+
+def test_hbm_report_arithmetic():
+    n, rows = 256, 64
+    per_kind = {"build": {"ms_per_step": 0.5, "launches_per_step": 1},
+                "sweep_block": {"ms_per_step": 2.0, "launches_per_step": 2},
+                "fold_gemm": {"ms_per_step": 9.0, "launches_per_step": 1}}
+    rep = bench.hbm_report(per_kind, n, rows, "q4tp", peak_gbs=1000.0)
+    assert set(rep) == {"build", "sweep_block"}  # kinds that did not run are left out
+    b = n * (n + 1) // 2 * 4 + n * n * 4
+    assert rep["build"]["bytes_per_group"] == b
+    assert rep["build"]["gbs"] == pytest.approx(b / 0.5e-3 / 1e9)
+    assert rep["build"]["frac"] == pytest.approx(rep["build"]["gbs"] / 1000.0)
+    sw = rows * n * 4 + n * 128 * 4 + rows * n // 2 + rows * (n // 32) * 5
+    assert rep["sweep_block"]["bytes_per_group"] == sw
+    q2 = bench.hbm_report(per_kind, n, rows, "q2tp", peak_gbs=None)
+    assert q2["sweep_block"]["bytes_per_group"] == sw - rows * n // 2 + rows * n // 4
+    assert q2["build"]["frac"] is None
