@@ -229,7 +229,8 @@ def cpu_baseline_sample(cfg, n_fold=None, rows_sweep=8, codec="q4tp"):
     t_sweep = time.perf_counter() - t0
     est = t_fold * (cfg.n / n_fold) ** 3 + t_sweep * (cfg.rows / rows_sweep)
     sample = (f"oracle fold at n={n_fold} ({t_fold:.2f} s, x(n/{n_fold})^3) + oracle {codec} ladder and "
-              f"sweep of {rows_sweep} rows at n={cfg.n} ({t_sweep:.2f} s, x{cfg.rows}/{rows_sweep})")
+              f"sweep of {rows_sweep} rows at n={cfg.n} ({t_sweep:.2f} s, x{cfg.rows}/{rows_sweep}); "
+              f"the fold's matrix products in numpy's BLAS/LAPACK on all cores, the sweep's loops on one")
     return est, sample, t_fold + t_sweep
 
 
