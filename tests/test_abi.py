@@ -99,3 +99,40 @@ def test_q2tp_and_debias_argument_errors(clib):
     assert clib.gptq_debias(4, fake, 4, 64, fake, fake, fake, fake, fake, fake, None, ws, 16, None) == 3
     assert clib.gptq_debias_workspace_bytes(5120, 17408) >= 2 * 17408 * 17408 * 4
     assert clib.gptq_debias_workspace_bytes(0, 64) == 0
+
+
+def test_gram_and_act_order_argument_errors(clib):
+    P = ctypes.c_void_p
+    fake = P(1 << 20)
+    mis = P((1 << 20) + 4)
+    ws = P(1 << 21)
+    big = 1 << 40
+    # Gram: shapes, pointers, workspace; an empty window (T = 0) is a no-op.
+    assert clib.gptq_gram_workspace_bytes(0) == 0
+    assert clib.gptq_gram_add(fake, 0, fake, 10, ws, big, None) == 2
+    assert clib.gptq_gram_add(fake, 64, fake, -1, ws, big, None) == 2
+    assert clib.gptq_gram_add(None, 64, fake, 10, ws, big, None) == 1
+    assert clib.gptq_gram_add(fake, 64, None, 10, ws, big, None) == 1
+    assert clib.gptq_gram_add(fake, 64, mis, 10, ws, big, None) == 1
+    assert clib.gptq_gram_add(fake, 64, fake, 10, ws, 16, None) == 3
+    assert clib.gptq_gram_add(fake, 64, None, 0, ws, big, None) == 0
+    # Act order.
+    lam = ctypes.c_double()
+    assert clib.gptq_act_order_perm(fake, 0, fake, None) == 2
+    assert clib.gptq_act_order_perm(None, 64, fake, None) == 1
+    assert clib.gptq_act_order_perm(fake, 64, mis, None) == 1
+    assert clib.gptq_fold_permuted(fake, 64, float("nan"), fake, fake, None, None, ctypes.byref(lam), ws, big,
+                                   None) == 1
+    assert clib.gptq_fold_permuted(fake, 64, 0.01, None, fake, None, None, ctypes.byref(lam), ws, big, None) == 1
+    assert clib.gptq_fold_permuted(fake, 64, 0.01, fake, fake, None, None, ctypes.byref(lam), ws, 16, None) == 3
+    assert clib.gptq_static_rungs(fake, 4, 48, fake, fake, fake, fake, None) == 2
+    assert clib.gptq_static_rungs(fake, 4, 64, fake, fake, None, fake, None) == 1
+    assert clib.gptq_q4tp_sweep_act_order(fake, 0, 64, fake, fake, fake, fake, fake, ws, big, None) == 2
+    assert clib.gptq_q4tp_sweep_act_order(fake, 4, 64, fake, mis, fake, fake, fake, ws, big, None) == 1
+    assert clib.gptq_q4tp_sweep_act_order(fake, 4, 64, fake, fake, fake, fake, fake, ws, 16, None) == 3
+    assert clib.gptq_sweep_act_order_workspace_bytes(0, 64) == 0
+    assert clib.gptq_quantize_group_act_order(fake, 64, 0.01, fake, 4, fake, fake, fake, None, None, None,
+                                              ws, 16, None) == 3
+    assert clib.gptq_quantize_group_act_order(fake, 64, float("inf"), fake, 4, fake, fake, fake, None, None,
+                                              None, ws, big, None) == 1
+    assert clib.gptq_group_act_order_workspace_bytes(4, 0) == 0
