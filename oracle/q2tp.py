@@ -23,7 +23,13 @@ Readings where the pages are silent (the converter functions
   of one piece: for an outer set O,
   ``s_O = (1.5 sum_O h|w| + 0.5 sum_rest h|w|) / (2.25 sum_O h + 0.25 sum_rest h)``.
   The oracle evaluates E at s_O for every "top-k by |w|" set O (k = 0..32)
-  and keeps the smallest E (ties: the smaller s).  A group takes part only
+  and keeps the smallest E.  Ties: the page asks for "the" optimal scale and
+  names no tie-break, while a group can have two exact optima (all |w_t|
+  equal: s = a/1.5 with every weight outer and s = 2a with every weight
+  inner, both E = 0) whose f64 scores differ only by rounding.  So scores
+  within TIE_REL * sum_t h_t w_t^2 of the smallest count as equal (an f64
+  32-term score carries errors near 1e-16 of that sum), and the smallest
+  such s is taken.  A group takes part only
   when some t has ``h_t > 0`` and ``w_t != 0``; otherwise E has no positive
   minimiser and the group is left out of the ladder.
 * ladder -- the layout of the host page's ``q2tp`` params: an f16 pair
@@ -49,6 +55,7 @@ F32 = np.float32
 GROUP = 32
 NRUNG = 32
 LMAX = 30  # rungs 1..LMAX+1
+TIE_REL = 1e-12  # placement: scores this close (relative to sum h w^2) are ties
 Q2_BLOCK = 128  # host page: columns per lazy-update block
 
 
@@ -100,7 +107,8 @@ def place_scale(w, h):
             cands.append(num / den)
     cands = np.array(sorted(set(cands)))
     errs = group_err_f64(w, h, cands)
-    return float(cands[int(np.argmin(errs))])  # first minimum = the smaller s
+    band = errs.min() + TIE_REL * float(np.sum(h * a * a))
+    return float(cands[np.nonzero(errs <= band)[0][0]])  # ascending: the smallest tied s
 
 
 def _f16(x):

@@ -95,14 +95,31 @@ def test_codes_minimise_weighted_error_bruteforce():
 def test_place_scale_equal_magnitudes():
     # |w_t| = a for every t: two scales fit exactly (E = 0), s = a/1.5 (every
     # weight on an outer level) and s = 2a (every weight on an inner level);
-    # the optimum is one of them, whatever the signs and weights.
+    # their f64 scores differ by rounding only, so they tie and the smaller,
+    # a/1.5, is taken, whatever the signs and weights.
     rng = np.random.default_rng(2)
-    for a in (0.3, 1e-3, 17.0):
-        w = a * rng.choice([-1.0, 1.0], 32)
-        h = rng.uniform(0.1, 5, 32)
-        s = o2.place_scale(w, h)
-        assert min(abs(s / (a / 1.5) - 1), abs(s / (2 * a) - 1)) < 1e-12
-        assert o2.group_err_f64(w, h, s)[0] <= 1e-28 * a * a
+    for a in (0.3, 1e-3, 17.0, 0.05):
+        for trial in range(5):
+            w = a * rng.choice([-1.0, 1.0], 32)
+            h = rng.uniform(0.1, 5, 32)
+            s = o2.place_scale(w, h)
+            assert abs(s / (a / 1.5) - 1) < 1e-12
+            assert o2.group_err_f64(w, h, s)[0] <= 1e-28 * a * a
+            assert o2.group_err_f64(w, h, 2 * a)[0] <= 1e-28 * a * a
+
+
+def test_place_scale_tie_band():
+    # Two pieces whose exact scores differ by far more than the band are not
+    # ties: shrinking the outer weights a little makes the all-inner fit
+    # (s = 2 * median-like scale) strictly better or worse, and the smaller
+    # score wins whichever scale it has.
+    w = np.full(32, 0.05)
+    w[:16] = 0.05 * (1 - 1e-3)
+    h = np.ones(32)
+    s = o2.place_scale(w, h)
+    cands = np.linspace(0.01, 0.15, 20001)
+    e = o2.group_err_f64(w, h, cands)
+    assert o2.group_err_f64(w, h, s)[0] <= e.min() + 1e-15
 
 
 def test_place_scale_single_spike_closed_form():
