@@ -14,7 +14,8 @@
 // for an outer set O = the k largest |w| (k = 0..32).  The kernel scores the
 // pieces in f32 with compensated sums; when a group's two best f32 scores
 // are within their f32 error of each other both are scored again in f64
-// (ties: the smaller scale), and the scales that set the row's ladder (its
+// (scores within 1e-12 sum h w^2 of each other are a tie: the smaller
+// scale), and the scales that set the row's ladder (its
 // extremes) are recomputed in f64.  A group takes part only if some
 // channel has h > 0 and w != 0.  The row's ladder: lo = f16(log2 min s*),
 // step = f16(max(0, (log2 max s* - lo) / 30)) (0 if min == max), rung 0 = 0,
@@ -28,6 +29,11 @@ namespace gq {
 namespace {
 
 constexpr int PLACE_THREADS = 128;
+// Two pieces' f64 scores closer than this times sum_t h_t w_t^2 count as a
+// tie (an f64 score of 32 terms is exact to about 1e-16 of that sum); the
+// smaller scale is taken.  A group whose weights all share one magnitude a
+// has two exact optima, a/1.5 and 2a, that only rounding tells apart.
+constexpr double PLACE_TIE_REL = 1e-12;
 
 __device__ __forceinline__ float hclip(float h) { return h > 0.f ? h : 0.f; }
 
@@ -228,7 +234,10 @@ __global__ void __launch_bounds__(PLACE_THREADS, 3) k_q2tp_place(const float* __
       const float a = fabsf(wr[g * GROUP + lane]), h = hclip(hw[g * GROUP + lane]);
       const double s1 = warp_scale_f64(a, h, thr1s[g]), s2 = warp_scale_f64(a, h, thr2s[g]);
       const double e1 = warp_err_f64(a, h, s1), e2 = warp_err_f64(a, h, s2);
-      const bool take2 = e2 < e1 || (e2 == e1 && s2 < s1);
+      // Scores within PLACE_TIE_REL * sum h w^2 are equal: the smaller scale.
+      const double band = PLACE_TIE_REL * warp_sum_f64((double)h * (double)a * (double)a);
+      const bool tied = fabs(e1 - e2) <= band;
+      const bool take2 = tied ? s2 < s1 : e2 < e1;
       __syncwarp();
       if (lane == 0) {
         gs[g] = (float)(take2 ? s2 : s1);

@@ -150,12 +150,13 @@ gptq_status gptq_q4tp_group(const float* tile, int rows, const float* ublk, cons
 
 /*
  * gptq_q4tp_sweep_noalloc -- gptq_q4tp_sweep for callers that cannot
- * allocate device memory (no cudaMalloc, no allocator of their own, no
- * workspace to lend): for example code that runs inside a stream that is
- * being captured, where an allocation would break the capture, or a plugin
- * whose host framework owns all device memory and hands it only the input and
- * output buffers.  The pages have no counterpart; it is a packaging of the
- * same sweep.
+ * allocate device memory and have no workspace to lend.  Two kinds of caller
+ * are meant: a plugin or custom operator inside a host framework that owns
+ * every device allocation (its pool or budget is not reachable from here) and
+ * hands the plugin only the input and output buffers; and a latency-bound
+ * caller that must keep cudaMalloc off its hot path, because cudaMalloc can
+ * synchronise the whole device and stall the caller's other streams.  The
+ * pages have no counterpart; it is a packaging of the same sweep.
  *
  * Arguments, layouts and results are those of gptq_q4tp_sweep, without
  * ws/ws_bytes.  Scratch lives instead in one file-scope device array of
@@ -163,17 +164,21 @@ gptq_status gptq_q4tp_group(const float* tile, int rows, const float* ublk, cons
  * library holds until the process exits.  It fits shapes with
  * rows*2048 + n*2048 bytes (plus slack) <= that size (about rows + n <= 24575,
  * e.g. 5120 rows x 17408 channels); larger shapes return GPTQ_ERR_NOMEM
- * before any work.  Where the array also holds gptq_sweep_workspace_bytes,
- * the result is the workspace call's bit for bit; otherwise it runs pairs of
- * blocks per update (same mathematics, different f32 summation order).  The
- * call allocates nothing.
+ * before any work.  Where the array also holds gptq_sweep_workspace_bytes
+ * (about rows + n <= 12287) the result is the workspace call's bit for bit;
+ * otherwise it runs pairs of blocks per update (same mathematics, different
+ * f32 summation order), as gptq_q4tp_sweep does with a workspace of half
+ * that size.  The call calls no cudaMalloc, cudaFree or allocating library
+ * routine.
  *
- * The first call on a device looks up the array's device address (once per
- * device, with that device current); make that first call before any stream
- * capture.  All calls share the one array and it keeps the previous call's
- * contents (everything that must start at zero is cleared by each call), so
- * calls whose work overlaps on the GPU -- on different streams, or from
- * different host threads -- race on it: serialize them.
+ * Set-up: the first call on a device (with that device current) looks up
+ * the array's device address with cudaGetSymbolAddress and keeps it for that
+ * device's context; after a device reset the next call looks it up again.
+ * Make the first call on each device before any stream capture begins.  All
+ * calls share the one array and it keeps the previous call's contents
+ * (everything that must start at zero is cleared by each call), so calls
+ * whose work overlaps on the GPU -- on different streams, or from different
+ * host threads -- race on it: serialise them.
  */
 #define GPTQ_SWEEP_NOALLOC_SCRATCH_BYTES (48u << 20)
 gptq_status gptq_q4tp_sweep_noalloc(float* W, int rows, int n, const float* U, const float* hw,
@@ -191,7 +196,8 @@ gptq_status gptq_q4tp_sweep_noalloc(float* W, int rows, int n, const float* U, c
  * Reading implemented: each group's scale s*_g is the exact minimiser over
  * s > 0 of sum_t h_t (w_t - (q2_level(w_t/s + 1.5) - 1.5) s)^2 with h = hw
  * clipped at 0 (found among the 33 stationary points of its quadratic
- * pieces, winner recomputed in f64); groups with no channel where h > 0 and
+ * pieces, winner recomputed in f64; two scores within 1e-12 * sum h w^2 of
+ * each other are a tie, taken by the smaller scale); groups with no channel where h > 0 and
  * w != 0 are left out.  lo = f16(log2 min s*), step = f16(max(0, (log2 max
  * s* - lo)/30)) (0 if min == max), tab[0] = 0, tab[c] = f32(2^(lo + (c-1)
  * step)) for c = 1..31; a row with no group left gets zeros.
@@ -386,6 +392,19 @@ gptq_status gptq_gram_add(float* H_packed, int n, const float* X, int T, void* w
  */
 long long gptq_launch_count(void);
 int gptq_kernel_kinds(void);
+/*
+ * gptq_test_set_wait -- test hook for the bounded device waits (the pages
+ * have no counterpart: their device path reports a failed pivot through a
+ * flag and never waits on another agent).  Every wait inside the
+ * tensor-core kernels gives up after wait_ns of device time (0 = the default,
+ * 2 s; at most 10 s, else GPTQ_ERR_ARG), stops issuing, drains what it
+ * started, frees its tensor memory and sets the status that the calls report
+ * as GPTQ_ERR_TIMEOUT.  no_loads = 1 makes the GEMM producers issue no loads
+ * at all, so that those waits run out on purpose; no_loads = 0 restores
+ * normal work.  Applies to launches made after the call, from any thread;
+ * not meant to change while calls are in flight.
+ */
+gptq_status gptq_test_set_wait(unsigned long long wait_ns, int no_loads);
 const char* gptq_kernel_kind_name(int kind);
 void gptq_profile_select(unsigned kind_mask);
 gptq_status gptq_profile_start(int max_launches);
