@@ -51,6 +51,7 @@ SIGNATURES = {
     "gptq_profile_select": (None, [ctypes.c_uint]),
     "gptq_profile_start": (_I, [_I]),
     "gptq_profile_stop": (_I, [_P, _P, _I]),
+    "gptq_test_set_wait": (_I, [ctypes.c_ulonglong, _I]),
 }
 
 
@@ -313,6 +314,12 @@ def quantize_group(h_packed, n, w, lam=0.01, ws=None, want_u=True, stream=None, 
     _check("gptq_quantize_group", code)
     return dict(nibbles=nib, rungs=rungs, scales=scales, tab=tab, lost=lost, u=u, d=d, hdiag=hd,
                 lam=lam_used.value)
+
+
+def test_set_wait(wait_ns: int = 0, no_loads: bool = False):
+    """gptq_test_set_wait: the device-wait limit in ns (0 = the default 2 s)
+    and the test hook that makes the GEMM producers issue no loads."""
+    _check("gptq_test_set_wait", load().gptq_test_set_wait(int(wait_ns), 1 if no_loads else 0))
 
 
 def launch_count() -> int:

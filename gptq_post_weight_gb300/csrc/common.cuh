@@ -12,6 +12,8 @@
 #include <stdint.h>
 #include <stddef.h>
 
+#include <mutex>
+
 #include "../../include/gptq_fold.h"
 
 namespace gq {
@@ -64,6 +66,46 @@ inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Streaming multiprocessors of the current device (queried once).
 int num_sms();
+
+// Limit of every bounded device wait (globaltimer ns) and a test hook:
+// with no_loads set, the GEMM producers issue no loads, so the consumers'
+// waits run out and the launch reports a timeout (status bit 1) without any
+// fault.  wait_cfg() is the current setting (default: 2 s, loads issued),
+// changed only by gptq_test_set_wait.
+struct WaitCfg {
+  unsigned long long ns;
+  int no_loads;
+};
+WaitCfg wait_cfg();
+
+// The calling thread's current CUDA context (driver handle), or null when
+// none can be had.  A device reset ends a context; the next one differs.
+CUcontext current_context();
+
+// Set-up that must run once per device and context (kernel attributes,
+// device symbol addresses): run() calls `f` with the device current, the
+// first time it sees the calling thread's (device, context), and again
+// after that device's context has changed; concurrent first calls from
+// several host threads serialise on the mutex.  A failed `f` is retried on
+// the next call.
+struct DeviceOnce {
+  static constexpr int kMaxDevices = 64;
+  std::mutex mu;
+  CUcontext ctx[kMaxDevices] = {};
+  template <class F>
+  gptq_status run(F&& f) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GPTQ_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(mu);
+    const CUcontext cur = current_context();
+    if (cur != nullptr && ctx[dev] == cur) return GPTQ_OK;
+    const gptq_status st = f(dev);
+    // `f` made the runtime bind the device's context to this thread, if it
+    // was not yet; a null context is simply looked up again next time.
+    if (st == GPTQ_OK) ctx[dev] = current_context();
+    return st;
+  }
+};
 
 // Bump allocator over the caller's workspace (256-byte aligned pieces).
 struct Carve {

@@ -396,12 +396,12 @@ constexpr int POTRF_SMEM = POTRF_SMEM_BYTES;
 constexpr int APPLY_SMEM = (NB * NB + 2 * APPLY_ROWS * LV) * 4;
 
 static gptq_status init_attrs() {
-  static bool done = false;
-  if (done) return GPTQ_OK;
-  GQ_CUDA(cudaFuncSetAttribute(k_potrf, cudaFuncAttributeMaxDynamicSharedMemorySize, POTRF_SMEM));
-  GQ_CUDA(cudaFuncSetAttribute(k_apply, cudaFuncAttributeMaxDynamicSharedMemorySize, APPLY_SMEM));
-  done = true;
-  return GPTQ_OK;
+  static DeviceOnce once;
+  return once.run([](int) -> gptq_status {
+    GQ_CUDA(cudaFuncSetAttribute(k_potrf, cudaFuncAttributeMaxDynamicSharedMemorySize, POTRF_SMEM));
+    GQ_CUDA(cudaFuncSetAttribute(k_apply, cudaFuncAttributeMaxDynamicSharedMemorySize, APPLY_SMEM));
+    return GPTQ_OK;
+  });
 }
 
 // One factorisation attempt at damping lam: build, interleaved Cholesky +

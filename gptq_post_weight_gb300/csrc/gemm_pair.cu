@@ -72,7 +72,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
     k_gemm_pair(const __grid_constant__ CUtensorMap m0, const __grid_constant__ CUtensorMap m1,
                 const __grid_constant__ CUtensorMap m2, const __grid_constant__ CUtensorMap m3,
                 const __grid_constant__ CUtensorMap cmap, PJob j0, PJob j1, int K, int kseg,
-                const unsigned* flag, unsigned* status, FusedPotrf fp) {
+                const unsigned* flag, unsigned* status, FusedPotrf fp, WaitCfg wc) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   __shared__ __align__(8) uint64_t full[PSTAGES], empty[PSTAGES], tfull[2], tempty[2], drain;
@@ -123,7 +123,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
       const CUtensorMap* maps[4] = {&m0, &m1, &m2, &m3};
       int stage = 0;
       uint32_t phase = 0;
-      for (int t = t0; t < total && !*abort; t += tstride) {
+      // wc.no_loads (a test hook): issue nothing, so that the waits of the
+      // MMA thread and of both epilogues run out and report a timeout.
+      for (int t = t0; t < total && !*abort && !wc.no_loads; t += tstride) {
         const bool second = t >= j0.ntiles;
         const PJob& J = second ? j1 : j0;
         int ti, tj;
@@ -135,7 +137,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
         const CUtensorMap* bhi = maps[J.j.b_map];
         const CUtensorMap* blo = maps[J.j.b_map + 1];
         for (int c = 0; c < nk; ++c) {
-          if (!mbar_wait_cl(&empty[stage], phase ^ 1u, abort)) break;
+          if (!mbar_wait_cl(&empty[stage], phase ^ 1u, abort, wc.ns)) break;
           const uint32_t sb = smem_u32(smem + stage * P_STAGE);
           const uint32_t fb = mapa_u32(smem_u32(&full[stage]), 0);
           if (rank == 0) mbar_expect_tx(&full[stage], 2 * P_STAGE);
@@ -157,7 +159,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
       for (int t = t0; t < total && !*abort; t += tstride) {
         bool ok = true;
         for (int sg = 0; sg < nseg && ok; ++sg) {
-          if (!mbar_wait_cl(&tempty[acc], aphase ^ 1u, abort)) {
+          if (!mbar_wait_cl(&tempty[acc], aphase ^ 1u, abort, wc.ns)) {
             ok = false;
             break;
           }
@@ -165,7 +167,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
           const uint32_t d = tmem + (uint32_t)(acc * PN);
           const int cend = (sg + 1) * segc < nk ? (sg + 1) * segc : nk;
           for (int c = sg * segc; c < cend; ++c) {
-            if (!mbar_wait_cl(&full[stage], phase, abort)) {
+            if (!mbar_wait_cl(&full[stage], phase, abort, wc.ns)) {
               ok = false;
               break;
             }
@@ -196,9 +198,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
       }
       // Every MMA issued has completed once `drain` flips.
       mma_commit_pair(&drain);
-      if (!mbar_wait_cl(&drain, 0u, abort)) {
+      if (!mbar_wait_cl(&drain, 0u, abort, wc.ns)) {
         const uint64_t tt = globaltimer();
-        while (!mbar_try_wait_cl(&drain, 0u) && globaltimer() - tt < WAIT_NS) {
+        while (!mbar_try_wait_cl(&drain, 0u) && globaltimer() - tt < wc.ns) {
         }
       }
     }
@@ -213,7 +215,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
     for (int w = t0 * nseg; go && w < total * nseg;
          w += (w % nseg == nseg - 1) ? (tstride - 1) * nseg + 1 : 1) {
       const int t = w / nseg;
-      if (!epi_all(mbar_wait_cl(&tfull[acc], aphase, abort))) {
+      if (!epi_all(mbar_wait_cl(&tfull[acc], aphase, abort, wc.ns))) {
         go = false;
         break;
       }
@@ -316,11 +318,11 @@ PJob to_pjob(const TcJob& j) {
 gptq_status gemm_pair_sub(const OperandMaps& maps, const TcJob& j0, const TcJob& j1, int K,
                           const unsigned* flag, unsigned* status, int kind, cudaStream_t s,
                           const FusedPotrf& fp, int kseg) {
-  static bool attr = false;
-  if (!attr) {
+  static DeviceOnce attr;
+  GQ_TRY(attr.run([](int) -> gptq_status {
     GQ_CUDA(cudaFuncSetAttribute(k_gemm_pair, cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM));
-    attr = true;
-  }
+    return GPTQ_OK;
+  }));
   if (K % PBK != 0 || K <= 0) return GPTQ_ERR_ARG;
   const PJob p0 = to_pjob(j0), p1 = to_pjob(j1);
   const int total = p0.ntiles + p1.ntiles;
@@ -331,7 +333,7 @@ gptq_status gemm_pair_sub(const OperandMaps& maps, const TcJob& j0, const TcJob&
   if (pairs < 1) pairs = 1;
   GQ_PROF(kind, s);
   k_gemm_pair<<<2 * pairs, P_THREADS, P_SMEM, s>>>(maps.m[0], maps.m[1], maps.m[2], maps.m[3], maps.c, p0,
-                                                   p1, K, kseg, flag, status, fp);
+                                                   p1, K, kseg, flag, status, fp, wait_cfg());
   GQ_LAUNCHED();
   return GPTQ_OK;
 }

@@ -78,7 +78,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap m0, const __grid_constant__ CUtensorMap m1,
               const __grid_constant__ CUtensorMap m2, const __grid_constant__ CUtensorMap m3,
               const __grid_constant__ CUtensorMap cmap, TcJob j0, TcJob j1, int K, int kseg,
-              const unsigned* flag, unsigned* status, FusedPotrf fp) {
+              const unsigned* flag, unsigned* status, FusedPotrf fp, WaitCfg wc) {
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment by an offset on the shared array itself (not an
   // integer round trip), so that accesses through `smem` stay shared-memory
@@ -144,7 +144,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       const CUtensorMap* maps[4] = {&m0, &m1, &m2, &m3};
       int stage = 0, issued = 0;
       uint32_t phase = 0;
-      for (int t = t0; t < total && !*abort; t += tstride) {
+      // wc.no_loads (a test hook): issue nothing, so that the MMA and
+      // epilogue waits below run out and report a timeout.
+      for (int t = t0; t < total && !*abort && !wc.no_loads; t += tstride) {
         const bool second = t >= j0.ntiles;
         const TcJob& J = second ? j1 : j0;
         int ti, tj;
@@ -155,7 +157,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         const CUtensorMap* bhi = maps[J.b_map];
         const CUtensorMap* blo = maps[J.b_map + 1];
         for (int c = 0; c < nk; ++c) {
-          if (!mbar_wait(&empty[stage], phase ^ 1u, abort)) break;
+          if (!mbar_wait(&empty[stage], phase ^ 1u, abort, wc.ns)) break;
           const uint32_t sb = smem_u32(smem + stage * STAGE_BYTES);
           mbar_expect_tx(&full[stage], STAGE_BYTES);
           tma_load_2d(sb, ahi, c * BK, ay, &full[stage]);
@@ -178,7 +180,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (int t = t0; t < total && !*abort; t += tstride) {
         bool ok = true;
         for (int sg = 0; sg < nseg && ok; ++sg) {
-          if (!mbar_wait(&tempty[acc], aphase ^ 1u, abort)) {
+          if (!mbar_wait(&tempty[acc], aphase ^ 1u, abort, wc.ns)) {
             ok = false;
             break;
           }
@@ -186,7 +188,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           const uint32_t d = tmem + (uint32_t)(acc * BN);
           const int cend = (sg + 1) * segc < nk ? (sg + 1) * segc : nk;
           for (int c = sg * segc; c < cend; ++c) {
-            if (!mbar_wait(&full[stage], phase, abort)) {
+            if (!mbar_wait(&full[stage], phase, abort, wc.ns)) {
               ok = false;
               break;
             }
@@ -219,10 +221,10 @@ __global__ void __launch_bounds__(THREADS, 1)
       consumed_sh = consumed;
       // Every MMA this thread issued has completed once `drain` flips.
       mma_commit(&drain);
-      if (!mbar_wait(&drain, 0u, abort)) {
+      if (!mbar_wait(&drain, 0u, abort, wc.ns)) {
         // Give the drain a last bounded chance even after an abort.
         const uint64_t t0 = globaltimer();
-        while (!mbar_try_wait(&drain, 0u) && globaltimer() - t0 < WAIT_NS) {
+        while (!mbar_try_wait(&drain, 0u) && globaltimer() - t0 < wc.ns) {
         }
       }
     }
@@ -237,7 +239,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int t = w / nseg;
       // All 128 epilogue threads agree before any of them reaches the
       // .sync.aligned loads or the named barriers below.
-      if (!epi_all(mbar_wait(&tfull[acc], aphase, abort))) {
+      if (!epi_all(mbar_wait(&tfull[acc], aphase, abort, wc.ns))) {
         go = false;
         break;
       }
@@ -300,7 +302,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (int i = consumed_sh; i < issued_sh; ++i) {
       const uint64_t t0 = globaltimer();
       while (!mbar_try_wait(&full[i % STAGES], (uint32_t)((i / STAGES) & 1)) &&
-             globaltimer() - t0 < WAIT_NS) {
+             globaltimer() - t0 < wc.ns) {
       }
     }
     atomicOr(status, 2u);
@@ -324,29 +326,56 @@ __global__ void __launch_bounds__(THREADS, 1)
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (fn == nullptr) {
+  // A function-local static: initialised once, thread-safe.
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
     void* p = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
             cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
+      return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    return static_cast<PFN_cuTensorMapEncodeTiled_v12000>(nullptr);
+  }();
   return fn;
 }
 
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+
+CtxGetCurrentFn ctx_get_current_fn() {
+  static CtxGetCurrentFn fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      return reinterpret_cast<CtxGetCurrentFn>(p);
+    return static_cast<CtxGetCurrentFn>(nullptr);
+  }();
+  return fn;
+}
+
+DeviceOnce g_tc_attr;
+
 }  // namespace
 
+CUcontext current_context() {
+  const auto fn = ctx_get_current_fn();
+  CUcontext c = nullptr;
+  if (fn == nullptr || fn(&c) != CUDA_SUCCESS) return nullptr;
+  return c;
+}
+
 int num_sms() {
-  static int sms = 0;
-  if (sms == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (sms <= 0) sms = 148;
+  static std::mutex mu;
+  static int sms[DeviceOnce::kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= DeviceOnce::kMaxDevices) dev = 0;
+  std::lock_guard<std::mutex> lk(mu);
+  if (sms[dev] <= 0) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 148;
+    sms[dev] = v;
   }
-  return sms;
+  return sms[dev];
 }
 
 
@@ -381,18 +410,17 @@ gptq_status make_c_map(CUtensorMap* m, float* base, long long rows, long long co
 gptq_status gemm_tc_sub(const OperandMaps& maps, const TcJob& j0, const TcJob& j1, int K,
                         const unsigned* flag, unsigned* status, int kind, cudaStream_t s,
                         const FusedPotrf& fp, int kseg) {
-  static bool attr = false;
-  if (!attr) {
+  GQ_TRY(g_tc_attr.run([](int) -> gptq_status {
     GQ_CUDA(cudaFuncSetAttribute(k_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES));
-    attr = true;
-  }
+    return GPTQ_OK;
+  }));
   if (K % BK != 0 || K <= 0) return GPTQ_ERR_ARG;
   const int total = j0.ntiles + j1.ntiles;
   if (total <= 0) return GPTQ_OK;
   const int grid = total < num_sms() ? total : num_sms();
   GQ_PROF(kind, s);
   k_gemm_tc<<<grid, THREADS, SMEM_BYTES, s>>>(maps.m[0], maps.m[1], maps.m[2], maps.m[3], maps.c, j0,
-                                              j1, K, kseg, flag, status, fp);
+                                              j1, K, kseg, flag, status, fp, wait_cfg());
   GQ_LAUNCHED();
   return GPTQ_OK;
 }

@@ -19,6 +19,11 @@ int g_used = 0;
 int g_open = -1;
 unsigned g_mask = ~0u;  // kinds that record events
 
+constexpr unsigned long long kDefaultWaitNs = 2000000000ull;  // 2 s
+constexpr unsigned long long kMaxWaitNs = 10000000000ull;     // 10 s
+std::atomic<unsigned long long> g_wait_ns{kDefaultWaitNs};
+std::atomic<int> g_no_loads{0};
+
 const char* kNames[K_NKINDS] = {"diag", "build", "potrf", "trsm", "fold_gemm", "ladder",
                                 "sweep_block", "prep_ut", "sweep_gemm", "group", "copy",
                                 "gram_prep", "gram_gemm", "place", "debias",
@@ -44,11 +49,25 @@ void prof_end(int kind, cudaStream_t s) {
   g_open = -1;
 }
 
+WaitCfg wait_cfg() {
+  WaitCfg c;
+  c.ns = g_wait_ns.load(std::memory_order_relaxed);
+  c.no_loads = g_no_loads.load(std::memory_order_relaxed);
+  return c;
+}
+
 }  // namespace gq
 
 using namespace gq;
 
 extern "C" {
+
+gptq_status gptq_test_set_wait(unsigned long long wait_ns, int no_loads) {
+  if (wait_ns > kMaxWaitNs || (no_loads != 0 && no_loads != 1)) return GPTQ_ERR_ARG;
+  g_wait_ns.store(wait_ns == 0 ? kDefaultWaitNs : wait_ns);
+  g_no_loads.store(no_loads);
+  return GPTQ_OK;
+}
 
 long long gptq_launch_count(void) { return g_launches.load(); }
 

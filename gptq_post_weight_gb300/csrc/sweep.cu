@@ -593,16 +593,16 @@ size_t sweep_ws_bytes(int rows, int n) { return sweep_ws_bytes_g(rows, n, GMAX);
 size_t sweep_ws_min_bytes(int rows, int n) { return sweep_ws_bytes_g(rows, n, GMIN); }
 
 static gptq_status sweep_attrs() {
-  static bool done = false;
-  if (done) return GPTQ_OK;
-  GQ_CUDA(cudaFuncSetAttribute(k_sweep_block<MODE_Q4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               SWEEP_SMEM));
-  GQ_CUDA(cudaFuncSetAttribute(k_sweep_block<MODE_Q4_ACT>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, SWEEP_SMEM));
-  GQ_CUDA(cudaFuncSetAttribute(k_sweep_block<MODE_Q2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               SWEEP_SMEM));
-  done = true;
-  return GPTQ_OK;
+  static DeviceOnce once;
+  return once.run([](int) -> gptq_status {
+    GQ_CUDA(cudaFuncSetAttribute(k_sweep_block<MODE_Q4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 SWEEP_SMEM));
+    GQ_CUDA(cudaFuncSetAttribute(k_sweep_block<MODE_Q4_ACT>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, SWEEP_SMEM));
+    GQ_CUDA(cudaFuncSetAttribute(k_sweep_block<MODE_Q2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 SWEEP_SMEM));
+    return GPTQ_OK;
+  });
 }
 
 gptq_status ladder_run(const float* W, int rows, int n, float* tab, float* lost, cudaStream_t s) {
@@ -632,28 +632,28 @@ gptq_status copy_dead_zeroed(const float* W, int rows, int n, const float* hdiag
 
 // Scratch for gptq_q4tp_sweep_noalloc: a file-scope device array, so that a
 // caller that must not allocate device memory can still run the sweep.  Its
-// host-side name is only a stand-in; the device address comes from
-// cudaGetSymbolAddress, looked up once per device (on that device's first
-// call) and cached.
+// host-side name is only a stand-in, never a device address: the address
+// comes from cudaGetSymbolAddress, looked up with the device current on the
+// first call in each device's context (again after a device reset, whose
+// new context places the array anew), and kept for later calls.
 namespace {
 __device__ __align__(256) unsigned char g_noalloc_scratch[GPTQ_SWEEP_NOALLOC_SCRATCH_BYTES];
-constexpr int kMaxDevices = 64;
-std::mutex g_noalloc_mu;
-void* g_noalloc_ptr[kMaxDevices] = {};
+DeviceOnce g_noalloc_once;
+void* g_noalloc_ptr[DeviceOnce::kMaxDevices] = {};
 }  // namespace
 
 gptq_status noalloc_scratch(void** out) {
-  int dev = 0;
-  GQ_CUDA(cudaGetDevice(&dev));
-  if (dev < 0 || dev >= kMaxDevices) return GPTQ_ERR_CUDA;
-  std::lock_guard<std::mutex> lk(g_noalloc_mu);
-  if (g_noalloc_ptr[dev] == nullptr) {
+  GQ_TRY(g_noalloc_once.run([](int dev) -> gptq_status {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return GPTQ_ERR_CUDA;
     g_noalloc_ptr[dev] = p;
-  }
+    return GPTQ_OK;
+  }));
+  int dev = 0;
+  GQ_CUDA(cudaGetDevice(&dev));
+  std::lock_guard<std::mutex> lk(g_noalloc_once.mu);
   *out = g_noalloc_ptr[dev];
-  return GPTQ_OK;
+  return *out != nullptr ? GPTQ_OK : GPTQ_ERR_CUDA;
 }
 
 static gptq_status sweep_core(int mode, float* W, int rows, int n, const float* U, const float* hw,

@@ -6,9 +6,9 @@
 
 namespace gq {
 
-// Bound on every wait (globaltimer, ns): past it a kernel stops issuing,
-// drains what it started and reports a timeout.
-constexpr unsigned long long WAIT_NS = 2000000000ull;
+// Every wait is bounded by WaitCfg::ns of globaltimer (2 s unless a test
+// sets it shorter): past it a kernel stops issuing, drains what it started
+// and reports a timeout.
 
 static __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
@@ -44,14 +44,15 @@ static __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t par
 }
 
 // Wait for the phase of `bar` with the given parity; false once `abort` is
-// set (by anyone) or after WAIT_NS (then this thread sets it).
-static __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+// set (by anyone) or after `limit` ns (then this thread sets it).
+static __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                                 uint64_t limit) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   for (;;) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
-    if (globaltimer() - t0 > WAIT_NS) {
+    if (globaltimer() - t0 > limit) {
       *abort = 1;
       return false;
     }
@@ -172,13 +173,14 @@ static __device__ __forceinline__ bool mbar_try_wait_cl(uint64_t* bar, uint32_t 
       : "memory");
   return ok != 0u;
 }
-static __device__ __forceinline__ bool mbar_wait_cl(uint64_t* bar, uint32_t parity, volatile int* abort) {
+static __device__ __forceinline__ bool mbar_wait_cl(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                                    uint64_t limit) {
   if (mbar_try_wait_cl(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   for (;;) {
     if (mbar_try_wait_cl(bar, parity)) return true;
     if (*abort) return false;
-    if (globaltimer() - t0 > WAIT_NS) {
+    if (globaltimer() - t0 > limit) {
       *abort = 1;
       return false;
     }

@@ -136,3 +136,10 @@ def test_gram_and_act_order_argument_errors(clib):
     assert clib.gptq_quantize_group_act_order(fake, 64, float("inf"), fake, 4, fake, fake, fake, None, None,
                                               None, ws, big, None) == 1
     assert clib.gptq_group_act_order_workspace_bytes(4, 0) == 0
+
+
+def test_wait_hook_arguments(clib):
+    # Host-side checks only: nothing here launches a kernel.
+    assert clib.gptq_test_set_wait(ctypes.c_ulonglong(20_000_000_000), 0) == 1  # above 10 s
+    assert clib.gptq_test_set_wait(ctypes.c_ulonglong(1_000_000), 2) == 1
+    assert clib.gptq_test_set_wait(ctypes.c_ulonglong(0), 0) == 0
