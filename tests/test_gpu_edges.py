@@ -4,10 +4,10 @@ debias, against the oracle (the oracle's own U and ladders go to both sides).
 * n = 32 (one group): the device rule is the oracle's rule on the same
   tile, so codes, rungs and scales are bit-exact;
 * wider ragged shapes (a partial last block, rows not a multiple of the
-  40-row tile): the later columns differ from the oracle only by the f32
-  summation order of the residual updates, so >= 98 % of codes agree (a
-  handful of rows: one flipped code is already 1/rows of a percent) and the
-  output error is within 2 %;
+  40-row tile, over 400 rows so that the bar is measurable): the later
+  columns differ from the oracle only by the f32 summation order of the
+  residual updates, so the end-to-end bar applies: >= 99.9 % of codes
+  agree and the output error is within 1 %;
 * all-zero rows: rung 0, every code at the zero level (q4tp nibble 8, q2tp
   code 0 with scale 0), and the debias leaves them alone.
 """
@@ -75,16 +75,17 @@ def test_single_group_bit_exact(lib, rows):
         assert np.array_equal(scales.view(np.uint32), res["scale"].view(np.uint32))
 
 
-@pytest.mark.parametrize("n,rows", [(64, 3), (160, 41), (288, 81), (96, 40)])
+@pytest.mark.parametrize("n,rows", [(64, 403), (160, 441), (288, 481), (96, 440), (416, 3)])
 def test_ragged_shapes(lib, n, rows):
     hp, w, wz, u, hw, dead = problem(n, rows, n + rows)
     h = oracle.unpack_upper(hp, n)
     for run, deq in ((run_q4, oracle.dequant_q4tp), (run_q2, oracle.dequant_q2tp)):
         res, q, rungs, scales, _ = run(wz, u, hw, dead)
-        assert (q == res["q"].astype(q.dtype)).mean() >= 0.98
+        agree = (q == res["q"].astype(q.dtype)).mean()
+        assert agree >= 0.999, (run.__name__, agree)
         e_dev = oracle.output_error(wz, deq(q, scales), h)
         e_or = oracle.output_error(wz, deq(res["q"], res["scale"]), h)
-        assert abs(e_dev - e_or) <= 0.02 * e_or, (run.__name__, e_dev, e_or)
+        assert abs(e_dev - e_or) <= 0.01 * e_or, (run.__name__, e_dev, e_or)
 
 
 def test_zero_rows(lib):

@@ -83,7 +83,7 @@ def test_fold_rank_deficient_retry(lib):
     # f32 may need one more x10 step than f64; never less damping.
     assert lamo <= lam <= 10 * lamo * (1 + 1e-12)
     uo = oracle.fold(hp, n, lam)[0]
-    assert rel_fro(np_(u), uo) <= 1e-3
+    assert rel_fro(np_(u), uo) <= 1e-4, rel_fro(np_(u), uo)
 
 
 def test_fold_not_spd_and_nan(lib):
@@ -253,7 +253,7 @@ def test_gptq_beats_rtn_on_device(lib):
 # ------------------------------------------------------------------ full sizes (sampled rows)
 
 @pytest.mark.slow
-@pytest.mark.parametrize("name", ["n4096", "n17408"])
+@pytest.mark.parametrize("name", ["n4096", "n14336", "n17408"])
 def test_full_size_group(lib, name, oracle_folds):
     """The bench's workload: GPU inputs, full fold compared with the f64
     oracle, the sweep on sampled rows (rows are independent given U)."""
