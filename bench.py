@@ -11,6 +11,12 @@ problems, no collective on the data path): weak scaling.  ``--codec q2tp``
 times the same step with the q2tp "placed" rule instead (placed ladder,
 31-rung search, 2-bit codes: gptq_quantize_group_q2tp), under its own metric.
 
+The default line also carries the 11-group batch (config "batch": seeds
+0..10, four streams, total wall time and groups/s) measured after the
+headline (``--no-batch`` leaves it out), the whole fold's and the sweep
+GEMMs' fractions of the 3xTF32 peak, and that peak measured in-process
+(cuBLAS TF32).
+
 ``--impl reference`` times the CPU oracle (the plain f64/f32 restatement of
 the pages) on the host cores, on a bounded sample of the same workload
 scaled to seconds per group.
@@ -127,6 +133,38 @@ def hbm_report(per_kind, n, rows, codec="q4tp", peak_gbs=None, NB=128, SB=128):
         out[kind] = {"what": what, "bytes_per_group": nbytes, "ms_per_group": ms, "gbs": gbs,
                      "frac": gbs / peak_gbs if peak_gbs else None}
     return out
+
+
+def measure_tf32_tflops(torch, dev, size=8192, reps=10):
+    """Dense TF32 peak of this GPU, measured here: cuBLAS f32 matmul with TF32
+    allowed at size^3 (2 size^3 flops), best of `reps` after warm-up, timed
+    with CUDA events on the current stream.  A burst figure: the roofline
+    denominators of kernels timed in a seconds-long run at full clocks."""
+    prev = torch.backends.cuda.matmul.allow_tf32
+    torch.backends.cuda.matmul.allow_tf32 = True
+    try:
+        g = torch.Generator(device=dev)
+        g.manual_seed(7)
+        a = torch.randn(size, size, device=dev, generator=g)
+        b = torch.randn(size, size, device=dev, generator=g)
+        c = torch.empty(size, size, device=dev)
+        for _ in range(3):
+            torch.matmul(a, b, out=c)
+        torch.cuda.synchronize()
+        best = None
+        for _ in range(reps):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            torch.matmul(a, b, out=c)
+            e1.record()
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1)
+            best = ms if best is None else min(best, ms)
+        del a, b, c
+        return 2.0 * size ** 3 / (best / 1e3) / 1e12
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = prev
 
 
 class ClockSampler:
@@ -272,11 +310,11 @@ def aggregate(t_local: float, steps: int, world: int, pg=None):
     return t, t / (steps * world)
 
 
-def run_batch(args, rank, world, dev, lib, _lib, torch, synth):
+def batch_measure(args, dev, lib, _lib, torch, synth, steps, warmup):
     """11 independent n = 17408 groups (seeds 0..10) back to back on one GPU:
     `--streams` host threads, each with its own CUDA stream and workspace,
     take groups in turn.  Device-timed from one event that every stream
-    waits on to one event that waits on every stream."""
+    waits on to one event that waits on every stream.  Returns a dict."""
     import concurrent.futures as cf
 
     ngroups = 11
@@ -314,28 +352,41 @@ def run_batch(args, rank, world, dev, lib, _lib, torch, synth):
         return start, end
 
     with cf.ThreadPoolExecutor(S) as pool:
-        for _ in range(max(args.warmup, 0)):
+        for _ in range(max(warmup, 0)):
             one_pass(pool)
         torch.cuda.synchronize()
         sampler = ClockSampler(dev.index or 0)
         sampler.start()
         time.sleep(0.3)
         l0 = _lib.launch_count()
-        marks = [one_pass(pool) for _ in range(args.steps)]
+        t_h0 = time.perf_counter()
+        marks = [one_pass(pool) for _ in range(steps)]
         torch.cuda.synchronize()
+        t_h1 = time.perf_counter()
         launches = _lib.launch_count() - l0
-        clocks = sampler.stop()
+        clocks = sampler.stop(t_h0, t_h1)
     t = sum(s.elapsed_time(e) for s, e in marks) / 1e3
-    t_max, value = aggregate(t / ngroups, args.steps, world, None)
+    out = {"workload": f"batch: {ngroups} independent groups, each " + workload_desc(cfgs[0]).split(": ", 1)[1]
+                       + f"; seeds 0..{ngroups - 1}; {S} streams",
+           "groups": ngroups, "streams": S, "passes": steps, "warmup": warmup,
+           "total_s_per_pass": t / steps, "s_per_group": t / steps / ngroups,
+           "groups_per_s": ngroups * steps / t, "gpu_launches": launches, "clocks": clocks,
+           "timing": "CUDA events: one event every stream waits on, one that waits on every stream"}
+    del probs, wss, outs
+    torch.cuda.empty_cache()
+    return out
+
+
+def run_batch(args, rank, world, dev, lib, _lib, torch, synth):
+    b = batch_measure(args, dev, lib, _lib, torch, synth, args.steps, args.warmup)
+    t_max, value = aggregate(b["s_per_group"] * args.steps, args.steps, world, None)
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-                "warmup": args.warmup, "ms_per_step": t / args.steps * 1e3, "higher_is_better": False,
+                "warmup": args.warmup, "ms_per_step": b["total_s_per_pass"] * 1e3, "higher_is_better": False,
                 "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-                "config": {"workload": f"batch: {ngroups} independent groups, each " + workload_desc(cfgs[0]).split(": ", 1)[1]
-                           + f"; seeds 0..{ngroups - 1}; {S} streams", "groups_per_step": ngroups,
-                           "groups_per_s": ngroups * args.steps / t,
-                           "l2": "inputs larger than L2; no flush"},
-                "gpu_launches": launches, "clocks": clocks}
+                "config": {"workload": b["workload"], "groups_per_step": b["groups"],
+                           "groups_per_s": b["groups_per_s"], "l2": "inputs larger than L2; no flush"},
+                "gpu_launches": b["gpu_launches"], "clocks": b["clocks"]}
         print(json.dumps(line), flush=True)
 
 
@@ -405,6 +456,9 @@ def main():
     ap.add_argument("--rows", type=int, default=None)
     ap.add_argument("--streams", type=int, default=4, help="host threads / streams for --config batch")
     ap.add_argument("--codec", choices=["q4tp", "q2tp"], default="q4tp")
+    ap.add_argument("--no-batch", action="store_true",
+                    help="leave out the 11-group batch measured after the headline (n17408 q4tp only)")
+    ap.add_argument("--batch-passes", type=int, default=3)
     ap.add_argument("--debias", action="store_true",
                     help="add the output debias (W H on the tensor cores, per-row lo shift) to the step")
     args = ap.parse_args()
@@ -471,6 +525,7 @@ def main():
         res = step()
     torch.cuda.synchronize()
     lam_used = res["lam"] if res is not None else None
+    tf32_meas = measure_tf32_tflops(torch, dev)
 
     def barrier():
         if pg is not None:
@@ -563,8 +618,30 @@ def main():
                "d2h_bytes_per_step": sum(o.numel() * o.element_size() for o in outs),
                "overlap": "next group's upload on a copy stream under the current group's compute"}
 
+    # The 11-group batch (seeds 0..10 on several streams), after the headline.
+    batch = None
+    if (not args.no_batch and world == 1 and not q2 and not args.debias and args.config == "n17408"
+            and args.n is None and args.rows is None):
+        batch = batch_measure(args, dev, lib, _lib, torch, synth, max(1, args.batch_passes), 1)
+
     # Roofline of the dominant kernel kind, from the live event timings.
+    # 3xTF32: three TF32 MMAs per f32 product, so the algorithmic rate is held
+    # against one third of the TF32 dense peak.  That peak is measured here
+    # (cuBLAS TF32, a burst figure); it is used as is when the SM clocks
+    # stayed at their maximum through the timed region (no power or thermal
+    # reason), else scaled by the driver's sustained / burst bf16 ratio.
     pk, src = peaks()
+    at_max = bool(clocks and clocks.get("sm_max_mhz") and clocks["sm_mhz"] >= 0.98 * clocks["sm_max_mhz"]
+                  and not clocks.get("reasons"))
+    if tf32_meas:
+        tf32 = tf32_meas if at_max else tf32_meas * pk.get("bf16_tflops_sustained", 1.0) / pk.get("bf16_tflops", 1.0)
+        peak_src = (f"measured here: cuBLAS TF32 8192^3 best of 10 = {tf32_meas:.1f} TFLOP/s"
+                    + ("" if at_max else " x the driver's bf16 sustained/burst ratio (clocks left their maximum)")
+                    + " / 3 (3xTF32 split)")
+    else:
+        tf32 = pk.get("bf16_tflops_sustained", pk.get("bf16_tflops")) * TF32_PER_BF16
+        peak_src = f"{src} bf16 sustained x 1.1/2.25 (nominal TF32 ratio) / 3 (3xTF32 split)"
+    peak = tf32 / 3.0
     kinds = {k: v for k, v in prof.items() if k in ("fold_gemm", "sweep_gemm")}
     top = max(kinds, key=lambda k: kinds[k][0])
     ms_top, cnt_top = kinds[top]
@@ -574,21 +651,19 @@ def main():
     if top in flops and cnt_top > 0:
         per_launch = flops[top] / cnt_top
         achieved = per_launch / (ms_top / cnt_top / 1e3) / 1e12
-        # 3xTF32: three TF32 MMAs per f32 product, so the algorithmic rate is
-        # held against one third of the TF32 dense peak (the measured bf16
-        # figure x the nominal TF32:BF16 ratio; sustained, since the kernel
-        # runs inside a long step).
-        tf32 = pk.get("bf16_tflops_sustained", pk.get("bf16_tflops")) * TF32_PER_BF16
-        peak = tf32 / 3.0
         roof = {"bound": "tensor", "kernel": top, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "traffic": TRAFFIC.get(top),
                 "timing": f"CUDA events around each launch of this kind over a second timed region of "
                           f"{args.steps} steps (the headline steps carry no events)",
-                "peak_source": f"{src} bf16 sustained {pk.get('bf16_tflops_sustained')} x 1.1/2.25 (TF32) / 3 (3xTF32 split)",
-                "flop_per_launch": per_launch}
+                "peak_source": peak_src, "flop_per_launch": per_launch}
     fold_flops = 2 * n ** 3 / 3
     per_kind = {k: {"ms_per_step": v[0], "launches_per_step": v[1]}
                 for k, v in breakdown.items() if not k.startswith("_") and v[1] > 0}
+    fold_kinds = ("fold_gemm", "build", "potrf", "trsm", "diag", "fold_strip")
+    fold_ms = sum(per_kind.get(k, {}).get("ms_per_step", 0.0) for k in fold_kinds)
+    fold_tflops = fold_flops / (fold_ms / 1e3) / 1e12 if "fold_gemm" in per_kind and fold_ms > 0 else None
+    sweep_ms = per_kind.get("sweep_gemm", {}).get("ms_per_step")
+    sweep_tflops = sweep_gemm_flops(rows, n) / (sweep_ms / 1e3) / 1e12 if sweep_ms else None
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -608,10 +683,16 @@ def main():
                              % (hp.numel() * 4 / 1e6, w.numel() * 4 / 1e6, n * n * 4 / 1e6),
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "roofline": roof,
-            "fold_tflops_algorithmic": fold_flops / (per_kind.get("fold_gemm", {}).get("ms_per_step", 0) / 1e3
-                                                     + sum(per_kind.get(k, {}).get("ms_per_step", 0) / 1e3
-                                                           for k in ("build", "potrf", "trsm", "diag", "fold_strip"))
-                                                     ) / 1e12 if "fold_gemm" in per_kind else None,
+            "fold_tflops_algorithmic": fold_tflops,
+            "fold_frac": fold_tflops / peak if fold_tflops else None,
+            "fold_frac_what": "whole fold (every fold kernel: diag, build, diagonal-block steps, panel products, "
+                              "strip and trailing updates), 2 n^3 / 3 algorithmic flops over their time per group, "
+                              "against the 3xTF32 peak of roofline.peak",
+            "sweep_gemm_tflops_algorithmic": sweep_tflops,
+            "sweep_gemm_frac": sweep_tflops / peak if sweep_tflops else None,
+            "sweep_gemm_frac_what": "every trailing update of the sweep (thin and K = 512), rows n^2 algorithmic "
+                                    "flops over their time per group, against the same peak",
+            "batch": batch,
             "per_kernel": per_kind,
             "per_kernel_source": "one extra untimed step with every launch bracketed by events",
             "hbm": {"unit": "GB/s", "peak": pk.get("hbm_gbs"), "peak_source": src,
@@ -621,7 +702,10 @@ def main():
             "gpu_launches": launches,
             "clocks": clocks,
             "peaks": {"source": src, "hbm_gbs": pk.get("hbm_gbs"), "bf16_tflops": pk.get("bf16_tflops"),
-                      "tf32_tflops_equiv": pk.get("bf16_tflops", 0) * TF32_PER_BF16},
+                      "bf16_tflops_sustained": pk.get("bf16_tflops_sustained"),
+                      "tf32_tflops_measured": tf32_meas,
+                      "tf32_tflops_nominal_ratio": pk.get("bf16_tflops", 0) * TF32_PER_BF16,
+                      "tf32_used": tf32, "clocks_at_max": at_max},
         }
         print(json.dumps(line), flush=True)
     if pg is not None:
