@@ -184,23 +184,36 @@ inline TcJob tc_lower(int c_x0, int c_y0, int map, int row0, int M) {
   return j;
 }
 
+// Maps of the fold's panel product on the tensor cores (apply_tc.cu): the
+// working matrix A (box 32 x 128, as for a C map), the TF32 pair of the
+// diagonal block's inverse (NB x NB each, operand maps with boxes of 32
+// rows), and the panel buffers P hi/lo, Yp hi/lo (p.m[0..3], operand maps).
+struct ApplyMaps {
+  CUtensorMap a, lhi, llo;
+  OperandMaps p;
+};
+gptq_status apply_tc_run(const ApplyMaps& am, int k, int s0, int N, int col0, int zero_end, unsigned* flag,
+                         float* U, const float* dabs, int n, cudaStream_t s);
+
 // Tensor map over the f32 matrix C [rows][cols] (leading dimension ld) for
 // the GEMM's reduce-add epilogue (box 32 x 128, 128-byte swizzle).
 gptq_status make_c_map(CUtensorMap* m, float* base, long long rows, long long cols, long long ld);
 
-// Tensor map over a K-major f32 operand array [rows][K] (box 32 x 128,
-// 128-byte swizzle).  K must be a multiple of 32, base 16-byte aligned.
-gptq_status make_operand_map(CUtensorMap* m, const float* base, long long rows, int K);
+// Tensor map over a K-major f32 operand array [rows][K] (box 32 x box_rows,
+// 128 rows unless given; 128-byte swizzle).  K must be a multiple of 32,
+// base 16-byte aligned, box_rows a multiple of 8 up to 256.
+gptq_status make_operand_map(CUtensorMap* m, const float* base, long long rows, int K, int box_rows = 128);
 
 // Diagonal-block step fused into an update (fold only): the block at (k, k)
 // of the N x N matrix A (leading dimension lda) must be tile 0 of job 0; its
-// Cholesky inverse goes, transposed, to LinvT and a bad pivot to bit 0 of
-// the status word.
+// Cholesky inverse goes, as a TF32 hi/lo pair (row-major), to Lhi / Llo and
+// a bad pivot to bit 0 of the status word.
 struct FusedPotrf {
   const float* A;
   long long lda;
   int k;
-  float* LinvT;
+  float* Lhi;
+  float* Llo;
   int on;
 };
 

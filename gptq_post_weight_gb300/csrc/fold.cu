@@ -9,11 +9,13 @@
 //   * its strict upper triangle: Y = X^T, the inverse being accumulated.
 // Cholesky and inverse run interleaved in one right-looking loop over
 // column blocks k (NB wide):
-//   potrf(k)      factor the diagonal block (one CTA, shared memory);
-//   trsm_panel(k) L[i, k-block] for i below (forward substitution per row)
-//                 -> panel buffer P;
-//   trsm_inv(k)   X[k-block, c] = L_kk^-1 X[k-block, c] for c < k+NB (rows of
-//                 Y) -> panel buffer Yp, and the finished rows of U;
+//   potrf(k)      factor and invert the diagonal block (one CTA, shared
+//                 memory) -> L_kk^-1 as a TF32 pair;
+//   apply(k)      both triangular solves as one tensor-core product with
+//                 that inverse (apply_tc.cu): the panel L[i, k-block] for i
+//                 below -> panel buffer P; the inverse's block row
+//                 X[k-block, c] for c < k+NB (rows of Y) -> panel buffer Yp,
+//                 and the finished entries of U;
 //   update(k)     A[i][j] -= P_i P_j^T (lower tiles, i, j >= k+NB) and
 //                 Y[c][i] -= Yp_c P_i^T (c < k+NB <= i): one GEMM launch.
 // A pivot that is not positive (or NaN) sets a device flag; every later
@@ -124,182 +126,19 @@ __global__ void __launch_bounds__(256) k_build(const float* __restrict__ hp, int
   }
 }
 
-// Standalone launch of the diagonal-block step (the first block of a fold).
+// Standalone launch of the diagonal-block step.
 __global__ void __launch_bounds__(256) k_potrf(const float* __restrict__ A, long long lda, int k,
-                                               float* __restrict__ LinvT, unsigned* flag) {
+                                               float* __restrict__ Lhi, float* __restrict__ Llo,
+                                               unsigned* flag) {
   if (flagged(flag)) return;
   extern __shared__ float S[];
-  potrf_inverse_block(A + (long long)k * lda + k, lda, LinvT, flag, S);
+  potrf_inverse_block(A + (long long)k * lda + k, lda, Lhi, Llo, flag, S);
 }
 
-constexpr int APPLY_ROWS = 32;     // rows per tile
-constexpr int APPLY_THREADS = 256;
-constexpr int LV = NB + 4;  // row stride of the row-vector tiles (float4 rows)
 // Panel buffers hold two steps side by side (columns [0, NB) and [NB, 2NB)),
 // so that a pair of steps updates the trailing matrix once with K = 2 NB.
+// The panel product that fills them is apply_tc.cu.
 constexpr int PW = 2 * NB;
-
-// Both triangular solves of step k as one product with the explicit inverse:
-// z = L_kk^-1 v for every row vector v, i.e. Z = V Linv^T:
-//  * rows i >= s0 = k+NB: the Cholesky panel (fold page chol_panel),
-//    v = A[i][k..k+NB), z -> P[i][*];
-//  * rows c < s0: the inverse's block row (fold page inv_rows), v =
-//    Y[c][k..k+NB) (the unit vector e_{c-k} when c is in block k, so that row
-//    of Z is a column of Linv), z -> Yp[c][*], and the finished entries of U:
-//    U[n-1-i][n-1-c] = X[i][c] / |d_{n-1-c}| ([fold page] make_u; taken as X times
-//    the rounded reciprocal, within a rounding of the quotient), i = k+t.
-// z is stored as its TF32 hi/lo split, the operand format of the update GEMM,
-// in columns [col0, col0 + NB) of the 2 NB-wide panel buffers; panel rows
-// below zero_end also clear their Yp entries there (see fold_attempt).
-// Persistent (two CTAs per SM): a CTA keeps L_kk^-T in shared memory and
-// walks tiles of 32 rows, the next tile's vectors arriving (asynchronous
-// copies) while the current one is multiplied.  The sums stop at the diagonal of Linv (z_c
-// needs v_u for u <= c only); warp w owns the 8-column blocks w and 15 - w,
-// so every warp does the same number of multiply-adds.  Thread (l % 16,
-// l / 16): rows l % 16 and l % 16 + 16, 4 columns of each block.  Z goes
-// back through shared memory for row-contiguous stores.
-__global__ void __launch_bounds__(APPLY_THREADS, 2) k_apply(const float* __restrict__ A, long long lda,
-                                                           int k, int s0, int N, int col0, int zero_end,
-                                                           const float* __restrict__ LinvT,
-                                                           float* __restrict__ P_hi, float* __restrict__ P_lo,
-                                                           float* __restrict__ Y_hi, float* __restrict__ Y_lo,
-                                                           const unsigned* flag, float* __restrict__ U,
-                                                           const float* __restrict__ dabs, int n) {
-  if (flagged(flag)) return;
-  extern __shared__ __align__(16) float sm[];
-  float* Lt = sm;                         // [NB][NB]: Lt[u][c] = Linv[c][u]
-  float* Vb = Lt + NB * NB;               // 2 x [APPLY_ROWS][LV]: row vectors, then Z
-  const int tid = threadIdx.x;
-  const int ntiles = N / APPLY_ROWS;
-  // Vectors of tile t into buffer b: copies for rows of A, plain stores for
-  // the unit rows of block k (rows past N do not occur: N is a multiple of
-  // the tile).
-  auto fetch = [&](int t, float* buf) {
-    const int r0 = t * APPLY_ROWS;
-#pragma unroll
-    for (int i = 0; i < APPLY_ROWS * NB / 4 / APPLY_THREADS; ++i) {
-      const int e = tid + i * APPLY_THREADS, rr = e / (NB / 4), c4 = e % (NB / 4);
-      const int r = r0 + rr;
-      float* dst = buf + rr * LV + 4 * c4;
-      if (!(r >= k && r < s0)) {
-        cp_async16(dst, A + (long long)r * lda + k + 4 * c4);
-      } else {
-        const int u = r - k;
-        *reinterpret_cast<float4*>(dst) = make_float4(4 * c4 == u ? 1.f : 0.f, 4 * c4 + 1 == u ? 1.f : 0.f,
-                                                      4 * c4 + 2 == u ? 1.f : 0.f, 4 * c4 + 3 == u ? 1.f : 0.f);
-      }
-    }
-  };
-  const int t0 = blockIdx.x;
-  if (t0 >= ntiles) return;
-#pragma unroll 4
-  for (int e = tid; e < NB * NB / 4; e += APPLY_THREADS) cp_async16(Lt + 4 * e, LinvT + 4 * e);
-  fetch(t0, Vb);
-  asm volatile("cp.async.commit_group;" ::: "memory");
-  const int warp = tid / 32, lane = tid % 32;
-  const int lr = lane & 15, h = lane >> 4;
-  const int c1 = 8 * warp + 4 * h;          // block w
-  const int c2 = 8 * (15 - warp) + 4 * h;   // block 15 - w
-  const int ua = 8 * warp + 8;              // u bound of block w
-  const int ub = 8 * (16 - warp);           // u bound of block 15 - w
-  int it = 0;
-  for (int t = t0; t < ntiles; t += gridDim.x, ++it) {
-    float* Vs = Vb + (it & 1) * APPLY_ROWS * LV;
-    float* Zs = Vs;  // Z replaces the tile's vectors once all warps are done with them
-    if (t + (int)gridDim.x < ntiles) fetch(t + gridDim.x, Vb + ((it + 1) & 1) * APPLY_ROWS * LV);
-    asm volatile("cp.async.commit_group;\ncp.async.wait_group 1;" ::: "memory");
-    __syncthreads();
-    float acc[2][8];
-#pragma unroll
-    for (int i = 0; i < 2; ++i)
-#pragma unroll
-      for (int c = 0; c < 8; ++c) acc[i][c] = 0.f;
-    const float* v0p = Vs + lr * LV;
-    const float* v1p = Vs + (lr + 16) * LV;
-#pragma unroll 2
-    for (int u4 = 0; u4 < ua / 4; ++u4) {
-      const float4 v0 = *reinterpret_cast<const float4*>(v0p + 4 * u4);
-      const float4 v1 = *reinterpret_cast<const float4*>(v1p + 4 * u4);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float4 la = *reinterpret_cast<const float4*>(Lt + (4 * u4 + j) * NB + c1);
-        const float4 lb = *reinterpret_cast<const float4*>(Lt + (4 * u4 + j) * NB + c2);
-        const float x0 = j == 0 ? v0.x : j == 1 ? v0.y : j == 2 ? v0.z : v0.w;
-        const float x1 = j == 0 ? v1.x : j == 1 ? v1.y : j == 2 ? v1.z : v1.w;
-        acc[0][0] = fmaf(x0, la.x, acc[0][0]); acc[0][1] = fmaf(x0, la.y, acc[0][1]);
-        acc[0][2] = fmaf(x0, la.z, acc[0][2]); acc[0][3] = fmaf(x0, la.w, acc[0][3]);
-        acc[0][4] = fmaf(x0, lb.x, acc[0][4]); acc[0][5] = fmaf(x0, lb.y, acc[0][5]);
-        acc[0][6] = fmaf(x0, lb.z, acc[0][6]); acc[0][7] = fmaf(x0, lb.w, acc[0][7]);
-        acc[1][0] = fmaf(x1, la.x, acc[1][0]); acc[1][1] = fmaf(x1, la.y, acc[1][1]);
-        acc[1][2] = fmaf(x1, la.z, acc[1][2]); acc[1][3] = fmaf(x1, la.w, acc[1][3]);
-        acc[1][4] = fmaf(x1, lb.x, acc[1][4]); acc[1][5] = fmaf(x1, lb.y, acc[1][5]);
-        acc[1][6] = fmaf(x1, lb.z, acc[1][6]); acc[1][7] = fmaf(x1, lb.w, acc[1][7]);
-      }
-    }
-#pragma unroll 2
-    for (int u4 = ua / 4; u4 < ub / 4; ++u4) {
-      const float4 v0 = *reinterpret_cast<const float4*>(v0p + 4 * u4);
-      const float4 v1 = *reinterpret_cast<const float4*>(v1p + 4 * u4);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float4 lb = *reinterpret_cast<const float4*>(Lt + (4 * u4 + j) * NB + c2);
-        const float x0 = j == 0 ? v0.x : j == 1 ? v0.y : j == 2 ? v0.z : v0.w;
-        const float x1 = j == 0 ? v1.x : j == 1 ? v1.y : j == 2 ? v1.z : v1.w;
-        acc[0][4] = fmaf(x0, lb.x, acc[0][4]); acc[0][5] = fmaf(x0, lb.y, acc[0][5]);
-        acc[0][6] = fmaf(x0, lb.z, acc[0][6]); acc[0][7] = fmaf(x0, lb.w, acc[0][7]);
-        acc[1][4] = fmaf(x1, lb.x, acc[1][4]); acc[1][5] = fmaf(x1, lb.y, acc[1][5]);
-        acc[1][6] = fmaf(x1, lb.z, acc[1][6]); acc[1][7] = fmaf(x1, lb.w, acc[1][7]);
-      }
-    }
-    __syncthreads();  // every warp has read the vectors
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      float* z = Zs + (lr + 16 * i) * LV;
-      *reinterpret_cast<float4*>(z + c1) = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
-      *reinterpret_cast<float4*>(z + c2) = make_float4(acc[i][4], acc[i][5], acc[i][6], acc[i][7]);
-    }
-    __syncthreads();
-    // Panel / inverse-row stores: one row of 32 float4 per warp instruction.
-    const int r0 = t * APPLY_ROWS;
-#pragma unroll
-    for (int i = 0; i < APPLY_ROWS * NB / 4 / APPLY_THREADS; ++i) {
-      const int e = tid + i * APPLY_THREADS, rr = e / (NB / 4), c4 = e % (NB / 4);
-      const int r = r0 + rr;
-      const float4 z = *reinterpret_cast<const float4*>(Zs + rr * LV + 4 * c4);
-      const bool panel = r >= s0;
-      const long long off = (long long)r * PW + col0 + 4 * c4;
-      float4 hv, lv;
-      split_tf32(z.x, hv.x, lv.x);
-      split_tf32(z.y, hv.y, lv.y);
-      split_tf32(z.z, hv.z, lv.z);
-      split_tf32(z.w, hv.w, lv.w);
-      *reinterpret_cast<float4*>((panel ? P_hi : Y_hi) + off) = hv;
-      *reinterpret_cast<float4*>((panel ? P_lo : Y_lo) + off) = lv;
-      if (panel && r < zero_end) {
-        // Rows of the next block: their part of Yp in this half is X[block k][r] = 0.
-        *reinterpret_cast<float4*>(Y_hi + off) = make_float4(0.f, 0.f, 0.f, 0.f);
-        *reinterpret_cast<float4*>(Y_lo + off) = make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-    }
-    // Entries of U: for a fixed output column c, consecutive rows r are
-    // consecutive (descending) columns of U's row n-1-(k+c).
-    if (r0 < s0 && r0 < n) {
-      const int rr = tid % APPLY_ROWS;
-      const int r = r0 + rr;
-      if (r < s0 && r < n) {
-        const int m = n - 1 - r;
-        const float rdm = __frcp_rn(dabs[m]);  // U is compared within a tolerance: scale by 1/|d|
-#pragma unroll 4
-        for (int c = tid / APPLY_ROWS; c < NB; c += APPLY_THREADS / APPLY_ROWS) {
-          const int i = k + c;
-          if (i < n) U[(long long)(n - 1 - i) * n + m] = __fmul_rn(Zs[rr * LV + c], rdm);
-        }
-      }
-    }
-    __syncthreads();  // Z is read out before the buffer takes the tile after next
-  }
-  asm volatile("cp.async.wait_group 0;" ::: "memory");
-}
 
 // Act-order channel order ([host page] act_order_perm): descending H_ii in
 // Rust's total order on f32 (NaN and -0.0 ordered), ties by ascending index.
@@ -361,7 +200,8 @@ struct FoldWs {
   float* P_lo;
   float* Yp_hi;   // N x PW   (Y panels of the current pair of steps, TF32 hi/lo)
   float* Yp_lo;
-  float* Lkk;     // NB x NB: inverse of the current diagonal block of L, transposed
+  float* Lhi;     // NB x NB: inverse of the current diagonal block of L, TF32 hi
+  float* Llo;     //          and lo parts, row-major
   float* hdiag;   // n
   float* dabs;    // n
   double* base;   // 1
@@ -377,7 +217,8 @@ static bool carve_fold(Carve& c, int n, FoldWs& w) {
   w.P_lo = c.take<float>(N * PW);
   w.Yp_hi = c.take<float>(N * PW);
   w.Yp_lo = c.take<float>(N * PW);
-  w.Lkk = c.take<float>((size_t)NB * NB);
+  w.Lhi = c.take<float>((size_t)NB * NB);
+  w.Llo = c.take<float>((size_t)NB * NB);
   w.hdiag = c.take<float>((size_t)n);
   w.dabs = c.take<float>((size_t)n);
   w.base = c.take<double>(1);
@@ -393,21 +234,20 @@ size_t fold_ws_bytes(int n) {
 }
 
 constexpr int POTRF_SMEM = POTRF_SMEM_BYTES;
-constexpr int APPLY_SMEM = (NB * NB + 2 * APPLY_ROWS * LV) * 4;
 
 static gptq_status init_attrs() {
   static DeviceOnce once;
   return once.run([](int) -> gptq_status {
     GQ_CUDA(cudaFuncSetAttribute(k_potrf, cudaFuncAttributeMaxDynamicSharedMemorySize, POTRF_SMEM));
-    GQ_CUDA(cudaFuncSetAttribute(k_apply, cudaFuncAttributeMaxDynamicSharedMemorySize, APPLY_SMEM));
     return GPTQ_OK;
   });
 }
 
 // One factorisation attempt at damping lam: build, interleaved Cholesky +
 // inverse, U.  The pivot flag is left on the device.
-static gptq_status fold_attempt(const float* hp, const FoldWs& w, const OperandMaps& maps,
+static gptq_status fold_attempt(const float* hp, const FoldWs& w, const ApplyMaps& am,
                                 double lam, float* U, float* D, cudaStream_t s, const int* perm) {
+  const OperandMaps& maps = am.p;
   const int n = w.n, N = w.N;
   const long long ld = N;
   GQ_CUDA(cudaMemsetAsync(w.flag, 0, sizeof(unsigned), s));
@@ -432,19 +272,12 @@ static gptq_status fold_attempt(const float* hp, const FoldWs& w, const OperandM
   // right after the thin strip (the strip's own tiles are done within
   // microseconds, so nothing would hide it there), as does the very first.
   auto apply = [&](int k, int col0, int zero_end) -> gptq_status {
-    GQ_PROF(K_TRSM, s);
-    const int tiles = N / APPLY_ROWS;
-    const int ctas = 2 * num_sms();  // two CTAs per SM
-    k_apply<<<tiles < ctas ? tiles : ctas, APPLY_THREADS, APPLY_SMEM, s>>>(w.A, ld, k, k + NB, N, col0, zero_end,
-                                                               w.Lkk, w.P_hi, w.P_lo, w.Yp_hi,
-                                                               w.Yp_lo, w.flag, U, w.dabs, n);
-    GQ_LAUNCHED();
-    return GPTQ_OK;
+    return apply_tc_run(am, k, k + NB, N, col0, zero_end, w.flag, U, w.dabs, n, s);
   };
-  auto fused = [&](int k) { return FusedPotrf{w.A, ld, k, w.Lkk, 1}; };
+  auto fused = [&](int k) { return FusedPotrf{w.A, ld, k, w.Lhi, w.Llo, 1}; };
   {
     GQ_PROF(K_POTRF, s);
-    k_potrf<<<1, 256, POTRF_SMEM, s>>>(w.A, ld, 0, w.Lkk, w.flag);
+    k_potrf<<<1, 256, POTRF_SMEM, s>>>(w.A, ld, 0, w.Lhi, w.Llo, w.flag);
     GQ_LAUNCHED();
   }
   // maps: 0/1 = P hi/lo, 2/3 = Yp hi/lo (K = 2 NB wide).
@@ -462,7 +295,7 @@ static gptq_status fold_attempt(const float* hp, const FoldWs& w, const OperandM
         GQ_TRY(gemm_tc_sub(maps, syrk, inv, NB, w.flag, w.flag, K_FOLD_STRIP, s));
         {
           GQ_PROF(K_POTRF, s);
-          k_potrf<<<1, 256, POTRF_SMEM, s>>>(w.A, ld, k1, w.Lkk, w.flag);
+          k_potrf<<<1, 256, POTRF_SMEM, s>>>(w.A, ld, k1, w.Lhi, w.Llo, w.flag);
           GQ_LAUNCHED();
         }
       }
@@ -501,15 +334,19 @@ gptq_status fold_run(const float* hp, int n, double lambda, float* U, float* D, 
   }
   if (hdiag) GQ_CUDA(cudaMemcpyAsync(hdiag, w.hdiag, (size_t)n * 4, cudaMemcpyDeviceToDevice, s));
   GQ_CUDA(cudaMemsetAsync(U, 0, (size_t)n * n * 4, s));
-  OperandMaps maps;
+  ApplyMaps am;
+  OperandMaps& maps = am.p;
   GQ_TRY(make_operand_map(&maps.m[0], w.P_hi, w.N, PW));
   GQ_TRY(make_operand_map(&maps.m[1], w.P_lo, w.N, PW));
   GQ_TRY(make_operand_map(&maps.m[2], w.Yp_hi, w.N, PW));
   GQ_TRY(make_operand_map(&maps.m[3], w.Yp_lo, w.N, PW));
   GQ_TRY(make_c_map(&maps.c, w.A, w.N, w.N, w.N));
+  am.a = maps.c;  // the panel product loads A's vectors in the same boxes
+  GQ_TRY(make_operand_map(&am.lhi, w.Lhi, NB, NB, 32));
+  GQ_TRY(make_operand_map(&am.llo, w.Llo, NB, NB, 32));
   double lam = lambda > 0.0 ? lambda : 0.0;
   for (;;) {
-    GQ_TRY(fold_attempt(hp, w, maps, lam, U, D, s, perm));
+    GQ_TRY(fold_attempt(hp, w, am, lam, U, D, s, perm));
     unsigned hflag = 0;
     GQ_CUDA(cudaMemcpyAsync(&hflag, w.flag, sizeof(unsigned), cudaMemcpyDeviceToHost, s));
     GQ_CUDA(cudaStreamSynchronize(s));

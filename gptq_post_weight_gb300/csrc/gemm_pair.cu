@@ -298,7 +298,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
     // plain loads, then run the diagonal-block step on the finished block.
     if (threadIdx.x == 64) asm volatile("fence.proxy.async.global;" ::: "memory");
     __syncthreads();
-    potrf_inverse_block(fp.A + (long long)fp.k * fp.lda + fp.k, fp.lda, fp.LinvT, status,
+    potrf_inverse_block(fp.A + (long long)fp.k * fp.lda + fp.k, fp.lda, fp.Lhi, fp.Llo, status,
                         reinterpret_cast<float*>(smem));
   }
 }

@@ -320,7 +320,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     // load has landed and every MMA has retired).
     if (threadIdx.x == 64) asm volatile("fence.proxy.async.global;" ::: "memory");
     __syncthreads();
-    potrf_inverse_block(fp.A + (long long)fp.k * fp.lda + fp.k, fp.lda, fp.LinvT, status,
+    potrf_inverse_block(fp.A + (long long)fp.k * fp.lda + fp.k, fp.lda, fp.Lhi, fp.Llo, status,
                         reinterpret_cast<float*>(smem));
   }
 }
@@ -379,13 +379,14 @@ int num_sms() {
 }
 
 
-gptq_status make_operand_map(CUtensorMap* m, const float* base, long long rows, int K) {
+gptq_status make_operand_map(CUtensorMap* m, const float* base, long long rows, int K, int box_rows) {
   auto fn = encode_fn();
   if (fn == nullptr) return GPTQ_ERR_CUDA;
   if ((reinterpret_cast<uintptr_t>(base) & 15u) != 0 || K % BK != 0) return GPTQ_ERR_ARG;
+  if (box_rows <= 0 || box_rows > 256 || box_rows % 8 != 0) return GPTQ_ERR_ARG;
   cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)K * 4u};
-  cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)BM};
+  cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
   cuuint32_t es[2] = {1u, 1u};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims, strides, box, es,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,

@@ -23,13 +23,15 @@ constexpr int POTRF_SMEM_BYTES = 3 * NB * LDS * 4;
 // sum_{j <= m < i} L_im X_mj, as register-tiled block products.  Loops stay
 // rolled where unrolling buys little: the step runs once per block column on
 // whichever SM its CTA lands on, mostly from a cold instruction cache.
-// Output: LinvT = Linv transposed (NB x NB, LinvT[c][r] = Linv[r][c], zeros
-// below its diagonal).
+// Output: Linv itself as its TF32 hi/lo split (NB x NB row-major each,
+// zeros above the diagonal): the K-major operand of the panel product on
+// the tensor cores.
 // Runs on the whole CTA (any multiple of 32 threads >= 128); S is at least
 // POTRF_SMEM_BYTES of shared memory.  The block starts at Ablk (leading
 // dimension lda); it is read with L1-bypassing loads.
 static __device__ __noinline__ void potrf_inverse_block(const float* __restrict__ Ablk, long long lda,
-                                                 float* __restrict__ LinvT, unsigned* flag, float* S) {
+                                                 float* __restrict__ Lhi, float* __restrict__ Llo,
+                                                 unsigned* flag, float* S) {
   float* Li = S + NB * LDS;
   float* T = Li + NB * LDS;
   __shared__ float rinv[NB];
@@ -255,11 +257,12 @@ static __device__ __noinline__ void potrf_inverse_block(const float* __restrict_
     }
     __syncthreads();
   }
-  // Column-major (the transpose, row-contiguous for its consumer); Li's
-  // odd stride keeps the column reads free of bank conflicts.
   for (int e = tid; e < NB * NB; e += NT) {
-    const int c = e / NB, r = e % NB;
-    LinvT[e] = (c <= r) ? Li[r * LDS + c] : 0.f;
+    const int r = e / NB, c = e % NB;
+    float h = 0.f, l = 0.f;
+    if (c <= r) split_tf32(Li[r * LDS + c], h, l);
+    Lhi[e] = h;
+    Llo[e] = l;
   }
 }
 

@@ -77,9 +77,21 @@ static __device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map,
       "r"(x), "r"(y), "r"(src)
       : "memory");
 }
+// TMA store of a 128 x 32 f32 slice (128-byte swizzled in shared memory)
+// to the tensor at (x, y); completion tracked per bulk group.
+static __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(x), "r"(y), "r"(src)
+      : "memory");
+}
 static __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 static __device__ __forceinline__ void bulk_wait_read1() {
   asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+static __device__ __forceinline__ void bulk_wait_read0() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 static __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 static __device__ __forceinline__ void fence_proxy_async_smem() {
