@@ -267,10 +267,13 @@ def test_full_size_group(lib, name, oracle_folds):
     del hpd, wd
     uo, do, dead, lamo = oracle_folds(hp, cfg.n, cfg.lam, key=(cfg.name, cfg.seed))
     assert out["lam"] == lamo
-    assert rel_fro(np_(out["u"]), uo) <= 1e-4
+    u_err = rel_fro(np_(out["u"]), uo)
+    assert u_err <= 1e-4
     rng = np.random.default_rng(0)
     rows_idx = np.sort(rng.choice(cfg.rows, 24, replace=False))
     agree, rung_agree, e_dev, e_or = _compare_e2e(hp, w, cfg.n, rows_idx, out, uo=uo)
+    print(f"{name}: U rel err {u_err:.3e}, codes {agree:.5f}, rungs {rung_agree:.5f}, "
+          f"output error {e_dev:.6g} vs {e_or:.6g}")
     assert agree >= 0.999, agree
     assert rung_agree >= 0.999, rung_agree
     assert abs(e_dev - e_or) <= 0.01 * e_or, (e_dev, e_or)
