@@ -7,7 +7,8 @@
 //    v = Y[r][k .. k+NB) (for the rows of block k itself the unit vector
 //    e_{r-k}: that row of Z is a column of Linv), z -> the buffer Yp, and
 //    the finished entries of U ([fold page] make_u):
-//    U[n-1-i][n-1-r] = X[i][r] / |d_{n-1-r}|, i = k + c, taken as X times
+//    U[n-1-i][n-1-r] = X[i][r] / |d_{n-1-r}|, i = k + c (d given with a dead
+//    channel's sign), taken as X times
 //    the rounded reciprocal (within a rounding of the quotient);
 //  * rows of the next block (s0 <= r < zero_end): their Yp entries in this
 //    half are zero (X is lower triangular).
@@ -21,9 +22,9 @@
 // of Z: its MMAs run with N = NB - 32 kc into the accumulator's columns
 // from 32 kc, and only Linv's rows c >= 32 kc are loaded (boxes of 32
 // rows).  That keeps the whole tile's operands in 208 KB of shared memory.
-//   warp 0      TMA producer: per slice, the tile's raw f32 vectors (a
-//               128 x 32 box of A, 128-byte swizzle) and the rows of the
-//               TF32 pair of Linv the slice meets;
+//   warp 0      TMA producers, lane kc for slice kc: the tile's raw f32
+//               vectors (a 128 x 32 box of A, 128-byte swizzle) and the rows
+//               of the TF32 pair of Linv the slice meets;
 //   warps 2-5   split each slice's raw vectors into their TF32 pair in place
 //               (the unit rows of block k written directly), then, once the
 //               product is in tensor memory, the epilogue: tcgen05.ld of one
@@ -84,7 +85,7 @@ __global__ void __launch_bounds__(A_THREADS, 1)
                const __grid_constant__ CUtensorMap llo_map, const __grid_constant__ CUtensorMap phi_map,
                const __grid_constant__ CUtensorMap plo_map, const __grid_constant__ CUtensorMap yhi_map,
                const __grid_constant__ CUtensorMap ylo_map, int k, int s0, int N, int col0, int zero_end,
-               unsigned* flag, float* __restrict__ U, const float* __restrict__ dabs, int n, WaitCfg wc) {
+               unsigned* flag, float* __restrict__ U, const float* __restrict__ dsg, int n, WaitCfg wc) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   // full[kc]: slice kc landed; conv[kc]: slice kc split; tfull: the tile's
@@ -92,7 +93,9 @@ __global__ void __launch_bounds__(A_THREADS, 1)
   // operand area and tensor memory (the next tile may load).
   __shared__ __align__(8) uint64_t full[ANCH], conv[ANCH], tfull, ofree, drain;
   __shared__ uint32_t tmem_base_sh;
-  __shared__ int abort_sh, skip_sh, tiles_issued_sh;
+  __shared__ int abort_sh, skip_sh, issued_sh[ANCH];
+  pdl_trigger();
+  pdl_wait();  // the previous kernel's writes (A, Linv, the flag) are visible
   if (threadIdx.x == 0) skip_sh = (*(volatile const unsigned*)flag != 0u) ? 1 : 0;
   __syncthreads();
   if (skip_sh) return;
@@ -108,7 +111,7 @@ __global__ void __launch_bounds__(A_THREADS, 1)
     mbar_init(&ofree, 1);
     mbar_init(&drain, 1);
     abort_sh = 0;
-    tiles_issued_sh = 0;
+    for (int c = 0; c < ANCH; ++c) issued_sh[c] = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 1) {
@@ -126,24 +129,24 @@ __global__ void __launch_bounds__(A_THREADS, 1)
   uint8_t* const larea = smem + V_AREA;  // Linv hi part, then lo part
 
   if (warp == 0) {
-    if (lane == 0) {
+    if (lane < ANCH) {
+      // Lane kc issues slice kc's loads (the four slices' loads go out side
+      // by side).
+      const int kc = lane;
       int it = 0;
       // wc.no_loads (a test hook): issue nothing; the waits below run out.
       for (int t = blockIdx.x; t < ntiles && !*abort && !wc.no_loads; t += gridDim.x, ++it) {
         if (it > 0 && !mbar_wait(&ofree, (uint32_t)((it - 1) & 1), abort, wc.ns)) break;
         const int r0 = t * AM;
+        mbar_expect_tx(&full[kc], A_BOX + 2 * (ANCH - kc) * L_BOX);
+        tma_load_2d(smem_u32(smem + kc * 2 * A_BOX), &amap, k + kc * AK, r0, &full[kc]);
 #pragma unroll 1
-        for (int kc = 0; kc < ANCH; ++kc) {
-          mbar_expect_tx(&full[kc], A_BOX + 2 * (ANCH - kc) * L_BOX);
-          tma_load_2d(smem_u32(smem + kc * 2 * A_BOX), &amap, k + kc * AK, r0, &full[kc]);
-#pragma unroll 1
-          for (int cb = kc; cb < ANCH; ++cb) {
-            const uint32_t o = (uint32_t)(l_off(kc) + (cb - kc) * L_BOX);
-            tma_load_2d(smem_u32(larea + o), &lhi_map, kc * AK, cb * 32, &full[kc]);
-            tma_load_2d(smem_u32(larea + L_AREA + o), &llo_map, kc * AK, cb * 32, &full[kc]);
-          }
+        for (int cb = kc; cb < ANCH; ++cb) {
+          const uint32_t o = (uint32_t)(l_off(kc) + (cb - kc) * L_BOX);
+          tma_load_2d(smem_u32(larea + o), &lhi_map, kc * AK, cb * 32, &full[kc]);
+          tma_load_2d(smem_u32(larea + L_AREA + o), &llo_map, kc * AK, cb * 32, &full[kc]);
         }
-        tiles_issued_sh = it + 1;
+        issued_sh[kc] = it + 1;
       }
     }
   } else if (warp == 1) {
@@ -228,14 +231,13 @@ __global__ void __launch_bounds__(A_THREADS, 1)
       const CUtensorMap* mh = panel ? &phi_map : &yhi_map;
       const CUtensorMap* ml = panel ? &plo_map : &ylo_map;
       const bool uok = !panel && r < n;
-      const float rdm = uok ? __frcp_rn(dabs[n - 1 - r]) : 0.f;
+      const float rdm = uok ? __frcp_rn(fabsf(dsg[n - 1 - r])) : 0.f;
       float* ucol = U + (n - 1 - r);  // column n-1-r of U
       const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16);
 #pragma unroll 1
       for (int cc = 0; cc < NB; cc += 32) {
         uint32_t v[32];
-        tmem_ld16(tbase + (uint32_t)cc, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
-        tmem_ld16(tbase + (uint32_t)cc + 16u, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
+        tmem_ld32(tbase + (uint32_t)cc, v);
         tmem_ld_wait();
         // Staging: the first two slices' V areas (hi slice, then lo slice).
         uint8_t* buf = smem + (chunk & 1) * 2 * A_BOX;
@@ -252,7 +254,7 @@ __global__ void __launch_bounds__(A_THREADS, 1)
           *reinterpret_cast<float4*>(buf + A_BOX + off) = lo;
         }
         if (uok) {
-#pragma unroll 8
+#pragma unroll
           for (int j = 0; j < 32; ++j) {
             const int i = k + cc + j;
             if (i < n) ucol[(long long)(n - 1 - i) * n] = __fmul_rn(__uint_as_float(v[j]), rdm);
@@ -300,14 +302,13 @@ __global__ void __launch_bounds__(A_THREADS, 1)
 
   __syncthreads();
   if (threadIdx.x == 0 && abort_sh) {
-    // Loads issued for the last tile may still target this CTA's shared
-    // memory: wait (bounded) for each slice to land before the CTA exits.
-    const int ti = tiles_issued_sh;
-    if (ti > 0) {
-      for (int kc = 0; kc < ANCH; ++kc) {
-        const uint64_t t0 = globaltimer();
-        while (!mbar_try_wait(&full[kc], (uint32_t)((ti - 1) & 1)) && globaltimer() - t0 < wc.ns) {
-        }
+    // Loads issued for a slice's last tile may still target this CTA's
+    // shared memory: wait (bounded) for each to land before the CTA exits.
+    for (int kc = 0; kc < ANCH; ++kc) {
+      const int ti = issued_sh[kc];
+      if (ti == 0) continue;
+      const uint64_t t0 = globaltimer();
+      while (!mbar_try_wait(&full[kc], (uint32_t)((ti - 1) & 1)) && globaltimer() - t0 < wc.ns) {
       }
     }
     atomicOr(flag, 2u);
@@ -325,7 +326,7 @@ DeviceOnce g_apply_attr;
 }  // namespace
 
 gptq_status apply_tc_run(const ApplyMaps& am, int k, int s0, int N, int col0, int zero_end, unsigned* flag,
-                         float* U, const float* dabs, int n, cudaStream_t s) {
+                         float* U, const float* dsg, int n, cudaStream_t s) {
   GQ_TRY(g_apply_attr.run([](int) -> gptq_status {
     GQ_CUDA(cudaFuncSetAttribute(k_apply_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, A_SMEM));
     return GPTQ_OK;
@@ -334,9 +335,8 @@ gptq_status apply_tc_run(const ApplyMaps& am, int k, int s0, int N, int col0, in
   const int ntiles = N / AM;
   const int grid = ntiles < num_sms() ? ntiles : num_sms();
   GQ_PROF(K_TRSM, s);
-  k_apply_tc<<<grid, A_THREADS, A_SMEM, s>>>(am.a, am.lhi, am.llo, am.p.m[0], am.p.m[1], am.p.m[2], am.p.m[3],
-                                            k, s0, N, col0, zero_end, flag, U, dabs, n, wait_cfg());
-  GQ_LAUNCHED();
+  GQ_CUDA(launch_pdl(k_apply_tc, dim3(grid), dim3(A_THREADS), A_SMEM, s, am.a, am.lhi, am.llo, am.p.m[0],
+                     am.p.m[1], am.p.m[2], am.p.m[3], k, s0, N, col0, zero_end, flag, U, dsg, n, wait_cfg()));
   return GPTQ_OK;
 }
 
