@@ -23,6 +23,8 @@ gptq_status sweep_act_run(const float* W, int rows, int n, const float* Up, cons
 gptq_status build_only(const float* hp, int n, double lambda, float* A, float* D, void* ws,
                        size_t ws_bytes, cudaStream_t s);
 gptq_status ladder_run(const float* W, int rows, int n, float* tab, float* lost, cudaStream_t s);
+gptq_status copy_ladder_run(const float* W, int rows, int n, const float* hdiag, float* wz, float* tab,
+                            float* lost, cudaStream_t s);
 gptq_status group_run(const float* tile, int rows, const float* ublk, const float* hw,
                       const float* tab, const float* lost, uint8_t* nib, uint8_t* rungs,
                       float* scales, float* E, cudaStream_t s);
@@ -178,8 +180,7 @@ gptq_status gptq_quantize_group(const float* H_packed, int n, double lambda, con
   void* rest = static_cast<char*>(ws) + off;
   const size_t rest_bytes = ws_bytes - off;
   GQ_TRY(fold_run(H_packed, n, lambda, u, d, hd, lambda_used, rest, rest_bytes, s));
-  GQ_TRY(copy_dead_zeroed(W, rows, n, hd, wz, s));
-  GQ_TRY(ladder_run(wz, rows, n, tb, ls, s));
+  GQ_TRY(copy_ladder_run(W, rows, n, hd, wz, tb, ls, s));
   return sweep_run(wz, rows, n, u, hd, tb, ls, nibbles, rungs, scales, rest, rest_bytes, s);
 }
 
@@ -351,8 +352,7 @@ gptq_status gptq_quantize_group_act_order(const float* H_packed, int n, double l
   GQ_TRY(diag_run(H_packed, n, hraw, s));
   GQ_TRY(perm_run(hraw, n, perm, s));
   GQ_TRY(fold_run(H_packed, n, lambda, u, d, hperm, lambda_used, rest, rest_bytes, s, perm));
-  GQ_TRY(copy_dead_zeroed(W, rows, n, hraw, wz, s));
-  GQ_TRY(ladder_run(wz, rows, n, tb, ls, s));
+  GQ_TRY(copy_ladder_run(W, rows, n, hraw, wz, tb, ls, s));
   GQ_TRY(static_rungs_run(wz, rows, n, tb, ls, rungs, scales, s));
   return sweep_act_run(wz, rows, n, u, perm, tb, rungs, nibbles, rest, rest_bytes, s);
 }

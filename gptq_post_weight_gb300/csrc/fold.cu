@@ -63,11 +63,12 @@ __global__ void __launch_bounds__(1024) k_diag(const float* __restrict__ hp, int
   }
 }
 
-// Per attempt: |d_k| = sqrt(H_kk + damp) (sqrt(1 + damp) for a dead channel;
-// make_u divides by it, the builder never uses it for a dead row/column) and
-// the signed D of the fold page (-sqrt(1 + damp) marks a dead channel).
+// Per attempt: d_k = sqrt(H_kk + damp) and, for a dead channel, the fold
+// page's signed D: -sqrt(1 + damp) (make_u divides by |d|; the builder
+// never uses |d| of a dead row/column).  The working copy keeps the sign,
+// so one load tells the builder both |d| and deadness.
 __global__ void k_dvec(int n, const float* __restrict__ hdiag, const double* __restrict__ base,
-                       double lam, float* __restrict__ Dsigned, float* __restrict__ dabs) {
+                       double lam, float* __restrict__ Dsigned, float* __restrict__ dsg) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= n) return;
   const double damp = lam * (*base);
@@ -75,18 +76,20 @@ __global__ void k_dvec(int n, const float* __restrict__ hdiag, const double* __r
   const bool dead = !(h > 0.f);
   const float d = dead ? -(float)sqrt(1.0 + damp) : (float)sqrt((double)h + damp);
   if (Dsigned) Dsigned[i] = d;
-  dabs[i] = fabsf(d);
+  dsg[i] = d;
 }
 
 // One row i of A: lower part = equilibrated reversed damped H, upper part
 // zero (initial Y), padding rows identity.  [fold page] build_a.  With a
 // permutation (act order, host page's permute_sym) the matrix is
 // H[perm][perm]: its entries are gathered from the packed triangle.
+// Each thread fills four consecutive columns per pass (their packed-H and
+// d loads in flight together) and stores them as one float4; the packed
+// row is read once (streaming) and A written once (streaming).
 __global__ void __launch_bounds__(256) k_build(const float* __restrict__ hp, int n, int N,
                                                const int* __restrict__ perm,
-                                               const float* __restrict__ hdiag,
                                                const double* __restrict__ base, double lam,
-                                               const float* __restrict__ dabs,
+                                               const float* __restrict__ dsg,
                                                float* __restrict__ A, long long lda,
                                                int write_upper) {
   const int i = blockIdx.x;
@@ -98,31 +101,48 @@ __global__ void __launch_bounds__(256) k_build(const float* __restrict__ hp, int
   }
   const float dampf = (float)(lam * (*base));
   const int ii = n - 1 - i;
-  const bool dead_i = !(hdiag[ii] > 0.f);
-  const float di = dabs[ii];
+  const float sdi = dsg[ii];
+  const bool dead_i = sdi < 0.f;
+  const float di = fabsf(sdi);
   const long long prow = poff(ii, n);
   const int jend = write_upper ? N : i + 1;
-  for (int j = threadIdx.x; j < jend; j += blockDim.x) {
-    float v = 0.f;
-    if (j <= i) {
-      const int jj = n - 1 - j;  // jj >= ii
-      const bool dead_j = !(hdiag[jj] > 0.f);
-      if (dead_i || dead_j) {
-        v = (ii == jj) ? 1.f : 0.f;
+  // Columns j > i are zero (the upper part and the padding); the lower part
+  // needs H[ii][jj], jj = n-1-j >= ii.
+  auto entry = [&](int j) -> float {
+    if (j > i) return 0.f;
+    const int jj = n - 1 - j;  // jj >= ii
+    const float sdj = dsg[jj];
+    if (dead_i || sdj < 0.f) return (ii == jj) ? 1.f : 0.f;
+    float h;
+    if (perm) {
+      const int pa = perm[ii], pb = perm[jj];
+      const int a = pa < pb ? pa : pb, b = pa < pb ? pb : pa;
+      h = __ldcs(hp + poff(a, n) + (b - a));
+    } else {
+      h = __ldcs(hp + prow + (jj - ii));
+    }
+    if (ii == jj) h = __fadd_rn(h, dampf);
+    return __fdiv_rn(h, __fmul_rn(di, sdj));
+  };
+  if ((lda & 3) == 0) {
+    // Four columns per thread and pass; lda is a multiple of 4, so the
+    // float4 stores are aligned.
+    for (int j0 = 4 * threadIdx.x; j0 < jend; j0 += 4 * blockDim.x) {
+      float4 v;
+      v.x = entry(j0);
+      v.y = j0 + 1 < jend ? entry(j0 + 1) : 0.f;
+      v.z = j0 + 2 < jend ? entry(j0 + 2) : 0.f;
+      v.w = j0 + 3 < jend ? entry(j0 + 3) : 0.f;
+      if (j0 + 3 < jend) {
+        __stcs(reinterpret_cast<float4*>(arow + j0), v);
       } else {
-        float h;
-        if (perm) {
-          const int pa = perm[ii], pb = perm[jj];
-          const int a = pa < pb ? pa : pb, b = pa < pb ? pb : pa;
-          h = hp[poff(a, n) + (b - a)];
-        } else {
-          h = hp[prow + (jj - ii)];
-        }
-        if (ii == jj) h = __fadd_rn(h, dampf);
-        v = __fdiv_rn(h, __fmul_rn(di, dabs[jj]));
+        arow[j0] = v.x;
+        if (j0 + 1 < jend) arow[j0 + 1] = v.y;
+        if (j0 + 2 < jend) arow[j0 + 2] = v.z;
       }
     }
-    arow[j] = v;
+  } else {
+    for (int j = threadIdx.x; j < jend; j += blockDim.x) arow[j] = entry(j);
   }
 }
 
@@ -130,6 +150,8 @@ __global__ void __launch_bounds__(256) k_build(const float* __restrict__ hp, int
 __global__ void __launch_bounds__(256) k_potrf(const float* __restrict__ A, long long lda, int k,
                                                float* __restrict__ Lhi, float* __restrict__ Llo,
                                                unsigned* flag) {
+  pdl_trigger();
+  pdl_wait();  // the previous kernel's writes (A, the flag) are visible
   if (flagged(flag)) return;
   extern __shared__ float S[];
   potrf_inverse_block(A + (long long)k * lda + k, lda, Lhi, Llo, flag, S);
@@ -203,7 +225,7 @@ struct FoldWs {
   float* Lhi;     // NB x NB: inverse of the current diagonal block of L, TF32 hi
   float* Llo;     //          and lo parts, row-major
   float* hdiag;   // n
-  float* dabs;    // n
+  float* dsg;     // n: d with a dead channel's sign (see k_dvec)
   double* base;   // 1
   unsigned* flag; // 1 (+pad)
 };
@@ -220,7 +242,7 @@ static bool carve_fold(Carve& c, int n, FoldWs& w) {
   w.Lhi = c.take<float>((size_t)NB * NB);
   w.Llo = c.take<float>((size_t)NB * NB);
   w.hdiag = c.take<float>((size_t)n);
-  w.dabs = c.take<float>((size_t)n);
+  w.dsg = c.take<float>((size_t)n);
   w.base = c.take<double>(1);
   w.flag = c.take<unsigned>(4);
   return c.ok;
@@ -253,9 +275,9 @@ static gptq_status fold_attempt(const float* hp, const FoldWs& w, const ApplyMap
   GQ_CUDA(cudaMemsetAsync(w.flag, 0, sizeof(unsigned), s));
   {
     GQ_PROF(K_BUILD, s);
-    k_dvec<<<(n + 255) / 256, 256, 0, s>>>(n, w.hdiag, w.base, lam, D, w.dabs);
+    k_dvec<<<(n + 255) / 256, 256, 0, s>>>(n, w.hdiag, w.base, lam, D, w.dsg);
     GQ_LAUNCHED();
-    k_build<<<N, 256, 0, s>>>(hp, n, N, perm, w.hdiag, w.base, lam, w.dabs, w.A, ld, 1);
+    k_build<<<N, 256, 0, s>>>(hp, n, N, perm, w.base, lam, w.dsg, w.A, ld, 1);
     GQ_LAUNCHED();
   }
   // Steps go in pairs (k, k + NB) while two blocks remain:
@@ -272,7 +294,7 @@ static gptq_status fold_attempt(const float* hp, const FoldWs& w, const ApplyMap
   // right after the thin strip (the strip's own tiles are done within
   // microseconds, so nothing would hide it there), as does the very first.
   auto apply = [&](int k, int col0, int zero_end) -> gptq_status {
-    return apply_tc_run(am, k, k + NB, N, col0, zero_end, w.flag, U, w.dabs, n, s);
+    return apply_tc_run(am, k, k + NB, N, col0, zero_end, w.flag, U, w.dsg, n, s);
   };
   auto fused = [&](int k) { return FusedPotrf{w.A, ld, k, w.Lhi, w.Llo, 1}; };
   {
@@ -295,8 +317,7 @@ static gptq_status fold_attempt(const float* hp, const FoldWs& w, const ApplyMap
         GQ_TRY(gemm_tc_sub(maps, syrk, inv, NB, w.flag, w.flag, K_FOLD_STRIP, s));
         {
           GQ_PROF(K_POTRF, s);
-          k_potrf<<<1, 256, POTRF_SMEM, s>>>(w.A, ld, k1, w.Lhi, w.Llo, w.flag);
-          GQ_LAUNCHED();
+          GQ_CUDA(launch_pdl(k_potrf, dim3(1), dim3(256), POTRF_SMEM, s, w.A, ld, k1, w.Lhi, w.Llo, w.flag));
         }
       }
       GQ_TRY(apply(k1, NB, 0));
@@ -372,9 +393,9 @@ gptq_status build_only(const float* hp, int n, double lambda, float* A, float* D
   // Rows of the caller's n x n matrix, lower triangle only.
   GQ_PROF(K_BUILD, s);
   const double lam = lambda > 0 ? lambda : 0.0;
-  k_dvec<<<(n + 255) / 256, 256, 0, s>>>(n, w.hdiag, w.base, lam, D, w.dabs);
+  k_dvec<<<(n + 255) / 256, 256, 0, s>>>(n, w.hdiag, w.base, lam, D, w.dsg);
   GQ_LAUNCHED();
-  k_build<<<n, 256, 0, s>>>(hp, n, n, nullptr, w.hdiag, w.base, lam, w.dabs, A, n, 0);
+  k_build<<<n, 256, 0, s>>>(hp, n, n, nullptr, w.base, lam, w.dsg, A, n, 0);
   GQ_LAUNCHED();
   return GPTQ_OK;
 }

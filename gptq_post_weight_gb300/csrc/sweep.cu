@@ -130,26 +130,54 @@ __device__ __forceinline__ void q4tp_round(float (&w)[GROUP], float s, const flo
 }
 
 // Per-row ladder ([host page] gptq_quantize_q4tp_dev's tab / lost; the
-// converter itself is not on the pages -- reading in the header).
-__global__ void __launch_bounds__(128) k_ladder(const float* __restrict__ W, int n,
-                                                float* __restrict__ tab, float* __restrict__ lost) {
+// converter itself is not on the pages -- reading in the header).  With DZ
+// the kernel also writes the dead-zeroed copy of W ([host page]
+// gptq_quantize_q4tp_dev: "zero the dead columns", !(H_ii > 0)) and takes
+// the ladder from it: W is read once and its copy written once.
+// One CTA per row, streaming: consecutive threads take consecutive float4s
+// of the row (four passes in flight per thread), so the eight float4s of a
+// group sit in eight consecutive lanes and its absmax is a three-step
+// shuffle reduction.
+constexpr int LADDER_THREADS = 256;
+template <bool DZ>
+__global__ void __launch_bounds__(LADDER_THREADS) k_ladder(const float* __restrict__ W, int n,
+                                                           float* __restrict__ tab, float* __restrict__ lost,
+                                                           const float* __restrict__ hdiag,
+                                                           float* __restrict__ wz) {
   const int r = blockIdx.x;
-  const float* wr = W + (long long)r * n;
-  const int gpr = n / GROUP;
+  const float4* wr = reinterpret_cast<const float4*>(W + (long long)r * n);
+  const float4* h4 = reinterpret_cast<const float4*>(hdiag);
+  float4* o4 = reinterpret_cast<float4*>(wz + (long long)r * n);
+  const int nv = n / 4;  // n % 32 == 0: whole groups of eight float4s
   float xmin = INFINITY, xmax = 0.f;
   int cnt = 0;
-  for (int g = threadIdx.x; g < gpr; g += blockDim.x) {
-    const float4* p = reinterpret_cast<const float4*>(wr + g * GROUP);
-    float a = 0.f;
-#pragma unroll
-    for (int q = 0; q < GROUP / 4; ++q) {
-      float4 v = p[q];
-      a = fmaxf(a, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+  const int lane8 = threadIdx.x & 31;
+  const bool head = (threadIdx.x & 7) == 0;
+  // The trip count is the same for every lane of a warp (the shuffles below
+  // need the whole warp); lanes past the row's end load nothing.
+#pragma unroll 4
+  for (int v0 = threadIdx.x & ~31; v0 < nv; v0 += LADDER_THREADS) {
+    const int v = v0 + lane8;
+    const bool ok = v < nv;
+    float4 x = ok ? __ldcs(wr + v) : make_float4(0.f, 0.f, 0.f, 0.f);
+    if (DZ && ok) {
+      const float4 h = h4[v];
+      x.x = h.x > 0.f ? x.x : 0.f;
+      x.y = h.y > 0.f ? x.y : 0.f;
+      x.z = h.z > 0.f ? x.z : 0.f;
+      x.w = h.w > 0.f ? x.w : 0.f;
+      __stcs(o4 + v, x);
     }
-    if (a > 0.f) {
-      const float x = __fdiv_rn(a, 7.0f);
-      xmin = fminf(xmin, x);
-      xmax = fmaxf(xmax, x);
+    float a = fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w)));
+    // The group's eight float4s are lanes 8m .. 8m+7 of this warp (n is a
+    // multiple of 32, so a group is wholly inside or wholly past the row).
+    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
+    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
+    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 4));
+    if (ok && head && a > 0.f) {
+      const float xg = __fdiv_rn(a, 7.0f);
+      xmin = fminf(xmin, xg);
+      xmax = fmaxf(xmax, xg);
       ++cnt;
     }
   }
@@ -158,8 +186,8 @@ __global__ void __launch_bounds__(128) k_ladder(const float* __restrict__ W, int
     xmax = fmaxf(xmax, __shfl_xor_sync(0xffffffffu, xmax, o));
     cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
   }
-  __shared__ float smin[4], smax[4];
-  __shared__ int scnt[4];
+  __shared__ float smin[LADDER_THREADS / 32], smax[LADDER_THREADS / 32];
+  __shared__ int scnt[LADDER_THREADS / 32];
   __shared__ float slo, sst;
   const int wid = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (lane == 0) {
@@ -171,7 +199,7 @@ __global__ void __launch_bounds__(128) k_ladder(const float* __restrict__ W, int
   if (threadIdx.x == 0) {
     float mn = smin[0], mx = smax[0];
     int c = scnt[0];
-    for (int i = 1; i < 4; ++i) {
+    for (int i = 1; i < LADDER_THREADS / 32; ++i) {
       mn = fminf(mn, smin[i]);
       mx = fmaxf(mx, smax[i]);
       c += scnt[i];
@@ -236,6 +264,7 @@ constexpr int ESR = GROUP + 4;  // row stride of the group residuals in shared m
 constexpr int GMAX = 4, GMIN = 2;
 constexpr int SWEEP_SMEM = (SB * SB + SB + SWEEP_ROWS * LW + SWEEP_ROWS * ESR) * 4;
 
+
 // One lazy block [b0, b0+B) (B <= SB, a multiple of 32) for 40 rows per CTA.
 // The block's U (B x B), the rung weights and the rows' block of W sit in
 // shared memory.  Each row belongs to a quad of four lanes of one warp (8
@@ -284,6 +313,8 @@ __global__ void __launch_bounds__(SWEEP_THREADS) k_sweep_block(
   float* Es = Ws + SWEEP_ROWS * LW;  // [SWEEP_ROWS][ESR]
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   const int r0 = blockIdx.x * SWEEP_ROWS;
+  pdl_trigger();
+  pdl_wait();  // the previous update of W is visible
   {
     // The block's U and the rows' block of W by asynchronous 16-byte copies
     // (all in flight at once); rows past the end are filled with ones.
@@ -555,6 +586,8 @@ __global__ void k_prep_ut(const float* __restrict__ U, int n, int b0, int b1, in
                           float* __restrict__ Ut_hi, float* __restrict__ Ut_lo) {
   __shared__ float tile[32][33];
   const int c0 = blockIdx.x * 32, t0 = blockIdx.y * 32;
+  pdl_trigger();
+  pdl_wait();  // nothing of Ut is rewritten before the last update that read it is done
   const int ncol = n - b1;
   for (int i = threadIdx.y; i < 32; i += blockDim.y) {
     const int c = c0 + threadIdx.x;
@@ -607,7 +640,15 @@ static gptq_status sweep_attrs() {
 
 gptq_status ladder_run(const float* W, int rows, int n, float* tab, float* lost, cudaStream_t s) {
   GQ_PROF(K_LADDER, s);
-  k_ladder<<<rows, 128, 0, s>>>(W, n, tab, lost);
+  k_ladder<false><<<rows, LADDER_THREADS, 0, s>>>(W, n, tab, lost, nullptr, nullptr);
+  GQ_LAUNCHED();
+  return GPTQ_OK;
+}
+
+gptq_status copy_ladder_run(const float* W, int rows, int n, const float* hdiag, float* wz, float* tab,
+                            float* lost, cudaStream_t s) {
+  GQ_PROF(K_LADDER, s);
+  k_ladder<true><<<rows, LADDER_THREADS, 0, s>>>(W, n, tab, lost, hdiag, wz);
   GQ_LAUNCHED();
   return GPTQ_OK;
 }
@@ -682,25 +723,22 @@ static gptq_status sweep_core(int mode, float* W, int rows, int n, const float* 
   const int grid_rows = (rows + SWEEP_ROWS - 1) / SWEEP_ROWS;
   auto block = [&](int b0, int B, int ecol0) -> gptq_status {
     GQ_PROF(K_SWEEP_BLOCK, s);
+    const dim3 g(grid_rows), b(SWEEP_THREADS);
     if (mode == MODE_Q4_ACT)
-      k_sweep_block<MODE_Q4_ACT><<<grid_rows, SWEEP_THREADS, smem, s>>>(
-          W, rows, n, b0, B, U, hw, tab, lost, nib, rungs, scales, E_hi, E_lo, ecol0, ew, perm, codes);
+      GQ_CUDA(launch_pdl(k_sweep_block<MODE_Q4_ACT>, g, b, smem, s, W, rows, n, b0, B, U, hw, tab, lost, nib,
+                         rungs, scales, E_hi, E_lo, ecol0, ew, perm, codes));
     else if (mode == MODE_Q2)
-      k_sweep_block<MODE_Q2><<<grid_rows, SWEEP_THREADS, smem, s>>>(
-          W, rows, n, b0, B, U, hw, tab, lost, nib, rungs, scales, E_hi, E_lo, ecol0, ew, nullptr,
-          nullptr);
+      GQ_CUDA(launch_pdl(k_sweep_block<MODE_Q2>, g, b, smem, s, W, rows, n, b0, B, U, hw, tab, lost, nib, rungs,
+                         scales, E_hi, E_lo, ecol0, ew, (const int*)nullptr, (int8_t*)nullptr));
     else
-      k_sweep_block<MODE_Q4><<<grid_rows, SWEEP_THREADS, smem, s>>>(
-          W, rows, n, b0, B, U, hw, tab, lost, nib, rungs, scales, E_hi, E_lo, ecol0, ew, nullptr,
-          nullptr);
-    GQ_LAUNCHED();
+      GQ_CUDA(launch_pdl(k_sweep_block<MODE_Q4>, g, b, smem, s, W, rows, n, b0, B, U, hw, tab, lost, nib, rungs,
+                         scales, E_hi, E_lo, ecol0, ew, (const int*)nullptr, (int8_t*)nullptr));
     return GPTQ_OK;
   };
   auto prep = [&](int b0, int b1, int kt) -> gptq_status {
     GQ_PROF(K_PREP_UT, s);
     dim3 grid((n - b1 + 31) / 32, kt / 32);
-    k_prep_ut<<<grid, dim3(32, 8), 0, s>>>(U, n, b0, b1, ew, Ut_hi, Ut_lo);
-    GQ_LAUNCHED();
+    GQ_CUDA(launch_pdl(k_prep_ut, grid, dim3(32, 8), 0, s, U, n, b0, b1, ew, Ut_hi, Ut_lo));
     return GPTQ_OK;
   };
   // Groups of up to G blocks from b0: each block in turn, with the residuals
