@@ -90,6 +90,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   __shared__ int issued_sh, consumed_sh;
   __shared__ int skip_sh;
   // One read of the skip flag, shared by the whole CTA (uniform exit).
+  pdl_trigger();
+  pdl_wait();  // the previous kernel's writes (operands, C, the flag) are visible
   if (threadIdx.x == 0) skip_sh = (flag != nullptr && *(volatile const unsigned*)flag != 0u) ? 1 : 0;
   __syncthreads();
   if (skip_sh) return;
@@ -254,8 +256,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll 1
       for (int cc = 0; cc < BN; cc += 32) {
         uint32_t v[32];
-        tmem_ld16(tbase + (uint32_t)cc, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
-        tmem_ld16(tbase + (uint32_t)cc + 16u, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
+        tmem_ld32(tbase + (uint32_t)cc, v);
         tmem_ld_wait();
         uint8_t* buf = cstage + (chunk & 1) * CSLICE;
         if (leader) bulk_wait_read1();  // the reduce that last read `buf` is done
@@ -420,9 +421,8 @@ gptq_status gemm_tc_sub(const OperandMaps& maps, const TcJob& j0, const TcJob& j
   if (total <= 0) return GPTQ_OK;
   const int grid = total < num_sms() ? total : num_sms();
   GQ_PROF(kind, s);
-  k_gemm_tc<<<grid, THREADS, SMEM_BYTES, s>>>(maps.m[0], maps.m[1], maps.m[2], maps.m[3], maps.c, j0,
-                                              j1, K, kseg, flag, status, fp, wait_cfg());
-  GQ_LAUNCHED();
+  GQ_CUDA(launch_pdl(k_gemm_tc, dim3(grid), dim3(THREADS), SMEM_BYTES, s, maps.m[0], maps.m[1], maps.m[2],
+                     maps.m[3], maps.c, j0, j1, K, kseg, flag, status, fp, wait_cfg()));
   return GPTQ_OK;
 }
 
