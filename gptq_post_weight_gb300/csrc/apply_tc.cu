@@ -94,8 +94,6 @@ __global__ void __launch_bounds__(A_THREADS, 1)
   __shared__ __align__(8) uint64_t full[ANCH], conv[ANCH], tfull, ofree, drain;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh, skip_sh, issued_sh[ANCH];
-  pdl_trigger();
-  pdl_wait();  // the previous kernel's writes (A, Linv, the flag) are visible
   if (threadIdx.x == 0) skip_sh = (*(volatile const unsigned*)flag != 0u) ? 1 : 0;
   __syncthreads();
   if (skip_sh) return;
@@ -335,8 +333,9 @@ gptq_status apply_tc_run(const ApplyMaps& am, int k, int s0, int N, int col0, in
   const int ntiles = N / AM;
   const int grid = ntiles < num_sms() ? ntiles : num_sms();
   GQ_PROF(K_TRSM, s);
-  GQ_CUDA(launch_pdl(k_apply_tc, dim3(grid), dim3(A_THREADS), A_SMEM, s, am.a, am.lhi, am.llo, am.p.m[0],
-                     am.p.m[1], am.p.m[2], am.p.m[3], k, s0, N, col0, zero_end, flag, U, dsg, n, wait_cfg()));
+  k_apply_tc<<<grid, A_THREADS, A_SMEM, s>>>(am.a, am.lhi, am.llo, am.p.m[0], am.p.m[1], am.p.m[2], am.p.m[3],
+                                            k, s0, N, col0, zero_end, flag, U, dsg, n, wait_cfg());
+  GQ_LAUNCHED();
   return GPTQ_OK;
 }
 

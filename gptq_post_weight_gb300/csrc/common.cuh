@@ -64,33 +64,6 @@ struct ProfScope {
 
 inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Programmatic dependent launch.  The hot kernels of a group run back to
-// back on one stream, each a few to a few hundred microseconds long, so the
-// gap between two of them (launch, CTA dispatch, prologue) is a visible
-// share of a step.  A kernel launched by launch_pdl may be dispatched
-// while its predecessor is still finishing: it sets up (barriers, shared
-// memory) and then waits in pdl_wait() until the predecessor has completed
-// and its writes are visible, before it reads or writes global memory.
-// pdl_trigger() lets the successor be dispatched early.  Outside such a
-// launch both are no-ops.
-__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
-
-template <typename... KArgs, typename... Args>
-inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
-                              Args&&... args) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = block;
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
-}
 
 // Streaming multiprocessors of the current device (queried once).
 int num_sms();

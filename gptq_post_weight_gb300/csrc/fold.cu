@@ -150,8 +150,6 @@ __global__ void __launch_bounds__(256) k_build(const float* __restrict__ hp, int
 __global__ void __launch_bounds__(256) k_potrf(const float* __restrict__ A, long long lda, int k,
                                                float* __restrict__ Lhi, float* __restrict__ Llo,
                                                unsigned* flag) {
-  pdl_trigger();
-  pdl_wait();  // the previous kernel's writes (A, the flag) are visible
   if (flagged(flag)) return;
   extern __shared__ float S[];
   potrf_inverse_block(A + (long long)k * lda + k, lda, Lhi, Llo, flag, S);
@@ -317,7 +315,8 @@ static gptq_status fold_attempt(const float* hp, const FoldWs& w, const ApplyMap
         GQ_TRY(gemm_tc_sub(maps, syrk, inv, NB, w.flag, w.flag, K_FOLD_STRIP, s));
         {
           GQ_PROF(K_POTRF, s);
-          GQ_CUDA(launch_pdl(k_potrf, dim3(1), dim3(256), POTRF_SMEM, s, w.A, ld, k1, w.Lhi, w.Llo, w.flag));
+          k_potrf<<<1, 256, POTRF_SMEM, s>>>(w.A, ld, k1, w.Lhi, w.Llo, w.flag);
+          GQ_LAUNCHED();
         }
       }
       GQ_TRY(apply(k1, NB, 0));

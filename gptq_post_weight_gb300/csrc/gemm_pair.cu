@@ -78,8 +78,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
   __shared__ __align__(8) uint64_t full[PSTAGES], empty[PSTAGES], tfull[2], tempty[2], drain;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh, skip_sh;
-  pdl_trigger();
-  pdl_wait();  // the previous kernel's writes (operands, C, the flag) are visible
   if (threadIdx.x == 0) skip_sh = (flag != nullptr && *(volatile const unsigned*)flag != 0u) ? 1 : 0;
   __syncthreads();
   if (skip_sh) return;  // the same flag in both CTAs of a pair: both leave
@@ -333,8 +331,9 @@ gptq_status gemm_pair_sub(const OperandMaps& maps, const TcJob& j0, const TcJob&
   if (fp.on && total > 1 && pairs < 2) pairs = 2;  // pair 0 takes tile 0 only
   if (pairs < 1) pairs = 1;
   GQ_PROF(kind, s);
-  GQ_CUDA(launch_pdl(k_gemm_pair, dim3(2 * pairs), dim3(P_THREADS), P_SMEM, s, maps.m[0], maps.m[1], maps.m[2],
-                     maps.m[3], maps.c, p0, p1, K, kseg, flag, status, fp, wait_cfg()));
+  k_gemm_pair<<<2 * pairs, P_THREADS, P_SMEM, s>>>(maps.m[0], maps.m[1], maps.m[2], maps.m[3], maps.c, p0,
+                                                   p1, K, kseg, flag, status, fp, wait_cfg());
+  GQ_LAUNCHED();
   return GPTQ_OK;
 }
 

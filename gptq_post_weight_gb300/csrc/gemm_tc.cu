@@ -90,8 +90,6 @@ __global__ void __launch_bounds__(THREADS, 1)
   __shared__ int issued_sh, consumed_sh;
   __shared__ int skip_sh;
   // One read of the skip flag, shared by the whole CTA (uniform exit).
-  pdl_trigger();
-  pdl_wait();  // the previous kernel's writes (operands, C, the flag) are visible
   if (threadIdx.x == 0) skip_sh = (flag != nullptr && *(volatile const unsigned*)flag != 0u) ? 1 : 0;
   __syncthreads();
   if (skip_sh) return;
@@ -421,8 +419,9 @@ gptq_status gemm_tc_sub(const OperandMaps& maps, const TcJob& j0, const TcJob& j
   if (total <= 0) return GPTQ_OK;
   const int grid = total < num_sms() ? total : num_sms();
   GQ_PROF(kind, s);
-  GQ_CUDA(launch_pdl(k_gemm_tc, dim3(grid), dim3(THREADS), SMEM_BYTES, s, maps.m[0], maps.m[1], maps.m[2],
-                     maps.m[3], maps.c, j0, j1, K, kseg, flag, status, fp, wait_cfg()));
+  k_gemm_tc<<<grid, THREADS, SMEM_BYTES, s>>>(maps.m[0], maps.m[1], maps.m[2], maps.m[3], maps.c, j0,
+                                              j1, K, kseg, flag, status, fp, wait_cfg());
+  GQ_LAUNCHED();
   return GPTQ_OK;
 }
 

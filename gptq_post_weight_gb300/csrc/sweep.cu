@@ -313,8 +313,6 @@ __global__ void __launch_bounds__(SWEEP_THREADS) k_sweep_block(
   float* Es = Ws + SWEEP_ROWS * LW;  // [SWEEP_ROWS][ESR]
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   const int r0 = blockIdx.x * SWEEP_ROWS;
-  pdl_trigger();
-  pdl_wait();  // the previous update of W is visible
   {
     // The block's U and the rows' block of W by asynchronous 16-byte copies
     // (all in flight at once); rows past the end are filled with ones.
@@ -586,8 +584,7 @@ __global__ void k_prep_ut(const float* __restrict__ U, int n, int b0, int b1, in
                           float* __restrict__ Ut_hi, float* __restrict__ Ut_lo) {
   __shared__ float tile[32][33];
   const int c0 = blockIdx.x * 32, t0 = blockIdx.y * 32;
-  pdl_trigger();
-  pdl_wait();  // nothing of Ut is rewritten before the last update that read it is done
+
   const int ncol = n - b1;
   for (int i = threadIdx.y; i < 32; i += blockDim.y) {
     const int c = c0 + threadIdx.x;
@@ -723,22 +720,25 @@ static gptq_status sweep_core(int mode, float* W, int rows, int n, const float* 
   const int grid_rows = (rows + SWEEP_ROWS - 1) / SWEEP_ROWS;
   auto block = [&](int b0, int B, int ecol0) -> gptq_status {
     GQ_PROF(K_SWEEP_BLOCK, s);
-    const dim3 g(grid_rows), b(SWEEP_THREADS);
     if (mode == MODE_Q4_ACT)
-      GQ_CUDA(launch_pdl(k_sweep_block<MODE_Q4_ACT>, g, b, smem, s, W, rows, n, b0, B, U, hw, tab, lost, nib,
-                         rungs, scales, E_hi, E_lo, ecol0, ew, perm, codes));
+      k_sweep_block<MODE_Q4_ACT><<<grid_rows, SWEEP_THREADS, smem, s>>>(
+          W, rows, n, b0, B, U, hw, tab, lost, nib, rungs, scales, E_hi, E_lo, ecol0, ew, perm, codes);
     else if (mode == MODE_Q2)
-      GQ_CUDA(launch_pdl(k_sweep_block<MODE_Q2>, g, b, smem, s, W, rows, n, b0, B, U, hw, tab, lost, nib, rungs,
-                         scales, E_hi, E_lo, ecol0, ew, (const int*)nullptr, (int8_t*)nullptr));
+      k_sweep_block<MODE_Q2><<<grid_rows, SWEEP_THREADS, smem, s>>>(
+          W, rows, n, b0, B, U, hw, tab, lost, nib, rungs, scales, E_hi, E_lo, ecol0, ew, nullptr,
+          nullptr);
     else
-      GQ_CUDA(launch_pdl(k_sweep_block<MODE_Q4>, g, b, smem, s, W, rows, n, b0, B, U, hw, tab, lost, nib, rungs,
-                         scales, E_hi, E_lo, ecol0, ew, (const int*)nullptr, (int8_t*)nullptr));
+      k_sweep_block<MODE_Q4><<<grid_rows, SWEEP_THREADS, smem, s>>>(
+          W, rows, n, b0, B, U, hw, tab, lost, nib, rungs, scales, E_hi, E_lo, ecol0, ew, nullptr,
+          nullptr);
+    GQ_LAUNCHED();
     return GPTQ_OK;
   };
   auto prep = [&](int b0, int b1, int kt) -> gptq_status {
     GQ_PROF(K_PREP_UT, s);
     dim3 grid((n - b1 + 31) / 32, kt / 32);
-    GQ_CUDA(launch_pdl(k_prep_ut, grid, dim3(32, 8), 0, s, U, n, b0, b1, ew, Ut_hi, Ut_lo));
+    k_prep_ut<<<grid, dim3(32, 8), 0, s>>>(U, n, b0, b1, ew, Ut_hi, Ut_lo);
+    GQ_LAUNCHED();
     return GPTQ_OK;
   };
   // Groups of up to G blocks from b0: each block in turn, with the residuals
