@@ -257,12 +257,16 @@ static __device__ __noinline__ void potrf_inverse_block(const float* __restrict_
     }
     __syncthreads();
   }
-  for (int e = tid; e < NB * NB; e += NT) {
-    const int r = e / NB, c = e % NB;
-    float h = 0.f, l = 0.f;
-    if (c <= r) split_tf32(Li[r * LDS + c], h, l);
-    Lhi[e] = h;
-    Llo[e] = l;
+  // Four columns of a row per thread and pass, stored as float4s.
+  for (int e4 = tid; e4 < NB * NB / 4; e4 += NT) {
+    const int r = e4 / (NB / 4), c = 4 * (e4 % (NB / 4));
+    float4 h = make_float4(0.f, 0.f, 0.f, 0.f), l = h;
+    if (c <= r) split_tf32(Li[r * LDS + c], h.x, l.x);
+    if (c + 1 <= r) split_tf32(Li[r * LDS + c + 1], h.y, l.y);
+    if (c + 2 <= r) split_tf32(Li[r * LDS + c + 2], h.z, l.z);
+    if (c + 3 <= r) split_tf32(Li[r * LDS + c + 3], h.w, l.w);
+    reinterpret_cast<float4*>(Lhi)[e4] = h;
+    reinterpret_cast<float4*>(Llo)[e4] = l;
   }
 }
 

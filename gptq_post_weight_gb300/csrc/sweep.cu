@@ -580,25 +580,39 @@ __global__ void __launch_bounds__(SWEEP_THREADS) k_sweep_block(
 // for the GEMM, stored as their TF32 hi/lo split.  Rows b1 + c of U below
 // the diagonal are zero, so the same stripe serves the thin update of the
 // second block (c < SB, first SB of t) and the pair's trailing update.
-__global__ void k_prep_ut(const float* __restrict__ U, int n, int b0, int b1, int ew,
-                          float* __restrict__ Ut_hi, float* __restrict__ Ut_lo) {
-  __shared__ float tile[32][33];
-  const int c0 = blockIdx.x * 32, t0 = blockIdx.y * 32;
-
-  const int ncol = n - b1;
-  for (int i = threadIdx.y; i < 32; i += blockDim.y) {
-    const int c = c0 + threadIdx.x;
-    tile[i][threadIdx.x] = (c < ncol) ? U[(long long)(b0 + t0 + i) * n + b1 + c] : 0.f;
+// One CTA per 32 columns c x 128 rows t of the stripe: float4 loads of U's
+// rows into shared memory, float4 stores of Ut's rows (c fixed, 128
+// consecutive t) from it.
+constexpr int PREP_T = 128;
+__global__ void __launch_bounds__(256) k_prep_ut(const float* __restrict__ U, int n, int b0, int b1, int kt,
+                                                 int ew, float* __restrict__ Ut_hi, float* __restrict__ Ut_lo) {
+  __shared__ float tile[PREP_T][33];
+  const int c0 = blockIdx.x * 32, t0 = blockIdx.y * PREP_T;
+  const int ncol = n - b1, tid = threadIdx.x;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int tt = tid / 8 + 32 * i, c4 = tid % 8;
+    const int t = t0 + tt, c = c0 + 4 * c4;
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (t < kt && c < ncol) v = *reinterpret_cast<const float4*>(U + (long long)(b0 + t) * n + b1 + c);
+    tile[tt][4 * c4] = v.x;
+    tile[tt][4 * c4 + 1] = v.y;
+    tile[tt][4 * c4 + 2] = v.z;
+    tile[tt][4 * c4 + 3] = v.w;
   }
   __syncthreads();
-  for (int i = threadIdx.y; i < 32; i += blockDim.y) {
-    const int c = c0 + i;
-    if (c < ncol) {
-      float h, l;
-      split_tf32(tile[threadIdx.x][i], h, l);
-      Ut_hi[(long long)c * ew + t0 + threadIdx.x] = h;
-      Ut_lo[(long long)c * ew + t0 + threadIdx.x] = l;
-    }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int cc = tid / 32 + 8 * i, t4 = tid % 32;
+    const int c = c0 + cc, t = t0 + 4 * t4;
+    if (c >= ncol || t >= kt) continue;
+    float4 h, l;
+    split_tf32(tile[4 * t4][cc], h.x, l.x);
+    split_tf32(tile[4 * t4 + 1][cc], h.y, l.y);
+    split_tf32(tile[4 * t4 + 2][cc], h.z, l.z);
+    split_tf32(tile[4 * t4 + 3][cc], h.w, l.w);
+    *reinterpret_cast<float4*>(Ut_hi + (long long)c * ew + t) = h;
+    *reinterpret_cast<float4*>(Ut_lo + (long long)c * ew + t) = l;
   }
 }
 
@@ -736,8 +750,8 @@ static gptq_status sweep_core(int mode, float* W, int rows, int n, const float* 
   };
   auto prep = [&](int b0, int b1, int kt) -> gptq_status {
     GQ_PROF(K_PREP_UT, s);
-    dim3 grid((n - b1 + 31) / 32, kt / 32);
-    k_prep_ut<<<grid, dim3(32, 8), 0, s>>>(U, n, b0, b1, ew, Ut_hi, Ut_lo);
+    dim3 grid((n - b1 + 31) / 32, (kt + PREP_T - 1) / PREP_T);
+    k_prep_ut<<<grid, 256, 0, s>>>(U, n, b0, b1, kt, ew, Ut_hi, Ut_lo);
     GQ_LAUNCHED();
     return GPTQ_OK;
   };
