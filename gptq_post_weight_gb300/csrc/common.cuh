@@ -152,6 +152,8 @@ struct TcJob {
   // tile rows, down each band's columns (tiles running at the same time
   // then share operand panels in L2: for long K); 0 = row by row.
   int band;
+  // First column of the contraction in both operands (t = k0 .. k0 + K).
+  int k0;
 };
 
 struct OperandMaps {

@@ -121,6 +121,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
   if (warp == 0) {
     if (lane == 0) {
       const CUtensorMap* maps[4] = {&m0, &m1, &m2, &m3};
+      const uint64_t keep = l2_evict_last();  // operand panels: reread by many tiles
       int stage = 0;
       uint32_t phase = 0;
       // wc.no_loads (a test hook): issue nothing, so that the waits of the
@@ -141,10 +142,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
           const uint32_t sb = smem_u32(smem + stage * P_STAGE);
           const uint32_t fb = mapa_u32(smem_u32(&full[stage]), 0);
           if (rank == 0) mbar_expect_tx(&full[stage], 2 * P_STAGE);
-          tma_load_2d_pair(sb, ahi, c * PBK, ay, fb);
-          tma_load_2d_pair(sb + P_TILE_A, alo, c * PBK, ay, fb);
-          tma_load_2d_pair(sb + 2 * P_TILE_A, bhi, c * PBK, by, fb);
-          tma_load_2d_pair(sb + 2 * P_TILE_A + P_TILE_B, blo, c * PBK, by, fb);
+          const int kx = J.j.k0 + c * PBK;
+          tma_load_2d_pair_hint(sb, ahi, kx, ay, fb, keep);
+          tma_load_2d_pair_hint(sb + P_TILE_A, alo, kx, ay, fb, keep);
+          tma_load_2d_pair_hint(sb + 2 * P_TILE_A, bhi, kx, by, fb, keep);
+          tma_load_2d_pair_hint(sb + 2 * P_TILE_A + P_TILE_B, blo, kx, by, fb, keep);
           if (++stage == PSTAGES) {
             stage = 0;
             phase ^= 1u;
@@ -207,6 +209,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
   } else {
     const int q = warp & 3;  // TMEM lane quarter this warp may read
     const bool leader = threadIdx.x == 64;
+    const uint64_t stream_c = l2_evict_first();  // C passes through once per update
     uint8_t* cstage = smem + PSTAGES * P_STAGE;
     const uint32_t tempty_cl[2] = {mapa_u32(smem_u32(&tempty[0]), 0), mapa_u32(smem_u32(&tempty[1]), 0)};
     int acc = 0, chunk = 0;
@@ -259,7 +262,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
         fence_proxy_async_smem();
         epi_sync();
         if (leader) {
-          tma_reduce_add_2d(&cmap, smem_u32(buf), J.j.c_x0 + cb, J.j.c_y0 + ti * PM + (int)rank * HM);
+          tma_reduce_add_2d_hint(&cmap, smem_u32(buf), J.j.c_x0 + cb, J.j.c_y0 + ti * PM + (int)rank * HM,
+                                 stream_c);
           bulk_commit();
         }
         ++chunk;

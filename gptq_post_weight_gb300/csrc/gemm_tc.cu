@@ -160,10 +160,11 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort, wc.ns)) break;
           const uint32_t sb = smem_u32(smem + stage * STAGE_BYTES);
           mbar_expect_tx(&full[stage], STAGE_BYTES);
-          tma_load_2d(sb, ahi, c * BK, ay, &full[stage]);
-          tma_load_2d(sb + TILE_A, alo, c * BK, ay, &full[stage]);
-          tma_load_2d(sb + 2 * TILE_A, bhi, c * BK, by, &full[stage]);
-          tma_load_2d(sb + 2 * TILE_A + TILE_B, blo, c * BK, by, &full[stage]);
+          const int kx = J.k0 + c * BK;
+          tma_load_2d(sb, ahi, kx, ay, &full[stage]);
+          tma_load_2d(sb + TILE_A, alo, kx, ay, &full[stage]);
+          tma_load_2d(sb + 2 * TILE_A, bhi, kx, by, &full[stage]);
+          tma_load_2d(sb + 2 * TILE_A + TILE_B, blo, kx, by, &full[stage]);
           ++issued;
           if (++stage == STAGES) {
             stage = 0;

@@ -314,12 +314,11 @@ __global__ void __launch_bounds__(SWEEP_THREADS) k_sweep_block(
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   const int r0 = blockIdx.x * SWEEP_ROWS;
   {
-    // The block's U and the rows' block of W by asynchronous 16-byte copies
-    // (all in flight at once); rows past the end are filled with ones.
+    // The rows' block of W and the first group's rows of the block's U by
+    // asynchronous 16-byte copies (one commit group), then the rest of U
+    // (a second group, which lands while group 0 is worked); rows past the
+    // end are filled with ones.
     const int q4 = B / 4;
-#pragma unroll 4
-    for (int e = tid; e < B * q4; e += SWEEP_THREADS)
-      cp_async16(Us + (e / q4) * SB + 4 * (e % q4), U + (long long)(b0 + e / q4) * n + b0 + 4 * (e % q4));
 #pragma unroll 4
     for (int e = tid; e < SWEEP_ROWS * q4; e += SWEEP_THREADS) {
       const int rr = e / q4, c4 = e % q4;
@@ -329,7 +328,14 @@ __global__ void __launch_bounds__(SWEEP_THREADS) k_sweep_block(
       else  // rows past the end round ones (a zero dividend sends a division down its slow path)
         *reinterpret_cast<float4*>(dst) = make_float4(1.f, 1.f, 1.f, 1.f);
     }
-    cp_async_wait_all();
+#pragma unroll 4
+    for (int e = tid; e < GROUP * q4; e += SWEEP_THREADS)
+      cp_async16(Us + (e / q4) * SB + 4 * (e % q4), U + (long long)(b0 + e / q4) * n + b0 + 4 * (e % q4));
+    asm volatile("cp.async.commit_group;" ::: "memory");
+#pragma unroll 4
+    for (int e = GROUP * q4 + tid; e < B * q4; e += SWEEP_THREADS)
+      cp_async16(Us + (e / q4) * SB + 4 * (e % q4), U + (long long)(b0 + e / q4) * n + b0 + 4 * (e % q4));
+    asm volatile("cp.async.commit_group;\ncp.async.wait_group 1;" ::: "memory");
   }
   for (int e = tid; e < B; e += SWEEP_THREADS) {
     const float h = ACT ? 0.f : hw[b0 + e];
@@ -352,6 +358,11 @@ __global__ void __launch_bounds__(SWEEP_THREADS) k_sweep_block(
   }
   for (int g = 0; g < B / GROUP; ++g) {
     const int gc = g * GROUP;
+    if (g == 1) {
+      // The rest of the block's U (group 0 needed only its own rows).
+      asm volatile("cp.async.wait_group 0;" ::: "memory");
+      __syncthreads();
+    }
     float w[GROUP];
 #pragma unroll
     for (int q = 0; q < GROUP / 4; ++q) {
@@ -755,11 +766,13 @@ static gptq_status sweep_core(int mode, float* W, int rows, int n, const float* 
     GQ_LAUNCHED();
     return GPTQ_OK;
   };
-  // Groups of up to G blocks from b0: each block in turn, with the residuals
-  // of the group's earlier blocks brought into its columns first (a thin
-  // update, K = i * SB); then one update with K = (blocks) * SB for every
-  // column right of the group.  Ut[c][t] = U[b0 + t][b0 + SB + c] (TF32
-  // split), E[r][t] = the group's residuals, t < K.
+  // Groups of up to G blocks from b0: each block in turn; after block i a
+  // thin update (K = SB, block i's residuals, contraction columns
+  // i SB .. (i+1) SB) brings every later column of the group up to date, so
+  // the group's next block starts from current weights; then one update
+  // with K = (blocks) * SB for every column right of the group.
+  // Ut[c][t] = U[b0 + t][b0 + SB + c] (TF32 split), E[r][t] = the group's
+  // residuals, t < K.
   // maps: 0/1 = Ut hi/lo, 2/3 = E hi/lo.
   int b0 = 0;
   while (b0 < n) {
@@ -776,9 +789,9 @@ static gptq_status sweep_core(int mode, float* W, int rows, int n, const float* 
       if (i == 0 && b1 < n) GQ_TRY(prep(b0, b1, kt));
       if (i + 1 < nb) {
         const int bn = bi + SB;
-        const int Bn = (n - bn) < SB ? (n - bn) : SB;
-        GQ_TRY(gemm_tc_sub(maps, tc_rect(bn, 0, 2, 0, 0, bn - b1, rows, Bn), none, (i + 1) * SB,
-                           status, status, K_SWEEP_GEMM, s));
+        TcJob thin = tc_rect(bn, 0, 2, 0, 0, bn - b1, rows, b0 + kt - bn);
+        thin.k0 = i * SB;
+        GQ_TRY(gemm_tc_sub(maps, thin, none, SB, status, status, K_SWEEP_GEMM, s));
       }
     }
     if (bend < n)

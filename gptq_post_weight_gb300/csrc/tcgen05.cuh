@@ -218,6 +218,37 @@ static __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUte
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
       : "memory");
 }
+// L2 eviction policies for the updates: the operand panels are reread by
+// many tiles and should stay in L2 (evict_last); C streams through once per
+// update (evict_first).
+static __device__ __forceinline__ uint64_t l2_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+static __device__ __forceinline__ uint64_t l2_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+// tma_load_2d_pair with an L2 cache policy.
+static __device__ __forceinline__ void tma_load_2d_pair_hint(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                                             uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(policy)
+      : "memory");
+}
+// tma_reduce_add_2d with an L2 cache policy.
+static __device__ __forceinline__ void tma_reduce_add_2d_hint(const CUtensorMap* map, uint32_t src, int x, int y,
+                                                              uint64_t policy) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group.L2::cache_hint [%0, {%1, %2}], [%3], "
+      "%4;" ::"l"(reinterpret_cast<uint64_t>(map)),
+      "r"(x), "r"(y), "r"(src), "l"(policy)
+      : "memory");
+}
 // Arrive once on `bar` in both CTAs of the pair when the MMAs issued so far
 // have completed.
 static __device__ __forceinline__ void mma_commit_pair(uint64_t* bar) {
