@@ -46,9 +46,9 @@ FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1
 TF32_PER_BF16 = 1.1 / 2.25
 # DRAM bytes (read + write) per launch of the update kinds at the bench
 # workload, from a one-pass ncu launch list of the current kernels (the
-# fold's 67 K = 256 trailing updates: 53.87 GB); drop an entry whenever its
+# fold's 67 K = 256 trailing updates: 53.63 GB); drop an entry whenever its
 # kernels change.
-TRAFFIC = {"fold_gemm": 804.0e6}
+TRAFFIC = {"fold_gemm": 800.46e6}
 
 
 def peaks():
