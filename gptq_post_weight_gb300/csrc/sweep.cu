@@ -258,11 +258,10 @@ __global__ void __launch_bounds__(128) k_group(const float* __restrict__ tile, i
 constexpr int SWEEP_ROWS = 40;                 // 5 warps: 5120 rows fill 128 CTAs, one wave
 constexpr int SWEEP_THREADS = 4 * SWEEP_ROWS;  // a quad of lanes per row
 constexpr int LW = SB + 16;  // W block row stride: float4 rows, two rows per phase conflict-free
-constexpr int ESR = GROUP + 4;  // row stride of the group residuals in shared memory
 // Blocks whose residuals one trailing update applies (K = GMAX * SB); a
 // workspace too small for that runs groups of GMIN blocks.
 constexpr int GMAX = 4, GMIN = 2;
-constexpr int SWEEP_SMEM = (SB * SB + SB + SWEEP_ROWS * LW + SWEEP_ROWS * ESR) * 4;
+constexpr int SWEEP_SMEM = (SB * SB + SB + SWEEP_ROWS * LW) * 4;
 
 
 // One lazy block [b0, b0+B) (B <= SB, a multiple of 32) for 40 rows per CTA.
@@ -310,7 +309,6 @@ __global__ void __launch_bounds__(SWEEP_THREADS) k_sweep_block(
   float* Us = sm;             // [SB][SB]
   float* hws = Us + SB * SB;  // [SB]
   float* Ws = hws + SB;       // [SWEEP_ROWS][LW]
-  float* Es = Ws + SWEEP_ROWS * LW;  // [SWEEP_ROWS][ESR]
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   const int r0 = blockIdx.x * SWEEP_ROWS;
   {
@@ -350,7 +348,6 @@ __global__ void __launch_bounds__(SWEEP_THREADS) k_sweep_block(
   const int gpr = n / GROUP;
   const float* tabrow = tab + (long long)rs * 32;
   float* wrow = Ws + rl * LW;
-  float* es = Es + rl * ESR;
   float lo = 0.f, st = 0.f;
   if (MODE == MODE_Q4) {
     lo = lost[2 * rs];
@@ -476,6 +473,16 @@ __global__ void __launch_bounds__(SWEEP_THREADS) k_sweep_block(
     uint32_t words[NWORDS];
 #pragma unroll
     for (int i = 0; i < NWORDS; ++i) words[i] = 0u;
+    // The chain's own U entries (diagonal and first superdiagonal) in
+    // registers before it starts, and the residuals kept in registers (every
+    // lane of the quad computes every e_j): no shared-memory store inside the
+    // chain, so nothing orders its loads behind one.
+    float ud[GROUP], u1[GROUP], e[GROUP];
+#pragma unroll
+    for (int j = 0; j < GROUP; ++j) {
+      ud[j] = Ug[j * SB + j];
+      u1[j] = j + 1 < GROUP ? Ug[j * SB + j + 1] : 0.f;
+    }
     float eprev = 0.f;
 #pragma unroll
     for (int j = 0; j < GROUP; ++j) {
@@ -504,28 +511,18 @@ __global__ void __launch_bounds__(SWEEP_THREADS) k_sweep_block(
         q = sj > 0.f ? fminf(fmaxf(rintf(t1), -8.f), 7.f) : 0.f;
         lev = q;
       }
-      const float dj = Ug[j * SB + j];
+      const float dj = ud[j];
       float ej = 0.f;
       if (dj > 0.f) ej = __fdiv_rn(__fsub_rn(x, __fmul_rn(lev, sj)), dj);
-      es[j] = ej;  // the same value from the four lanes
+      e[j] = ej;
       if (ACT)
         words[j / 4] |= ((uint32_t)(int)q & 255u) << (8 * (j % 4));
       else if (Q2)
         words[j / 16] |= (uint32_t)q << (2 * (j % 16));
       else
         words[j / 8] |= ((uint32_t)((int)q + 8) & 15u) << (4 * (j % 8));
-      if (j + 1 < GROUP) w[j + 1] = __fsub_rn(w[j + 1], __fmul_rn(ej, Ug[j * SB + j + 1]));
+      if (j + 1 < GROUP) w[j + 1] = __fsub_rn(w[j + 1], __fmul_rn(ej, u1[j]));
       eprev = ej;
-    }
-    __syncwarp();
-    float e[GROUP];
-#pragma unroll
-    for (int q = 0; q < GROUP / 4; ++q) {
-      const float4 v = *reinterpret_cast<const float4*>(es + 4 * q);
-      e[4 * q] = v.x;
-      e[4 * q + 1] = v.y;
-      e[4 * q + 2] = v.z;
-      e[4 * q + 3] = v.w;
     }
     if (live) {
       if (ACT) {
