@@ -261,7 +261,7 @@ constexpr int LW = SB + 16;  // W block row stride: float4 rows, two rows per ph
 // Blocks whose residuals one trailing update applies (K = GMAX * SB); a
 // workspace too small for that runs groups of GMIN blocks.
 constexpr int GMAX = 4, GMIN = 2;
-constexpr int SWEEP_SMEM = (SB * SB + SB + SWEEP_ROWS * LW) * 4;
+constexpr int SWEEP_SMEM = (SB * SB + SB + SWEEP_ROWS * LW + SWEEP_ROWS * 32) * 4;
 
 
 // One lazy block [b0, b0+B) (B <= SB, a multiple of 32) for 40 rows per CTA.
@@ -309,6 +309,7 @@ __global__ void __launch_bounds__(SWEEP_THREADS) k_sweep_block(
   float* Us = sm;             // [SB][SB]
   float* hws = Us + SB * SB;  // [SB]
   float* Ws = hws + SB;       // [SWEEP_ROWS][LW]
+  float* Ts = Ws + SWEEP_ROWS * LW;  // [SWEEP_ROWS][32]: the rows' rung tables
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   const int r0 = blockIdx.x * SWEEP_ROWS;
   {
@@ -329,6 +330,11 @@ __global__ void __launch_bounds__(SWEEP_THREADS) k_sweep_block(
 #pragma unroll 4
     for (int e = tid; e < GROUP * q4; e += SWEEP_THREADS)
       cp_async16(Us + (e / q4) * SB + 4 * (e % q4), U + (long long)(b0 + e / q4) * n + b0 + 4 * (e % q4));
+    // The rows' rung tables (a row past the end takes the last row's).
+    for (int e = tid; e < SWEEP_ROWS * 8; e += SWEEP_THREADS) {
+      const int rr = e / 8, rsrc = r0 + rr < rows ? r0 + rr : rows - 1;
+      cp_async16(Ts + rr * 32 + 4 * (e % 8), tab + (long long)rsrc * 32 + 4 * (e % 8));
+    }
     asm volatile("cp.async.commit_group;" ::: "memory");
 #pragma unroll 4
     for (int e = GROUP * q4 + tid; e < B * q4; e += SWEEP_THREADS)
@@ -346,7 +352,7 @@ __global__ void __launch_bounds__(SWEEP_THREADS) k_sweep_block(
   const bool live = r < rows;
   const int rs = live ? r : rows - 1;  // rows past the end compute on a real row, store nothing
   const int gpr = n / GROUP;
-  const float* tabrow = tab + (long long)rs * 32;
+  const float* tabrow = Ts + rl * 32;
   float* wrow = Ws + rl * LW;
   float lo = 0.f, st = 0.f;
   if (MODE == MODE_Q4) {
@@ -560,7 +566,7 @@ __global__ void __launch_bounds__(SWEEP_THREADS) k_sweep_block(
     }
     // The group's residuals into the rest of the block.
     const int rest = B - gc - GROUP;
-#pragma unroll 1
+#pragma unroll 2
     for (int m = 0; m < rest / 16; ++m) {
       const int c = gc + GROUP + 16 * m + 4 * sub;
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
