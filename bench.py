@@ -117,8 +117,9 @@ def hbm_report(per_kind, n, rows, codec="q4tp", peak_gbs=None, NB=128, SB=128):
     parts = {
         "build": ("a2 builder: read the packed H, write the N x N working matrix", n * (n + 1) // 2 * 4 + N * N * 4),
         "trsm": ("a6 U = P X P D^-1 fused into the panel products' store: U's upper triangle written "
-                 "(the kernel itself is bound by its FP32 triangular products)", n * (n + 1) // 2 * 4),
-        "ladder": ("a7 ladder: read W, write tab and lost", rows * n * 4 + tabs),
+                 "(the tensor-core panel product itself is bound by launch and load latency)", n * (n + 1) // 2 * 4),
+        "ladder": ("a7 dead-column zeroing fused with the ladder: read W and diag H, write the zeroed W, "
+                   "tab and lost", 2 * rows * n * 4 + n * 4 + tabs),
         "place": ("q2tp placement: read W, write tab and lost", rows * n * 4 + tabs),
         "copy": ("dead-column zeroing: read and write W", 2 * rows * n * 4),
         "sweep_block": ("a8, a9, a11: read W and U's diagonal blocks, write codes, rungs and scales "
