@@ -46,9 +46,9 @@ FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1
 TF32_PER_BF16 = 1.1 / 2.25
 # DRAM bytes (read + write) per launch of the update kinds at the bench
 # workload, from a one-pass ncu launch list of the current kernels (the
-# fold's 67 K = 256 trailing updates: 53.63 GB); drop an entry whenever its
+# fold's 33 K = 512 trailing updates: 30.51 GB); drop an entry whenever its
 # kernels change.
-TRAFFIC = {"fold_gemm": 800.46e6}
+TRAFFIC = {"fold_gemm": 924.42e6}
 
 
 def peaks():
@@ -67,33 +67,36 @@ def workload_desc(cfg, codec="q4tp"):
             f"lambda={cfg.lam}, group 32, " + ("q4tp" if codec == "q4tp" else "q2tp placed rule"))
 
 
-def fold_gemm_flops(n, NB=128, part="all"):
+def fold_gemm_flops(n, NB=128, part="all", G=4):
     """Algorithmic flops of the fold's update GEMM launches over one fold, on
-    the padded size, following the library's schedule: steps in pairs (a thin
-    K = NB strip update of the next block column between them, then one
-    K = 2 NB trailing update), a last unpaired step with K = NB.
-    part: "trailing" (the K = 2 NB and unpaired updates, kind fold_gemm),
-    "strip" (the thin K = NB strips, kind fold_strip) or "all"."""
+    the padded size, following the library's schedule: steps in groups of G
+    blocks (fewer at the end).  After step i of a group, a K = NB strip
+    update of the group's remaining block columns; after the group, one
+    K = G NB trailing update.
+    part: "trailing" (the group updates, kind fold_gemm), "strip" (the K = NB
+    strips, kind fold_strip) or "all"."""
     N = (n + NB - 1) // NB * NB
     strip = trail = 0
     k = 0
     while k < N:
-        if k + 2 * NB <= N:
-            k1, s1 = k + NB, k + 2 * NB
-            strip += 2 * NB * ((N - k1 - NB) * NB + NB * (NB + 1) // 2)  # SYRK strip
-            strip += 2 * NB * k1 * NB  # inverse strip
-            m = N - s1
-            # SYRK of the pair, then the inverse rectangle: step k's panel meets
-            # the rows c < k1 only (its rows of block k1 are zero: X is lower
-            # triangular, so the launch multiplies them but they are no work of
-            # the method), step k1's the rows c < s1.
-            trail += 2 * (2 * NB) * (m * (m + 1) // 2) + 2 * NB * (k1 + s1) * m
-            k = s1
-        else:
-            s0 = k + NB
-            m = N - s0
-            trail += 2 * NB * (m * (m + 1) // 2) + 2 * NB * s0 * m
-            k = s0
+        g = min(G, (N - k) // NB)
+        sg = k + g * NB
+        for i in range(g - 1):
+            kn = k + (i + 1) * NB
+            w = sg - kn
+            # SYRK strip: the rows below the group, and the lower triangle of
+            # the group's remaining square; the inverse's rows above kn.
+            strip += 2 * NB * ((N - sg) * w + w * (w + 1) // 2)
+            strip += 2 * NB * kn * w
+        m = N - sg
+        if m > 0:
+            # SYRK of the group, then the inverse rectangle: step i's panel
+            # meets the rows c < k_i + NB only (its rows of later blocks of the
+            # group are zero: X is lower triangular, so the launch multiplies
+            # them but they are no work of the method).
+            trail += 2 * (g * NB) * (m * (m + 1) // 2)
+            trail += sum(2 * NB * (k + (i + 1) * NB) * m for i in range(g))
+        k = sg
     return {"trailing": trail, "strip": strip, "all": trail + strip}[part]
 
 

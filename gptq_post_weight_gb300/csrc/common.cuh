@@ -171,10 +171,15 @@ inline TcJob tc_rect(int c_x0, int c_y0, int a_map, int a_row0, int b_map, int b
   return j;
 }
 
+// A strip below a diagonal: rows [0, M) by columns [0, N) of C with M >= N,
+// whose top N x N square is kept to its lower triangle (tiles above the
+// diagonal are not visited, the diagonal tiles are masked).  Single-SM
+// kernel only.
 inline TcJob tc_strip(int c_x0, int c_y0, int a_map, int a_row0, int b_map, int b_row0, int M,
                       int N) {
   TcJob j = tc_rect(c_x0, c_y0, a_map, a_row0, b_map, b_row0, M, N);
   j.mode = 2;
+  if (j.ntiles > 0) j.ntiles = j.mt * j.nt - j.nt * (j.nt - 1) / 2;
   return j;
 }
 

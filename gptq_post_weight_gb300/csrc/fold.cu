@@ -155,10 +155,12 @@ __global__ void __launch_bounds__(256) k_potrf(const float* __restrict__ A, long
   potrf_inverse_block(A + (long long)k * lda + k, lda, Lhi, Llo, flag, S);
 }
 
-// Panel buffers hold two steps side by side (columns [0, NB) and [NB, 2NB)),
-// so that a pair of steps updates the trailing matrix once with K = 2 NB.
-// The panel product that fills them is apply_tc.cu.
-constexpr int PW = 2 * NB;
+// Steps go in groups of up to FG blocks: the panel buffers hold a group's
+// panels side by side (step i of the group in columns [i NB, (i+1) NB)), so
+// that the trailing matrix is updated once per group with K = FG NB.  The
+// panel product that fills them is apply_tc.cu.
+constexpr int FG = 4;
+constexpr int PW = FG * NB;
 
 // Act-order channel order ([host page] act_order_perm): descending H_ii in
 // Rust's total order on f32 (NaN and -0.0 ordered), ties by ascending index.
@@ -216,9 +218,9 @@ gptq_status perm_run(const float* hdiag, int n, int* perm, cudaStream_t s) {
 struct FoldWs {
   int n, N;
   float* A;       // N x N
-  float* P_hi;    // N x PW   (L panels of the current pair of steps, TF32 hi/lo)
+  float* P_hi;    // N x PW   (L panels of the current group of steps, TF32 hi/lo)
   float* P_lo;
-  float* Yp_hi;   // N x PW   (Y panels of the current pair of steps, TF32 hi/lo)
+  float* Yp_hi;   // N x PW   (Y panels of the current group of steps, TF32 hi/lo)
   float* Yp_lo;
   float* Lhi;     // NB x NB: inverse of the current diagonal block of L, TF32 hi
   float* Llo;     //          and lo parts, row-major
@@ -278,64 +280,64 @@ static gptq_status fold_attempt(const float* hp, const FoldWs& w, const ApplyMap
     k_build<<<N, 256, 0, s>>>(hp, n, N, perm, w.base, lam, w.dsg, w.A, ld, 1);
     GQ_LAUNCHED();
   }
-  // Steps go in pairs (k, k + NB) while two blocks remain:
-  //   potrf(k); apply(k) -> panel columns [0, NB);
-  //   thin update of block column k + NB only (K = NB): SYRK strip and the
-  //   inverse's strip, so that block k + NB is current;
-  //   potrf(k + NB); apply(k + NB) -> panel columns [NB, 2 NB);
-  //   one trailing update with K = 2 NB (both panels) for everything right
-  //   of / below block k + NB.
-  // A last unpaired block runs as a single step (K = NB).
-  // The diagonal-block step (Cholesky + inverse of block k) of the first
-  // block of a pair rides in the update GEMM that finishes it (tile 0 of
-  // that GEMM is exactly that block); the second block's step runs alone
-  // right after the thin strip (the strip's own tiles are done within
-  // microseconds, so nothing would hide it there), as does the very first.
+  // Steps go in groups of FG blocks k_0 .. k_{G-1} (k_i = k + i NB; fewer
+  // at the end), s = k + G NB:
+  //   apply(k_i) -> panel columns [i NB, (i+1) NB), and zeros into the Yp
+  //   entries of the group's later rows (X is lower triangular);
+  //   then, if a block of the group remains, the strip update of the
+  //   group's remaining block columns [k_{i+1}, s) by panel i alone (K = NB):
+  //   the SYRK rows from k_{i+1} down (top square kept to its lower
+  //   triangle) and the inverse's rows above k_{i+1}; then the diagonal-block
+  //   step of block k_{i+1};
+  //   one trailing update with K = G NB (every panel of the group) for
+  //   everything right of / below the group.
+  // The diagonal-block step of a group's first block rides in the update
+  // GEMM that finishes it (tile 0 of that GEMM is exactly that block); a
+  // later block's step rides in the strip that finishes it when that strip
+  // is wider than one block (its other tiles then hide part of the step),
+  // else it runs alone right after the strip; the very first runs alone.
   auto apply = [&](int k, int col0, int zero_end) -> gptq_status {
     return apply_tc_run(am, k, k + NB, N, col0, zero_end, w.flag, U, w.dsg, n, s);
   };
   auto fused = [&](int k) { return FusedPotrf{w.A, ld, k, w.Lhi, w.Llo, 1}; };
-  {
+  auto potrf_alone = [&](int k) -> gptq_status {
     GQ_PROF(K_POTRF, s);
-    k_potrf<<<1, 256, POTRF_SMEM, s>>>(w.A, ld, 0, w.Lhi, w.Llo, w.flag);
+    k_potrf<<<1, 256, POTRF_SMEM, s>>>(w.A, ld, k, w.Lhi, w.Llo, w.flag);
     GQ_LAUNCHED();
-  }
-  // maps: 0/1 = P hi/lo, 2/3 = Yp hi/lo (K = 2 NB wide).
+    return GPTQ_OK;
+  };
+  GQ_TRY(potrf_alone(0));
+  // maps: 0/1 = P hi/lo, 2/3 = Yp hi/lo (K = PW wide).
   int k = 0;
   while (k < N) {
-    if (k + 2 * NB <= N) {
-      const int k1 = k + NB, s1 = k + 2 * NB;
-      GQ_TRY(apply(k, 0, s1));
-      {
-        const TcJob syrk = tc_strip(k1, k1, 0, k1, 0, k1, N - k1, NB);
-        const TcJob inv = tc_rect(k1, 0, 2, 0, 0, k1, k1, NB);
-        // The 128-wide strip update, then the diagonal-block step of block k1
-        // as its own one-CTA launch (faster here than fused into the strip:
-        // the strip's other tiles are done within microseconds).
-        GQ_TRY(gemm_tc_sub(maps, syrk, inv, NB, w.flag, w.flag, K_FOLD_STRIP, s));
-        {
-          GQ_PROF(K_POTRF, s);
-          k_potrf<<<1, 256, POTRF_SMEM, s>>>(w.A, ld, k1, w.Lhi, w.Llo, w.flag);
-          GQ_LAUNCHED();
+    const int G = (N - k) / NB < FG ? (N - k) / NB : FG;
+    const int sg = k + G * NB;
+    for (int i = 0; i < G; ++i) {
+      const int ki = k + i * NB, kn = ki + NB;
+      GQ_TRY(apply(ki, i * NB, sg));
+      if (kn < sg) {
+        const int wdt = sg - kn;
+        TcJob syrk = tc_strip(kn, kn, 0, kn, 0, kn, N - kn, wdt);
+        TcJob inv = tc_rect(kn, 0, 2, 0, 0, kn, kn, wdt);
+        syrk.k0 = inv.k0 = i * NB;
+        if (wdt > NB) {
+          GQ_TRY(gemm_tc_sub(maps, syrk, inv, NB, w.flag, w.flag, K_FOLD_STRIP, s, fused(kn)));
+        } else {
+          GQ_TRY(gemm_tc_sub(maps, syrk, inv, NB, w.flag, w.flag, K_FOLD_STRIP, s));
+          GQ_TRY(potrf_alone(kn));
         }
       }
-      GQ_TRY(apply(k1, NB, 0));
-      if (s1 < N) {
-        const TcJob syrk = tc_lower(s1, s1, 0, s1, N - s1);
-        const TcJob inv = tc_rect(s1, 0, 2, 0, 0, s1, s1, N - s1);
-        GQ_TRY(gemm_pair_sub(maps, syrk, inv, 2 * NB, w.flag, w.flag, K_FOLD_GEMM, s, fused(s1)));
-      }
-      k = s1;
-    } else {
-      const int s0 = k + NB;
-      GQ_TRY(apply(k, 0, 0));
-      if (s0 < N) {
-        const TcJob syrk = tc_lower(s0, s0, 0, s0, N - s0);
-        const TcJob inv = tc_rect(s0, 0, 2, 0, 0, s0, s0, N - s0);
-        GQ_TRY(gemm_tc_sub(maps, syrk, inv, NB, w.flag, w.flag, K_FOLD_GEMM, s, fused(s0)));
-      }
-      k = s0;
     }
+    if (sg < N) {
+      const TcJob syrk = tc_lower(sg, sg, 0, sg, N - sg);
+      const TcJob inv = tc_rect(sg, 0, 2, 0, 0, sg, sg, N - sg);
+      if (G > 1) {
+        GQ_TRY(gemm_pair_sub(maps, syrk, inv, G * NB, w.flag, w.flag, K_FOLD_GEMM, s, fused(sg)));
+      } else {
+        GQ_TRY(gemm_tc_sub(maps, syrk, inv, NB, w.flag, w.flag, K_FOLD_GEMM, s, fused(sg)));
+      }
+    }
+    k = sg;
   }
   return GPTQ_OK;
 }

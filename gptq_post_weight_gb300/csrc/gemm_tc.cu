@@ -61,16 +61,21 @@ __device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a, uint64_t b
       : "memory");
 }
 
+// Tile t of a job: mode 1 walks a lower triangle by rows; mode 2 (a strip
+// whose top nt x nt tiles straddle the diagonal) walks that top triangle by
+// rows, then the full rows below it; mode 0 walks a rectangle by rows.
 __device__ __forceinline__ void tile_of(const TcJob& J, int t, int& ti, int& tj) {
-  if (J.mode == 1) {
+  const int tri = J.mode == 1 ? J.ntiles : J.mode == 2 ? J.nt * (J.nt + 1) / 2 : 0;
+  if (t < tri) {
     int i = (int)((sqrtf(8.0f * (float)t + 1.0f) - 1.0f) * 0.5f);
     while ((i + 1) * (i + 2) / 2 <= t) ++i;
     while (i * (i + 1) / 2 > t) --i;
     ti = i;
     tj = t - i * (i + 1) / 2;
   } else {
-    ti = t / J.nt;
-    tj = t % J.nt;
+    const int u = t - tri, r0 = J.mode == 2 ? J.nt : 0;
+    ti = r0 + u / J.nt;
+    tj = u % J.nt;
   }
 }
 

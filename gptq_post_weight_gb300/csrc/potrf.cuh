@@ -23,9 +23,10 @@ constexpr int POTRF_SMEM_BYTES = 3 * NB * LDS * 4;
 // sum_{j <= m < i} L_im X_mj, as register-tiled block products.  Loops stay
 // rolled where unrolling buys little: the step runs once per block column on
 // whichever SM its CTA lands on, mostly from a cold instruction cache.
-// Output: Linv itself as its TF32 hi/lo split (NB x NB row-major each,
-// zeros above the diagonal): the K-major operand of the panel product on
-// the tensor cores.
+// Output: Linv itself as its TF32 hi/lo split (NB x NB row-major each):
+// the K-major operand of the panel product on the tensor cores.  Only the
+// 32 x 32 blocks on and below the block diagonal are written (zeros above
+// the diagonal inside the diagonal blocks); the rest is never read.
 // Runs on the whole CTA (any multiple of 32 threads >= 128); S is at least
 // POTRF_SMEM_BYTES of shared memory.  The block starts at Ablk (leading
 // dimension lda); it is read with L1-bypassing loads.
@@ -257,16 +258,24 @@ static __device__ __noinline__ void potrf_inverse_block(const float* __restrict_
     }
     __syncthreads();
   }
-  // Four columns of a row per thread and pass, stored as float4s.
-  for (int e4 = tid; e4 < NB * NB / 4; e4 += NT) {
-    const int r = e4 / (NB / 4), c = 4 * (e4 % (NB / 4));
-    float4 h = make_float4(0.f, 0.f, 0.f, 0.f), l = h;
-    if (c <= r) split_tf32(Li[r * LDS + c], h.x, l.x);
-    if (c + 1 <= r) split_tf32(Li[r * LDS + c + 1], h.y, l.y);
-    if (c + 2 <= r) split_tf32(Li[r * LDS + c + 2], h.z, l.z);
-    if (c + 3 <= r) split_tf32(Li[r * LDS + c + 3], h.w, l.w);
-    reinterpret_cast<float4*>(Lhi)[e4] = h;
-    reinterpret_cast<float4*>(Llo)[e4] = l;
+  // The ten 32 x 32 blocks on and below the block diagonal, four columns of
+  // a row per item; the diagonal blocks hold exact zeros above the diagonal
+  // (their identity rows' substitution starts with zeros).  The six blocks
+  // above are never read: the panel product loads, for each 32-wide slice
+  // of u, only the rows of Linv at or below that slice's diagonal block.
+  for (int e = tid; e < 10 * 32 * 8; e += NT) {
+    const int b = e >> 8, w = e & 255;
+    const int bi = b >= 6 ? 3 : b >= 3 ? 2 : b >= 1 ? 1 : 0;
+    const int bj = b - bi * (bi + 1) / 2;
+    const int r = 32 * bi + (w >> 3), c = 32 * bj + 4 * (w & 7);
+    const float* src = Li + r * LDS + c;
+    float4 h, l;
+    split_tf32(src[0], h.x, l.x);
+    split_tf32(src[1], h.y, l.y);
+    split_tf32(src[2], h.z, l.z);
+    split_tf32(src[3], h.w, l.w);
+    *reinterpret_cast<float4*>(Lhi + r * NB + c) = h;
+    *reinterpret_cast<float4*>(Llo + r * NB + c) = l;
   }
 }
 

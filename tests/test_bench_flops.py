@@ -6,7 +6,7 @@ through update GEMMs, one multiply-add per column of every block before j's
 own block (its own block's columns are the diagonal and panel kernels' work).
 Inverse accumulated alongside: entry (c, i), c < i, receives NB multiply-adds
 from every step k with c < k + NB <= i.  However the schedule groups the steps
-(pairs with a thin strip update between them), the sums must agree exactly.
+(groups of four, with strip updates between them), the sums must agree exactly.
 The sweep: column t of W receives one multiply-add per row for every column of
 the blocks before t's block.
 """
@@ -26,10 +26,12 @@ def per_entry_fold(n, NB=128):
     return 2 * (chol + inv)
 
 
-@pytest.mark.parametrize("n", [128, 256, 384, 640, 1000, 4096, 17408])
-def test_fold_update_flops_per_entry(n):
-    assert bench.fold_gemm_flops(n, part="all") == per_entry_fold(n)
-    assert bench.fold_gemm_flops(n, part="trailing") + bench.fold_gemm_flops(n, part="strip") == per_entry_fold(n)
+@pytest.mark.parametrize("n", [128, 256, 384, 512, 640, 896, 1000, 4096, 17408])
+@pytest.mark.parametrize("G", [1, 2, 4])
+def test_fold_update_flops_per_entry(n, G):
+    assert bench.fold_gemm_flops(n, part="all", G=G) == per_entry_fold(n)
+    assert (bench.fold_gemm_flops(n, part="trailing", G=G) + bench.fold_gemm_flops(n, part="strip", G=G)
+            == per_entry_fold(n))
 
 
 def test_fold_update_flops_near_textbook():
