@@ -174,13 +174,24 @@ gptq_status gptq_quantize_group(const float* H_packed, int n, double lambda, con
   float* wz = c.take<float>((size_t)rows * n);
   float* tb = tab ? tab : c.take<float>((size_t)rows * 32);
   float* ls = lost ? lost : c.take<float>((size_t)rows * 2);
-  c.take<float>((size_t)n);  // keeps the layout independent of which outputs are given
+  float* hd2 = c.take<float>((size_t)n);  // the ladder's own copy of diag(H)
   if (!c.ok) return GPTQ_ERR_NOMEM;
   const size_t off = round_up(c.off, 256);
   void* rest = static_cast<char*>(ws) + off;
   const size_t rest_bytes = ws_bytes - off;
-  GQ_TRY(fold_run(H_packed, n, lambda, u, d, hd, lambda_used, rest, rest_bytes, s));
-  GQ_TRY(copy_ladder_run(W, rows, n, hd, wz, tb, ls, s));
+  // The dead-zeroed copy of W and its ladder depend on W and diag(H) alone:
+  // they run on a side stream beside the fold (whose one-CTA steps leave
+  // the GPU mostly idle), joined before the sweep.
+  SideStream side;
+  GQ_TRY(side.init());
+  GQ_CUDA(cudaEventRecord(side.fork, s));
+  GQ_CUDA(cudaStreamWaitEvent(side.s, side.fork, 0));
+  GQ_TRY(diag_run(H_packed, n, hd2, side.s));
+  GQ_TRY(copy_ladder_run(W, rows, n, hd2, wz, tb, ls, side.s));
+  GQ_CUDA(cudaEventRecord(side.join, side.s));
+  const gptq_status fs = fold_run(H_packed, n, lambda, u, d, hd, lambda_used, rest, rest_bytes, s);
+  GQ_CUDA(cudaStreamWaitEvent(s, side.join, 0));
+  GQ_TRY(fs);
   return sweep_run(wz, rows, n, u, hd, tb, ls, nibbles, rungs, scales, rest, rest_bytes, s);
 }
 

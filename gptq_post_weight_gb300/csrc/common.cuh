@@ -241,6 +241,25 @@ gptq_status gemm_tc_sub(const OperandMaps& maps, const TcJob& j0, const TcJob& j
                         const unsigned* flag, unsigned* status, int kind, cudaStream_t s,
                         const FusedPotrf& fp = FusedPotrf{}, int kseg = 0);
 
+// A non-blocking side stream and two events for one call (fork: main ->
+// side, join: side -> main), released when the call returns; the side
+// stream's work is always joined back into the main stream before that.
+struct SideStream {
+  cudaStream_t s = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+  gptq_status init() {
+    GQ_CUDA(cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking));
+    GQ_CUDA(cudaEventCreateWithFlags(&fork, cudaEventDisableTiming));
+    GQ_CUDA(cudaEventCreateWithFlags(&join, cudaEventDisableTiming));
+    return GPTQ_OK;
+  }
+  ~SideStream() {
+    if (join) cudaEventDestroy(join);
+    if (fork) cudaEventDestroy(fork);
+    if (s) cudaStreamDestroy(s);
+  }
+};
+
 // TF32 split: hi = x rounded to TF32 (10-bit mantissa, nearest, ties away),
 // lo = (x - hi) rounded to TF32; x - hi is exact in f32.
 __device__ __forceinline__ float tf32_rna(float x) {

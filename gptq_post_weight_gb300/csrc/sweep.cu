@@ -762,11 +762,22 @@ static gptq_status sweep_core(int mode, float* W, int rows, int n, const float* 
     GQ_LAUNCHED();
     return GPTQ_OK;
   };
+  // A group's Ut stripe depends on U alone, so it is built on a side stream
+  // beside the group's first block (which leaves SMs and issue slots free):
+  // it waits for the previous group's update (the last reader of Ut) and the
+  // group's first thin update waits for it.
+  SideStream side;
+  GQ_TRY(side.init());
   auto prep = [&](int b0, int b1, int kt) -> gptq_status {
-    GQ_PROF(K_PREP_UT, s);
-    dim3 grid((n - b1 + 31) / 32, (kt + PREP_T - 1) / PREP_T);
-    k_prep_ut<<<grid, 256, 0, s>>>(U, n, b0, b1, kt, ew, Ut_hi, Ut_lo);
-    GQ_LAUNCHED();
+    GQ_CUDA(cudaEventRecord(side.fork, s));
+    GQ_CUDA(cudaStreamWaitEvent(side.s, side.fork, 0));
+    {
+      GQ_PROF(K_PREP_UT, side.s);
+      dim3 grid((n - b1 + 31) / 32, (kt + PREP_T - 1) / PREP_T);
+      k_prep_ut<<<grid, 256, 0, side.s>>>(U, n, b0, b1, kt, ew, Ut_hi, Ut_lo);
+      GQ_LAUNCHED();
+    }
+    GQ_CUDA(cudaEventRecord(side.join, side.s));
     return GPTQ_OK;
   };
   // Groups of up to G blocks from b0: each block in turn; after block i a
@@ -784,12 +795,13 @@ static gptq_status sweep_core(int mode, float* W, int rows, int n, const float* 
     const int b1 = b0 + SB;
     const int kt = (nb * SB < n - b0) ? nb * SB : n - b0;  // rows of U the group reads
     int bend = b0;
+    if (b1 < n) GQ_TRY(prep(b0, b1, kt));
     for (int i = 0; i < nb; ++i) {
       const int bi = b0 + i * SB;
       const int Bi = (n - bi) < SB ? (n - bi) : SB;
       GQ_TRY(block(bi, Bi, i * SB));
       bend = bi + Bi;
-      if (i == 0 && b1 < n) GQ_TRY(prep(b0, b1, kt));
+      if (i == 0 && b1 < n) GQ_CUDA(cudaStreamWaitEvent(s, side.join, 0));
       if (i + 1 < nb) {
         const int bn = bi + SB;
         TcJob thin = tc_rect(bn, 0, 2, 0, 0, bn - b1, rows, b0 + kt - bn);
