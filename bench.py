@@ -616,7 +616,7 @@ def main():
         # group's upload and the last group's readback have nothing to hide
         # under, and a run of 11 spreads them as a run of that length does.
         e2e_steps = max(args.steps, 11)
-        e2e_run(2)
+        e2e_run(max(args.warmup, 3))
         barrier()
         t0 = time.perf_counter()
         e2e_run(e2e_steps)
