@@ -288,9 +288,11 @@ def q4tp_group(tile, ublk, hw, tab, lost):
     return nib, rungs, scales, e
 
 
-def quantize_group(h_packed, n, w, lam=0.01, ws=None, want_u=True, stream=None, out=None):
+def quantize_group(h_packed, n, w, lam=0.01, ws=None, want_u=True, stream=None, out=None, want_aux=True):
     """Fold + ladder + sweep.  Returns dict(nibbles, rungs, scales, tab, lost,
-    u, d, hdiag, lam)."""
+    u, d, hdiag, lam); with want_aux=False, tab, lost, d and hdiag stay in the
+    workspace (None here), so that repeated calls on the same buffers pass the
+    library the same arguments (its graph replay keys on them)."""
     import torch
 
     lib = load()
@@ -298,11 +300,11 @@ def quantize_group(h_packed, n, w, lam=0.01, ws=None, want_u=True, stream=None, 
     dev = w.device
     _packed(h_packed, n, dev)
     nib, rungs, scales = _outs(torch, rows, n, dev, out)
-    tab = torch.empty(rows, 32, dtype=torch.float32, device=dev)
-    lost = torch.empty(rows, 2, dtype=torch.float32, device=dev)
+    tab = torch.empty(rows, 32, dtype=torch.float32, device=dev) if want_aux else None
+    lost = torch.empty(rows, 2, dtype=torch.float32, device=dev) if want_aux else None
     u = torch.empty(n, n, dtype=torch.float32, device=dev) if want_u else None
-    d = torch.empty(n, dtype=torch.float32, device=dev)
-    hd = torch.empty(n, dtype=torch.float32, device=dev)
+    d = torch.empty(n, dtype=torch.float32, device=dev) if want_aux else None
+    hd = torch.empty(n, dtype=torch.float32, device=dev) if want_aux else None
     if ws is None:
         ws = workspace(lib.gptq_group_workspace_bytes(rows, n), dev)
     _ws(ws, dev)

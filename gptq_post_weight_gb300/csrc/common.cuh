@@ -253,12 +253,26 @@ struct SideStream {
     GQ_CUDA(cudaEventCreateWithFlags(&join, cudaEventDisableTiming));
     return GPTQ_OK;
   }
+  // Drops the handles without releasing them (their context is gone).
+  void forget() { s = nullptr, fork = join = nullptr; }
+  SideStream() = default;
+  SideStream(const SideStream&) = delete;
+  SideStream& operator=(const SideStream&) = delete;
   ~SideStream() {
     if (join) cudaEventDestroy(join);
     if (fork) cudaEventDestroy(fork);
     if (s) cudaStreamDestroy(s);
   }
 };
+
+// The damping schedule after a failed attempt ([fold page] the pivot flag
+// and the host retry): 0 -> 1e-4, else x10.
+inline double next_lambda(double lam) { return lam == 0.0 ? 1e-4 : lam * 10.0; }
+
+// Whether per-launch profiling is recording (launches must then run one by
+// one), and launches replayed from a captured graph, for the launch count.
+bool prof_active();
+void prof_add_launches(long long n);
 
 // TF32 split: hi = x rounded to TF32 (10-bit mantissa, nearest, ties away),
 // lo = (x - hi) rounded to TF32; x - hi is exact in f32.

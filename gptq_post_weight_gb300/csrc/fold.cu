@@ -342,12 +342,12 @@ static gptq_status fold_attempt(const float* hp, const FoldWs& w, const ApplyMap
   return GPTQ_OK;
 }
 
-gptq_status fold_run(const float* hp, int n, double lambda, float* U, float* D, float* hdiag,
-                     double* lambda_used, void* ws, size_t ws_bytes, cudaStream_t s,
-                     const int* perm) {
+// The set-up every attempt shares: diag(H), the caller's copy of it, U
+// zeroed, the tensor maps of the workspace.
+static gptq_status fold_setup(const float* hp, int n, float* U, float* hdiag, void* ws, size_t ws_bytes,
+                              cudaStream_t s, const int* perm, FoldWs& w, ApplyMaps& am) {
   GQ_TRY(init_attrs());
   Carve c(ws, ws_bytes);
-  FoldWs w;
   if (!carve_fold(c, n, w)) return GPTQ_ERR_NOMEM;
   {
     GQ_PROF(K_DIAG, s);
@@ -356,7 +356,6 @@ gptq_status fold_run(const float* hp, int n, double lambda, float* U, float* D, 
   }
   if (hdiag) GQ_CUDA(cudaMemcpyAsync(hdiag, w.hdiag, (size_t)n * 4, cudaMemcpyDeviceToDevice, s));
   GQ_CUDA(cudaMemsetAsync(U, 0, (size_t)n * n * 4, s));
-  ApplyMaps am;
   OperandMaps& maps = am.p;
   GQ_TRY(make_operand_map(&maps.m[0], w.P_hi, w.N, PW));
   GQ_TRY(make_operand_map(&maps.m[1], w.P_lo, w.N, PW));
@@ -366,6 +365,15 @@ gptq_status fold_run(const float* hp, int n, double lambda, float* U, float* D, 
   am.a = maps.c;  // the panel product loads A's vectors in the same boxes
   GQ_TRY(make_operand_map(&am.lhi, w.Lhi, NB, NB, 32));
   GQ_TRY(make_operand_map(&am.llo, w.Llo, NB, NB, 32));
+  return GPTQ_OK;
+}
+
+gptq_status fold_run(const float* hp, int n, double lambda, float* U, float* D, float* hdiag,
+                     double* lambda_used, void* ws, size_t ws_bytes, cudaStream_t s,
+                     const int* perm) {
+  FoldWs w;
+  ApplyMaps am;
+  GQ_TRY(fold_setup(hp, n, U, hdiag, ws, ws_bytes, s, perm, w, am));
   double lam = lambda > 0.0 ? lambda : 0.0;
   for (;;) {
     GQ_TRY(fold_attempt(hp, w, am, lam, U, D, s, perm));
@@ -374,10 +382,20 @@ gptq_status fold_run(const float* hp, int n, double lambda, float* U, float* D, 
     GQ_CUDA(cudaStreamSynchronize(s));
     if (hflag & 2u) return GPTQ_ERR_TIMEOUT;
     if (hflag == 0u) break;
-    lam = (lam == 0.0) ? 1e-4 : lam * 10.0;
+    lam = next_lambda(lam);
     if (lam > 10.0) return GPTQ_ERR_NOT_SPD;
   }
   if (lambda_used) *lambda_used = lam;
+  return GPTQ_OK;
+}
+
+gptq_status fold_enqueue(const float* hp, int n, double lambda, float* U, float* D, float* hdiag,
+                         void* ws, size_t ws_bytes, cudaStream_t s, unsigned** flag_out) {
+  FoldWs w;
+  ApplyMaps am;
+  GQ_TRY(fold_setup(hp, n, U, hdiag, ws, ws_bytes, s, nullptr, w, am));
+  GQ_TRY(fold_attempt(hp, w, am, lambda > 0.0 ? lambda : 0.0, U, D, s, nullptr));
+  *flag_out = w.flag;
   return GPTQ_OK;
 }
 

@@ -58,6 +58,14 @@ WaitCfg wait_cfg() {
 
 }  // namespace gq
 
+namespace gq {
+bool prof_active() {
+  std::lock_guard<std::mutex> lk(g_mu);
+  return g_on;
+}
+void prof_add_launches(long long n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+}  // namespace gq
+
 using namespace gq;
 
 extern "C" {

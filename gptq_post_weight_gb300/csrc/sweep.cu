@@ -722,10 +722,15 @@ gptq_status noalloc_scratch(void** out) {
   return *out != nullptr ? GPTQ_OK : GPTQ_ERR_CUDA;
 }
 
+// side_in: a side stream made by the caller (null: one of the call's own);
+// status_out: null to read the status word back and wait for the stream
+// (the call's result), else only enqueue and hand back the device status
+// word (bit 1: a wait timed out).
 static gptq_status sweep_core(int mode, float* W, int rows, int n, const float* U, const float* hw,
                               const float* tab, const float* lost, uint8_t* nib, uint8_t* rungs,
                               float* scales, void* ws, size_t ws_bytes, cudaStream_t s,
-                              const int* perm, int8_t* codes) {
+                              const int* perm, int8_t* codes, const SideStream* side_in = nullptr,
+                              unsigned** status_out = nullptr) {
   GQ_TRY(sweep_attrs());
   const int G = ws_bytes >= sweep_ws_bytes_g(rows, n, GMAX) ? GMAX : GMIN;
   const int ew = G * SB;
@@ -766,8 +771,9 @@ static gptq_status sweep_core(int mode, float* W, int rows, int n, const float* 
   // beside the group's first block (which leaves SMs and issue slots free):
   // it waits for the previous group's update (the last reader of Ut) and the
   // group's first thin update waits for it.
-  SideStream side;
-  GQ_TRY(side.init());
+  SideStream own;
+  if (side_in == nullptr) GQ_TRY(own.init());
+  const SideStream& side = side_in ? *side_in : own;
   auto prep = [&](int b0, int b1, int kt) -> gptq_status {
     GQ_CUDA(cudaEventRecord(side.fork, s));
     GQ_CUDA(cudaStreamWaitEvent(side.s, side.fork, 0));
@@ -814,6 +820,10 @@ static gptq_status sweep_core(int mode, float* W, int rows, int n, const float* 
                            status, status, K_SWEEP_GEMM, s));
     b0 = bend;
   }
+  if (status_out) {
+    *status_out = status;
+    return GPTQ_OK;
+  }
   unsigned hs = 0;
   GQ_CUDA(cudaMemcpyAsync(&hs, status, sizeof(unsigned), cudaMemcpyDeviceToHost, s));
   GQ_CUDA(cudaStreamSynchronize(s));
@@ -825,6 +835,13 @@ gptq_status sweep_run(float* W, int rows, int n, const float* U, const float* hw
                       size_t ws_bytes, cudaStream_t s) {
   return sweep_core(MODE_Q4, W, rows, n, U, hw, tab, lost, nib, rungs, scales, ws, ws_bytes, s,
                     nullptr, nullptr);
+}
+
+gptq_status sweep_enqueue(float* W, int rows, int n, const float* U, const float* hw, const float* tab,
+                          const float* lost, uint8_t* nib, uint8_t* rungs, float* scales, void* ws,
+                          size_t ws_bytes, cudaStream_t s, const SideStream& side, unsigned** status_out) {
+  return sweep_core(MODE_Q4, W, rows, n, U, hw, tab, lost, nib, rungs, scales, ws, ws_bytes, s,
+                    nullptr, nullptr, &side, status_out);
 }
 
 // The q2tp "placed" sweep: the same blocks and updates with the q2tp rule in
