@@ -296,7 +296,21 @@ size_t gptq_group_workspace_bytes(int rows, int n);
  * Hessian group ([host page] run_quantize_gptq_tiled's device path:
  * gptq_fold_dev then gptq_quantize_q4tp_dev).  W is not modified (a zeroed
  * copy lives in the workspace).  U, D, hdiag may be NULL (then they live in
- * the workspace only); otherwise they receive the fold's outputs.
+ * the workspace only); otherwise they receive the fold's outputs.  The call
+ * returns once its work is done (it reads the pivot flag and the sweep's
+ * status back).
+ *
+ * Repeated calls: the library keeps, per process, the 32 argument sets it
+ * saw last (every pointer and size, lambda, the device context and the wait
+ * limits).  The second call with a set is captured into a CUDA graph -- one
+ * fold attempt at lambda, the ladder, the sweep -- on a stream of the
+ * library's own (one per host thread), ordered after the caller's work on
+ * `stream` by an event, and later calls replay it; the results are the
+ * same bit for bit.  If the attempt finds H not positive definite, the call
+ * continues on `stream` from the next lambda, as the first call would.
+ * Calls made while the caller captures `stream`, or while per-launch
+ * profiling records, never capture.  Buffers must stay valid while any call
+ * that uses them runs.
  */
 gptq_status gptq_quantize_group(const float* H_packed, int n, double lambda, const float* W,
                                 int rows, uint8_t* nibbles, uint8_t* rungs, float* scales,
