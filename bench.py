@@ -509,14 +509,13 @@ def main():
     gpr = n // 32
     ws = _lib.workspace(lib.gptq_group_workspace_bytes(rows, n), dev)
     q2 = args.codec == "q2tp"
-    if q2:
-        quantize = _lib.quantize_group_q2tp
-    else:
-        # Without the debias, the ladder and D are not needed back: they stay
-        # in the workspace, and every step passes the library the same
-        # arguments (its graph replay keys on them).
-        def quantize(*a, **kw):
-            return _lib.quantize_group(*a, want_aux=args.debias, **kw)
+    # Without the debias, the ladder and D are not needed back: they stay in
+    # the workspace, and every step passes the library the same arguments
+    # (its graph replay keys on them).
+    group_call = _lib.quantize_group_q2tp if q2 else _lib.quantize_group
+
+    def quantize(*a, **kw):
+        return group_call(*a, want_aux=args.debias, **kw)
     outs = (torch.empty(rows * n // (4 if q2 else 2), dtype=torch.uint8, device=dev),
             torch.empty(rows * gpr, dtype=torch.uint8, device=dev),
             torch.empty(rows * gpr, dtype=torch.float32, device=dev))

@@ -521,9 +521,10 @@ def q2tp_sweep(w, u, hw, tab, ws=None, out=None, stream=None):
     return codes, rungs, scales
 
 
-def quantize_group_q2tp(h_packed, n, w, lam=0.01, ws=None, want_u=True, stream=None, out=None):
+def quantize_group_q2tp(h_packed, n, w, lam=0.01, ws=None, want_u=True, stream=None, out=None,
+                        want_aux=True):
     """Fold + placed ladder + q2tp sweep.  Returns dict(codes, rungs, scales,
-    tab, lost, u, d, hdiag, lam)."""
+    tab, lost, u, d, hdiag, lam); want_aux as for quantize_group."""
     import torch
 
     lib = load()
@@ -531,11 +532,11 @@ def quantize_group_q2tp(h_packed, n, w, lam=0.01, ws=None, want_u=True, stream=N
     dev = w.device
     _packed(h_packed, n, dev)
     codes, rungs, scales = _outs_q2(torch, rows, n, dev, out)
-    tab = torch.empty(rows, 32, dtype=torch.float32, device=dev)
-    lost = torch.empty(rows, 2, dtype=torch.float32, device=dev)
+    tab = torch.empty(rows, 32, dtype=torch.float32, device=dev) if want_aux else None
+    lost = torch.empty(rows, 2, dtype=torch.float32, device=dev) if want_aux else None
     u = torch.empty(n, n, dtype=torch.float32, device=dev) if want_u else None
-    d = torch.empty(n, dtype=torch.float32, device=dev)
-    hd = torch.empty(n, dtype=torch.float32, device=dev)
+    d = torch.empty(n, dtype=torch.float32, device=dev) if want_aux else None
+    hd = torch.empty(n, dtype=torch.float32, device=dev) if want_aux else None
     if ws is None:
         ws = workspace(lib.gptq_group_workspace_bytes(rows, n), dev)
     _ws(ws, dev)

@@ -853,6 +853,13 @@ gptq_status sweep_q2_run(float* W, int rows, int n, const float* U, const float*
                     nullptr, nullptr);
 }
 
+gptq_status sweep_q2_enqueue(float* W, int rows, int n, const float* U, const float* hw, const float* tab,
+                             uint8_t* codes, uint8_t* rungs, float* scales, void* ws, size_t ws_bytes,
+                             cudaStream_t s, const SideStream& side, unsigned** status_out) {
+  return sweep_core(MODE_Q2, W, rows, n, U, hw, tab, nullptr, codes, rungs, scales, ws, ws_bytes, s,
+                    nullptr, nullptr, &side, status_out);
+}
+
 namespace {
 
 // Static rung of every (row, group): the rung rule with unit weights on the

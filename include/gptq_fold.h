@@ -251,7 +251,8 @@ gptq_status gptq_q2tp_sweep(float* W, int rows, int n, const float* U, const flo
  * q2tp sweep for one Hessian group ([host page] gptq_fold_dev then
  * gptq_quantize_q2tp_dev).  Arguments as gptq_quantize_group, with the
  * 2-bit plane `codes` (rows*n/4 bytes) in place of the nibbles;
- * ws >= gptq_group_workspace_bytes(rows, n).
+ * ws >= gptq_group_workspace_bytes(rows, n).  Repeated calls are replayed
+ * from a captured graph as gptq_quantize_group's are (its own argument sets).
  */
 gptq_status gptq_quantize_group_q2tp(const float* H_packed, int n, double lambda, const float* W,
                                      int rows, uint8_t* codes, uint8_t* rungs, float* scales,

@@ -4,7 +4,8 @@ The library runs the first call with a given set of arguments on the stream,
 captures the second into a graph (one fold attempt at the given damping, the
 ladder, the sweep) and replays it from then on.  Through the C ABI this
 checks that the replays give the stream path's results bit for bit (codes,
-rungs, scales, the ladder, D, diag H, U and the damping used), that each call
+rungs, scales, the ladder, D, diag H, U and the damping used; q4tp and
+q2tp), that each call
 counts the same number of kernel launches, that a first attempt that fails
 (H of rank n/2 at lambda = 0) falls back to the stream path's damping
 retry with the same result.
@@ -35,13 +36,14 @@ def _buffers(lib, n, rows):
     )
 
 
-def _call(lib, hp, n, w, rows, lam, b, stream):
+def _call(lib, hp, n, w, rows, lam, b, stream, q2=False):
     import ctypes
 
     from gptq_post_weight_gb300 import _lib
 
     used = ctypes.c_double(-1.0)
-    code = lib.gptq_quantize_group(
+    fn = lib.gptq_quantize_group_q2tp if q2 else lib.gptq_quantize_group
+    code = fn(
         _lib._ptr(hp), n, float(lam), _lib._ptr(w), rows, _lib._ptr(b["nib"]), _lib._ptr(b["rungs"]),
         _lib._ptr(b["scales"]), _lib._ptr(b["tab"]), _lib._ptr(b["lost"]), _lib._ptr(b["u"]), _lib._ptr(b["d"]),
         _lib._ptr(b["hd"]), ctypes.byref(used), _lib._ptr(b["ws"]), b["ws"].numel(), stream)
@@ -53,8 +55,8 @@ def _snapshot(b):
     return {k: v.clone() for k, v in b.items() if k != "ws"}
 
 
-@pytest.mark.parametrize("n,rows,seed", [(1024, 300, 21), (640, 97, 22)])
-def test_graph_replays_match_stream_path(lib, n, rows, seed):
+@pytest.mark.parametrize("n,rows,seed,q2", [(1024, 300, 21, False), (640, 97, 22, False), (1024, 300, 23, True)])
+def test_graph_replays_match_stream_path(lib, n, rows, seed, q2):
     cfg = synth.Config(f"gr{n}", n, rows, 4 * n, 0.02, 1.5, 3, 3, 0.01, seed)
     hp, w = synth.make_problem(cfg, "cuda")
     b = _buffers(lib, n, rows)
@@ -62,7 +64,7 @@ def test_graph_replays_match_stream_path(lib, n, rows, seed):
     runs = []
     for call in range(4):  # stream path, capture + replay, replay, replay
         l0 = lib.gptq_launch_count()
-        code, used = _call(lib, hp, n, w, rows, cfg.lam, b, st.cuda_stream)
+        code, used = _call(lib, hp, n, w, rows, cfg.lam, b, st.cuda_stream, q2)
         assert code == 0, (call, code)
         runs.append((_snapshot(b), used, lib.gptq_launch_count() - l0))
     ref, used0, launches0 = runs[0]
