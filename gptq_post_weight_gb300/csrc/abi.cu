@@ -39,7 +39,7 @@ gptq_status sweep_run(float* W, int rows, int n, const float* U, const float* hw
                       size_t ws_bytes, cudaStream_t s);
 gptq_status noalloc_scratch(void** out);
 gptq_status fold_enqueue(const float* hp, int n, double lambda, float* U, float* D, float* hdiag,
-                         void* ws, size_t ws_bytes, cudaStream_t s, unsigned** flag_out);
+                         void* ws, size_t ws_bytes, cudaStream_t s, const SideStream& side, unsigned** flag_out);
 gptq_status sweep_enqueue(float* W, int rows, int n, const float* U, const float* hw, const float* tab,
                           const float* lost, uint8_t* nib, uint8_t* rungs, float* scales, void* ws,
                           size_t ws_bytes, cudaStream_t s, const SideStream& side, unsigned** status_out);
@@ -125,7 +125,7 @@ struct ThreadStreams {
   CUcontext ctx = nullptr;
   cudaStream_t st = nullptr;
   cudaEvent_t in = nullptr;
-  SideStream ladder, sweep;
+  SideStream ladder, sweep, fold;
   gptq_status init(CUcontext c) {
     if (ctx == c && st != nullptr) return GPTQ_OK;
     // Handles of an old context went with it.
@@ -133,10 +133,12 @@ struct ThreadStreams {
     in = nullptr;
     ladder.forget();
     sweep.forget();
+    fold.forget();
     GQ_CUDA(cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking));
     GQ_CUDA(cudaEventCreateWithFlags(&in, cudaEventDisableTiming));
     GQ_TRY(ladder.init());
     GQ_TRY(sweep.init());
+    GQ_TRY(fold.init());
     ctx = c;
     return GPTQ_OK;
   }
@@ -417,7 +419,7 @@ gptq_status gptq_quantize_group(const float* H_packed, int n, double lambda, con
 
   auto enqueue = [&](cudaStream_t st, const ThreadStreams& ts, unsigned** flag, unsigned** status) -> gptq_status {
     GQ_TRY(enqueue_ladder(st, ts.ladder));
-    GQ_TRY(fold_enqueue(H_packed, n, lambda, u, d, hd, rest, rest_bytes, st, flag));
+    GQ_TRY(fold_enqueue(H_packed, n, lambda, u, d, hd, rest, rest_bytes, st, ts.fold, flag));
     GQ_CUDA(cudaStreamWaitEvent(st, ts.ladder.join, 0));
     return sweep_enqueue(wz, rows, n, u, hd, tb, ls, nibbles, rungs, scales, rest, rest_bytes, st, ts.sweep,
                          status);
@@ -502,7 +504,7 @@ gptq_status gptq_quantize_group_q2tp(const float* H_packed, int n, double lambda
   };
   auto enqueue = [&](cudaStream_t st, const ThreadStreams& ts, unsigned** flag, unsigned** status) -> gptq_status {
     GQ_TRY(enqueue_place(st, ts.ladder));
-    GQ_TRY(fold_enqueue(H_packed, n, lambda, u, d, hd, rest, rest_bytes, st, flag));
+    GQ_TRY(fold_enqueue(H_packed, n, lambda, u, d, hd, rest, rest_bytes, st, ts.fold, flag));
     GQ_CUDA(cudaStreamWaitEvent(st, ts.ladder.join, 0));
     return sweep_q2_enqueue(wz, rows, n, u, hd, tb, codes, rungs, scales, rest, rest_bytes, st, ts.sweep,
                             status);

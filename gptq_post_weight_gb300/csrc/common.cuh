@@ -216,6 +216,10 @@ gptq_status make_operand_map(CUtensorMap* m, const float* base, long long rows, 
 // of the N x N matrix A (leading dimension lda) must be tile 0 of job 0; its
 // Cholesky inverse goes, as a TF32 hi/lo pair (row-major), to Lhi / Llo and
 // a bad pivot to bit 0 of the status word.
+// on: 0 none; kFusedStep: the launch runs the step after tile 0;
+// kSkipTile0 (single-SM kernel only): the launch skips tile 0, which another
+// launch runs (and the step after it), and leaves that launch one SM.
+constexpr int kFusedStep = 1, kSkipTile0 = 2;
 struct FusedPotrf {
   const float* A;
   long long lda;

@@ -268,7 +268,8 @@ static gptq_status init_attrs() {
 // One factorisation attempt at damping lam: build, interleaved Cholesky +
 // inverse, U.  The pivot flag is left on the device.
 static gptq_status fold_attempt(const float* hp, const FoldWs& w, const ApplyMaps& am,
-                                double lam, float* U, float* D, cudaStream_t s, const int* perm) {
+                                double lam, float* U, float* D, cudaStream_t s, const int* perm,
+                                const SideStream& side) {
   const OperandMaps& maps = am.p;
   const int n = w.n, N = w.N;
   const long long ld = N;
@@ -292,21 +293,23 @@ static gptq_status fold_attempt(const float* hp, const FoldWs& w, const ApplyMap
   //   one trailing update with K = G NB (every panel of the group) for
   //   everything right of / below the group.
   // The diagonal-block step of a group's first block rides in the update
-  // GEMM that finishes it (tile 0 of that GEMM is exactly that block); a
-  // later block's step rides in the strip that finishes it when that strip
-  // is wider than one block (its other tiles then hide part of the step),
-  // else it runs alone right after the strip; the very first runs alone.
+  // GEMM that finishes it (tile 0 of that GEMM is exactly that block).  A
+  // later block's step runs alone on the side stream, right after a
+  // one-tile launch of the strip's tile 0 (that block), while the strip's
+  // other tiles run on the main stream: alone, the step's code stays warm
+  // (fused into a strip it ran a quarter slower from cold instruction
+  // caches).  The very first step runs alone.
   auto apply = [&](int k, int col0, int zero_end) -> gptq_status {
     return apply_tc_run(am, k, k + NB, N, col0, zero_end, w.flag, U, w.dsg, n, s);
   };
-  auto fused = [&](int k) { return FusedPotrf{w.A, ld, k, w.Lhi, w.Llo, 1}; };
-  auto potrf_alone = [&](int k) -> gptq_status {
-    GQ_PROF(K_POTRF, s);
-    k_potrf<<<1, 256, POTRF_SMEM, s>>>(w.A, ld, k, w.Lhi, w.Llo, w.flag);
+  auto fused = [&](int k) { return FusedPotrf{w.A, ld, k, w.Lhi, w.Llo, kFusedStep}; };
+  auto potrf_alone = [&](int k, cudaStream_t st) -> gptq_status {
+    GQ_PROF(K_POTRF, st);
+    k_potrf<<<1, 256, POTRF_SMEM, st>>>(w.A, ld, k, w.Lhi, w.Llo, w.flag);
     GQ_LAUNCHED();
     return GPTQ_OK;
   };
-  GQ_TRY(potrf_alone(0));
+  GQ_TRY(potrf_alone(0, s));
   // maps: 0/1 = P hi/lo, 2/3 = Yp hi/lo (K = PW wide).
   int k = 0;
   while (k < N) {
@@ -320,12 +323,21 @@ static gptq_status fold_attempt(const float* hp, const FoldWs& w, const ApplyMap
         TcJob syrk = tc_strip(kn, kn, 0, kn, 0, kn, N - kn, wdt);
         TcJob inv = tc_rect(kn, 0, 2, 0, 0, kn, kn, wdt);
         syrk.k0 = inv.k0 = i * NB;
-        if (wdt > NB) {
-          GQ_TRY(gemm_tc_sub(maps, syrk, inv, NB, w.flag, w.flag, K_FOLD_STRIP, s, fused(kn)));
-        } else {
-          GQ_TRY(gemm_tc_sub(maps, syrk, inv, NB, w.flag, w.flag, K_FOLD_STRIP, s));
-          GQ_TRY(potrf_alone(kn));
-        }
+        // Side stream: the strip's tile 0 (the diagonal block kn) and the
+        // step on it, alone (its code stays warm in a small kernel); main
+        // stream: the strip's other tiles; joined before the next panel
+        // product.
+        TcJob diag = tc_lower(kn, kn, 0, kn, NB);
+        diag.k0 = i * NB;
+        GQ_CUDA(cudaEventRecord(side.fork, s));
+        GQ_CUDA(cudaStreamWaitEvent(side.s, side.fork, 0));
+        GQ_TRY(gemm_tc_sub(maps, diag, TcJob{}, NB, w.flag, w.flag, K_FOLD_STRIP, side.s));
+        GQ_TRY(potrf_alone(kn, side.s));
+        GQ_CUDA(cudaEventRecord(side.join, side.s));
+        FusedPotrf skip0 = fused(kn);
+        skip0.on = kSkipTile0;
+        GQ_TRY(gemm_tc_sub(maps, syrk, inv, NB, w.flag, w.flag, K_FOLD_STRIP, s, skip0));
+        GQ_CUDA(cudaStreamWaitEvent(s, side.join, 0));
       }
     }
     if (sg < N) {
@@ -374,9 +386,11 @@ gptq_status fold_run(const float* hp, int n, double lambda, float* U, float* D, 
   FoldWs w;
   ApplyMaps am;
   GQ_TRY(fold_setup(hp, n, U, hdiag, ws, ws_bytes, s, perm, w, am));
+  SideStream side;
+  GQ_TRY(side.init());
   double lam = lambda > 0.0 ? lambda : 0.0;
   for (;;) {
-    GQ_TRY(fold_attempt(hp, w, am, lam, U, D, s, perm));
+    GQ_TRY(fold_attempt(hp, w, am, lam, U, D, s, perm, side));
     unsigned hflag = 0;
     GQ_CUDA(cudaMemcpyAsync(&hflag, w.flag, sizeof(unsigned), cudaMemcpyDeviceToHost, s));
     GQ_CUDA(cudaStreamSynchronize(s));
@@ -390,11 +404,11 @@ gptq_status fold_run(const float* hp, int n, double lambda, float* U, float* D, 
 }
 
 gptq_status fold_enqueue(const float* hp, int n, double lambda, float* U, float* D, float* hdiag,
-                         void* ws, size_t ws_bytes, cudaStream_t s, unsigned** flag_out) {
+                         void* ws, size_t ws_bytes, cudaStream_t s, const SideStream& side, unsigned** flag_out) {
   FoldWs w;
   ApplyMaps am;
   GQ_TRY(fold_setup(hp, n, U, hdiag, ws, ws_bytes, s, nullptr, w, am));
-  GQ_TRY(fold_attempt(hp, w, am, lambda > 0.0 ? lambda : 0.0, U, D, s, nullptr));
+  GQ_TRY(fold_attempt(hp, w, am, lambda > 0.0 ? lambda : 0.0, U, D, s, nullptr, side));
   *flag_out = w.flag;
   return GPTQ_OK;
 }

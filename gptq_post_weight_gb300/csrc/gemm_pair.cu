@@ -90,7 +90,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
   const int segc = (kseg > 0 && kseg / PBK < nk) ? kseg / PBK : nk;
   const int nseg = (nk + segc - 1) / segc;
   int t0 = pair, tstride = npairs;
-  if (fp.on) tstride = (pair == 0) ? total : npairs - 1;
+  if (fp.on == kFusedStep) tstride = (pair == 0) ? total : npairs - 1;
   if (threadIdx.x == 0) {
     for (int s = 0; s < PSTAGES; ++s) {
       mbar_init(&full[s], 1);   // the leader's expect_tx; bytes from both CTAs
@@ -296,7 +296,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
     asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(P_TMEM_COLS)
                  : "memory");
   }
-  if (fp.on && pair == 0 && rank == 0 && !abort_sh) {
+  if (fp.on == kFusedStep && pair == 0 && rank == 0 && !abort_sh) {
     // The epilogue leader waited for its reduce-adds; make them visible to
     // plain loads, then run the diagonal-block step on the finished block.
     if (threadIdx.x == 64) asm volatile("fence.proxy.async.global;" ::: "memory");
@@ -332,7 +332,7 @@ gptq_status gemm_pair_sub(const OperandMaps& maps, const TcJob& j0, const TcJob&
   if (total <= 0) return GPTQ_OK;
   int pairs = num_sms() / 2;
   if (pairs > total) pairs = total;
-  if (fp.on && total > 1 && pairs < 2) pairs = 2;  // pair 0 takes tile 0 only
+  if (fp.on == kFusedStep && total > 1 && pairs < 2) pairs = 2;  // pair 0 takes tile 0 only
   if (pairs < 1) pairs = 1;
   GQ_PROF(kind, s);
   k_gemm_pair<<<2 * pairs, P_THREADS, P_SMEM, s>>>(maps.m[0], maps.m[1], maps.m[2], maps.m[3], maps.c, p0,

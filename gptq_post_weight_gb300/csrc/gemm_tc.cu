@@ -109,12 +109,14 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int nseg = (nk + segc - 1) / segc;
   // Tile sequence of this CTA: t0, t0 + tstride, ...
   int t0 = blockIdx.x, tstride = gridDim.x;
-  if (fp.on) {
+  if (fp.on == kFusedStep) {
     if (blockIdx.x == 0) {
       tstride = total;  // tile 0 only
     } else {
       tstride = gridDim.x - 1;
     }
+  } else if (fp.on == kSkipTile0) {
+    t0 = blockIdx.x + 1;  // tile 0 is run elsewhere
   }
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -318,7 +320,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS)
                  : "memory");
   }
-  if (fp.on && blockIdx.x == 0 && !abort_sh) {
+  if (fp.on == kFusedStep && blockIdx.x == 0 && !abort_sh) {
     // The epilogue leader waited for its reduce-adds (wait_group 0); make
     // the tensor core's global writes visible to plain loads, then run the
     // diagonal-block step on the finished tile (shared memory is free: every
@@ -423,7 +425,10 @@ gptq_status gemm_tc_sub(const OperandMaps& maps, const TcJob& j0, const TcJob& j
   if (K % BK != 0 || K <= 0) return GPTQ_ERR_ARG;
   const int total = j0.ntiles + j1.ntiles;
   if (total <= 0) return GPTQ_OK;
-  const int grid = total < num_sms() ? total : num_sms();
+  // kSkipTile0: one tile fewer, and one SM left to the launch that runs it.
+  const int skip = fp.on == kSkipTile0 ? 1 : 0;
+  if (total - skip <= 0) return GPTQ_OK;
+  const int grid = total - skip < num_sms() - skip ? total - skip : num_sms() - skip;
   GQ_PROF(kind, s);
   k_gemm_tc<<<grid, THREADS, SMEM_BYTES, s>>>(maps.m[0], maps.m[1], maps.m[2], maps.m[3], maps.c, j0,
                                               j1, K, kseg, flag, status, fp, wait_cfg());
