@@ -35,43 +35,82 @@ __device__ __forceinline__ bool flagged(const unsigned* flag) {
   return *(volatile const unsigned*)flag != 0u;
 }
 
-// Raw diagonal, dead mask and base = max(mean(diag with dead := 1), 1e-12)
-// in f64 with a fixed summation order (one CTA).  [fold page] diag_get and
-// fold_inner's host lines; [host page] gptq_fold_operator_par.
+// Raw diagonal and dead mask, one channel per thread, and each CTA's part of
+// the f64 sum behind base = max(mean(diag with dead := 1), 1e-12), summed
+// in a fixed order.  [fold page] diag_get and fold_inner's host lines;
+// [host page] gptq_fold_operator_par.
 // With a permutation (act order), position i holds channel perm[i].
-__global__ void __launch_bounds__(1024) k_diag(const float* __restrict__ hp, int n,
-                                               const int* __restrict__ perm,
-                                               float* __restrict__ hdiag,
-                                               double* __restrict__ base_out) {
-  __shared__ double part[1024];
-  double acc = 0.0;
-  for (int i = threadIdx.x; i < n; i += 1024) {
+constexpr int DIAG_T = 256;
+
+__global__ void __launch_bounds__(DIAG_T) k_diag(const float* __restrict__ hp, int n,
+                                                 const int* __restrict__ perm,
+                                                 float* __restrict__ hdiag,
+                                                 double* __restrict__ part) {
+  __shared__ double red[DIAG_T];
+  const int i = blockIdx.x * DIAG_T + threadIdx.x;
+  double v = 0.0;
+  if (i < n) {
     const int ch = perm ? perm[i] : i;
-    float h = hp[poff(ch, n)];
+    const float h = hp[poff(ch, n)];
     hdiag[i] = h;
-    acc += (h > 0.f) ? (double)h : 1.0;
+    v = (h > 0.f) ? (double)h : 1.0;
   }
-  part[threadIdx.x] = acc;
+  red[threadIdx.x] = v;
   __syncthreads();
-  for (int s = 512; s > 0; s >>= 1) {
-    if (threadIdx.x < s) part[threadIdx.x] += part[threadIdx.x + s];
+  for (int s = DIAG_T / 2; s > 0; s >>= 1) {
+    if (threadIdx.x < s) red[threadIdx.x] += red[threadIdx.x + s];
     __syncthreads();
   }
-  if (threadIdx.x == 0) {
-    double mean = part[0] / (double)n;
-    *base_out = mean > 1e-12 ? mean : 1e-12;
+  if (threadIdx.x == 0) part[blockIdx.x] = red[0];
+}
+
+// base from k_diag's parts (fixed order); every CTA of k_dvec forms it.
+__device__ double diag_base(const double* __restrict__ part, int n) {
+  __shared__ double red[DIAG_T];
+  const int nparts = (n + DIAG_T - 1) / DIAG_T;
+  double acc = 0.0;
+  for (int p = threadIdx.x; p < nparts; p += DIAG_T) acc += part[p];
+  red[threadIdx.x] = acc;
+  __syncthreads();
+  for (int s = DIAG_T / 2; s > 0; s >>= 1) {
+    if (threadIdx.x < s) red[threadIdx.x] += red[threadIdx.x + s];
+    __syncthreads();
   }
+  const double mean = red[0] / (double)n;
+  return mean > 1e-12 ? mean : 1e-12;
+}
+
+// U's strict lower block triangle, the entries no panel-product store
+// reaches: U row u holds fold row i = n-1-u of block k = NB floor(i / NB),
+// whose store writes the columns from n - k - NB on.
+__global__ void __launch_bounds__(256) k_zero_lower(float* __restrict__ U, int n, int vec4) {
+  const int u = blockIdx.x;
+  const int i = n - 1 - u;
+  const int end = n - (i / NB) * NB - NB;  // columns [0, end)
+  if (end <= 0) return;
+  float* row = U + (long long)u * n;
+  int c0 = 0;
+  if (vec4) {
+    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+    c0 = end & ~3;
+    for (int c = 4 * threadIdx.x; c < c0; c += 4 * blockDim.x) __stcs(reinterpret_cast<float4*>(row + c), z);
+  }
+  for (int c = c0 + threadIdx.x; c < end; c += blockDim.x) row[c] = 0.f;
 }
 
 // Per attempt: d_k = sqrt(H_kk + damp) and, for a dead channel, the fold
 // page's signed D: -sqrt(1 + damp) (make_u divides by |d|; the builder
 // never uses |d| of a dead row/column).  The working copy keeps the sign,
 // so one load tells the builder both |d| and deadness.
-__global__ void k_dvec(int n, const float* __restrict__ hdiag, const double* __restrict__ base,
-                       double lam, float* __restrict__ Dsigned, float* __restrict__ dsg) {
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+__global__ void __launch_bounds__(DIAG_T) k_dvec(int n, const float* __restrict__ hdiag,
+                                                 const double* __restrict__ part, double lam,
+                                                 float* __restrict__ Dsigned, float* __restrict__ dsg,
+                                                 double* __restrict__ base_out) {
+  const double base = diag_base(part, n);
+  if (blockIdx.x == 0 && threadIdx.x == 0) *base_out = base;
+  const int i = blockIdx.x * DIAG_T + threadIdx.x;
   if (i >= n) return;
-  const double damp = lam * (*base);
+  const double damp = lam * base;
   const float h = hdiag[i];
   const bool dead = !(h > 0.f);
   const float d = dead ? -(float)sqrt(1.0 + damp) : (float)sqrt((double)h + damp);
@@ -227,6 +266,7 @@ struct FoldWs {
   float* hdiag;   // n
   float* dsg;     // n: d with a dead channel's sign (see k_dvec)
   double* base;   // 1
+  double* part;   // ceil(n / DIAG_T): k_diag's per-CTA sums
   unsigned* flag; // 1 (+pad)
 };
 
@@ -244,6 +284,7 @@ static bool carve_fold(Carve& c, int n, FoldWs& w) {
   w.hdiag = c.take<float>((size_t)n);
   w.dsg = c.take<float>((size_t)n);
   w.base = c.take<double>(1);
+  w.part = c.take<double>((size_t)(n + DIAG_T - 1) / DIAG_T);
   w.flag = c.take<unsigned>(4);
   return c.ok;
 }
@@ -276,7 +317,7 @@ static gptq_status fold_attempt(const float* hp, const FoldWs& w, const ApplyMap
   GQ_CUDA(cudaMemsetAsync(w.flag, 0, sizeof(unsigned), s));
   {
     GQ_PROF(K_BUILD, s);
-    k_dvec<<<(n + 255) / 256, 256, 0, s>>>(n, w.hdiag, w.base, lam, D, w.dsg);
+    k_dvec<<<(n + DIAG_T - 1) / DIAG_T, DIAG_T, 0, s>>>(n, w.hdiag, w.part, lam, D, w.dsg, w.base);
     GQ_LAUNCHED();
     k_build<<<N, 256, 0, s>>>(hp, n, N, perm, w.base, lam, w.dsg, w.A, ld, 1);
     GQ_LAUNCHED();
@@ -363,11 +404,16 @@ static gptq_status fold_setup(const float* hp, int n, float* U, float* hdiag, vo
   if (!carve_fold(c, n, w)) return GPTQ_ERR_NOMEM;
   {
     GQ_PROF(K_DIAG, s);
-    k_diag<<<1, 1024, 0, s>>>(hp, n, perm, w.hdiag, w.base);
+    k_diag<<<(n + DIAG_T - 1) / DIAG_T, DIAG_T, 0, s>>>(hp, n, perm, w.hdiag, w.part);
     GQ_LAUNCHED();
   }
   if (hdiag) GQ_CUDA(cudaMemcpyAsync(hdiag, w.hdiag, (size_t)n * 4, cudaMemcpyDeviceToDevice, s));
-  GQ_CUDA(cudaMemsetAsync(U, 0, (size_t)n * n * 4, s));
+  {
+    GQ_PROF(K_DIAG, s);
+    const int vec4 = (n % 4 == 0) && (reinterpret_cast<uintptr_t>(U) % 16 == 0);
+    k_zero_lower<<<n, 256, 0, s>>>(U, n, vec4);
+    GQ_LAUNCHED();
+  }
   OperandMaps& maps = am.p;
   GQ_TRY(make_operand_map(&maps.m[0], w.P_hi, w.N, PW));
   GQ_TRY(make_operand_map(&maps.m[1], w.P_lo, w.N, PW));
@@ -420,13 +466,13 @@ gptq_status build_only(const float* hp, int n, double lambda, float* A, float* D
   if (!carve_fold(c, n, w)) return GPTQ_ERR_NOMEM;
   {
     GQ_PROF(K_DIAG, s);
-    k_diag<<<1, 1024, 0, s>>>(hp, n, nullptr, w.hdiag, w.base);
+    k_diag<<<(n + DIAG_T - 1) / DIAG_T, DIAG_T, 0, s>>>(hp, n, nullptr, w.hdiag, w.part);
     GQ_LAUNCHED();
   }
   // Rows of the caller's n x n matrix, lower triangle only.
   GQ_PROF(K_BUILD, s);
   const double lam = lambda > 0 ? lambda : 0.0;
-  k_dvec<<<(n + 255) / 256, 256, 0, s>>>(n, w.hdiag, w.base, lam, D, w.dsg);
+  k_dvec<<<(n + DIAG_T - 1) / DIAG_T, DIAG_T, 0, s>>>(n, w.hdiag, w.part, lam, D, w.dsg, w.base);
   GQ_LAUNCHED();
   k_build<<<n, 256, 0, s>>>(hp, n, n, nullptr, w.base, lam, w.dsg, A, n, 0);
   GQ_LAUNCHED();

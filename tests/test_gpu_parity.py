@@ -70,6 +70,31 @@ def test_fold_parity(lib, n, sigma):
     assert np.array_equal(np_(hd), hp[np.arange(n) * (2 * n - np.arange(n) + 1) // 2])
 
 
+@pytest.mark.parametrize("n", [200, 333, 640, 1000])
+def test_fold_writes_every_entry_of_u(lib, n):
+    # U prefilled with NaN: the fold writes every entry, zeros below the
+    # diagonal included (n = 333: rows not a whole number of float4s).
+    import ctypes
+
+    from gptq_post_weight_gb300 import _lib
+
+    cfg, hp, _ = small_problem(n, 8, seed=5, sigma=1.5, n_out=2, n_dead=2)
+    hpt = torch.from_numpy(hp).to(DEV)
+    u = torch.full((n * n,), float("nan"), device=DEV)
+    hd = torch.empty(n, device=DEV)
+    ws = _lib.workspace(lib.gptq_fold_workspace_bytes(n), DEV)
+    used = ctypes.c_double(0.0)
+    code = lib.gptq_fold(_lib._ptr(hpt), n, 0.01, _lib._ptr(u), None, _lib._ptr(hd), ctypes.byref(used),
+                         _lib._ptr(ws), ws.numel(), _lib._stream(torch, None))
+    torch.cuda.synchronize()
+    assert code == 0
+    un = np_(u).reshape(n, n)
+    assert np.isfinite(un).all()
+    assert np.all(np.tril(un, -1) == 0)
+    uo = oracle.fold(hp, n, 0.01)[0]
+    assert rel_fro(un, uo) <= 1e-4, rel_fro(un, uo)
+
+
 def test_fold_rank_deficient_retry(lib):
     # Rank n/2, lambda = 0: the first attempt must fail and damping rise.
     from gptq_post_weight_gb300 import _lib
