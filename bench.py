@@ -46,9 +46,9 @@ FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1
 TF32_PER_BF16 = 1.1 / 2.25
 # DRAM bytes (read + write) per launch of the update kinds at the bench
 # workload, from a one-pass ncu launch list of the current kernels (the
-# fold's 33 K = 512 trailing updates: 30.51 GB); drop an entry whenever its
+# fold's 33 K = 512 trailing updates: 30.52 GB); drop an entry whenever its
 # kernels change.
-TRAFFIC = {"fold_gemm": 924.42e6}
+TRAFFIC = {"fold_gemm": 924.73e6}
 
 
 def peaks():
