@@ -6,6 +6,7 @@
 #include <math.h>
 #include <string.h>
 
+#include <memory>
 #include <mutex>
 #include <vector>
 
@@ -119,8 +120,9 @@ GroupGraph* find_graph(const GroupKey& key) {
   return nullptr;
 }
 
-// Per host thread: a stream to capture on and replay on, and the two side
-// streams the capture forks to.  Made on first use in a context.
+// Per host thread and device: a stream to capture on and replay on, and the
+// side streams the capture forks to.  Made on first use in the device's
+// context; made again if that context was replaced (a device reset).
 struct ThreadStreams {
   CUcontext ctx = nullptr;
   cudaStream_t st = nullptr;
@@ -141,6 +143,17 @@ struct ThreadStreams {
     GQ_TRY(fold.init());
     ctx = c;
     return GPTQ_OK;
+  }
+};
+
+// One ThreadStreams per device this thread has used, so that a thread that
+// moves between devices keeps (and at its exit releases) each device's set.
+struct ThreadDeviceStreams {
+  std::vector<std::unique_ptr<ThreadStreams>> dev;
+  ThreadStreams& get(int d) {
+    if (d >= (int)dev.size()) dev.resize((size_t)d + 1);
+    if (!dev[(size_t)d]) dev[(size_t)d].reset(new ThreadStreams());
+    return *dev[(size_t)d];
   }
 };
 
@@ -203,7 +216,9 @@ gptq_status run_graphed(const GroupKey& key, cudaStream_t s, double lambda, doub
   }
   if (use_stream) return stream_path(lambda);
 
-  static thread_local ThreadStreams ts;
+  static thread_local ThreadDeviceStreams tds;
+  if (key.dev < 0) return stream_path(lambda);
+  ThreadStreams& ts = tds.get(key.dev);
   GQ_TRY(ts.init(key.ctx));
   if (capture) {
     // Capture one attempt at lambda and instantiate it.
