@@ -305,7 +305,7 @@ size_t gptq_group_workspace_bytes(int rows, int n);
  * saw last (every pointer and size, lambda, the device context and the wait
  * limits).  The second call with a set is captured into a CUDA graph -- one
  * fold attempt at lambda, the ladder, the sweep -- on a stream of the
- * library's own (one per host thread), ordered after the caller's work on
+ * library's own (one per host thread and device), ordered after the caller's work on
  * `stream` by an event, and later calls replay it; the results are the
  * same bit for bit.  If the attempt finds H not positive definite, the call
  * continues on `stream` from the next lambda, as the first call would.
