@@ -395,8 +395,9 @@ static gptq_status fold_attempt(const float* hp, const FoldWs& w, const ApplyMap
   return GPTQ_OK;
 }
 
-// The set-up every attempt shares: diag(H), the caller's copy of it, U
-// zeroed, the tensor maps of the workspace.
+// The set-up every attempt shares: diag(H), the caller's copy of it, the
+// zeros of U's lower block triangle (the panel products store every other
+// entry), the tensor maps of the workspace.
 static gptq_status fold_setup(const float* hp, int n, float* U, float* hdiag, void* ws, size_t ws_bytes,
                               cudaStream_t s, const int* perm, FoldWs& w, ApplyMaps& am) {
   GQ_TRY(init_attrs());
